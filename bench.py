@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused score -> select -> sparse-verify step.
+
+Workload: Qwen2.5-72B-shaped attention, B=16 sequences of L=32768 context,
+Hq=64, Hkv=8, d=128, gamma=5, budget k=2048 (sinks 16, window 256, m 512),
+4 target + 4 draft SRH heads; seeded synthetic bf16 inputs (see synth/).
+The KV caches (2.15 GB) are far larger than L2, so no flush is needed
+between steps.
+
+One JSON line on rank 0.  ``value`` is the algorithmic HBM GB/s of the step
+(bytes the method must move / device time per step), summed over ranks;
+``ms_per_step`` is the step time.  ``--impl reference`` times the fp64 CPU
+oracle instead, on bounded samples of the same workload.
+
+Multi-GPU: each rank runs an independent replica of the workload on its own
+GPU (the sequences are independent, no collective on the data path); the
+step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse verify step µs & HBM GB/s (score+select+attend), B=16 L=32k k=2048"
+WORKLOAD = "batched32k"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------
+# algorithmic bytes (what the method must move; no implementation scratch)
+# --------------------------------------------------------------------------
+
+def slabs(wl):
+    """Distinct (channel, layer, KV head) slabs read by scoring."""
+    out = set()
+    for (c, l, h) in wl.srh:
+        if c == 0:
+            out.add((0, l, h // (wl.Hq_d // wl.Hkv_d)))
+        else:
+            out.add((1, l, h // (wl.Hq // wl.Hkv)))
+    return sorted(out)
+
+
+def algorithmic_bytes(wl, L=None, B=None):
+    L = wl.L if L is None else L
+    B = wl.B if B is None else B
+    T = wl.gamma + 1
+    k_reads = sum(B * L * (wl.d_d if c == 0 else wl.d) * 2 for (c, _, _) in slabs(wl))
+    imp = B * 2 * L * 4
+    score = k_reads + imp
+    select = imp + B * wl.k * 4
+    per_layer = (2 * B * wl.Hkv * wl.k * wl.d * 2 + 2 * B * wl.Hkv * T * wl.d * 2
+                 + B * T * wl.Hq * wl.d * 2 + B * T * wl.Hq * wl.d * 4)
+    verify = wl.n_layers * per_layer + B * wl.k * 4
+    dense = wl.n_layers * (2 * B * wl.Hkv * L * wl.d * 2 + 2 * B * wl.Hkv * T * wl.d * 2
+                           + B * T * wl.Hq * wl.d * 2 + B * T * wl.Hq * wl.d * 4)
+    return dict(score_kernel=k_reads, score=score, select=select, verify=verify,
+                step=score + select + verify, dense=dense)
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """Max of a per-rank scalar over all ranks (the step time of the job)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        pass
+
+    def result(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# --------------------------------------------------------------------------
+
+def oracle_steps_worker(n_steps: int, min_seconds: float = 0.0):
+    """Times the oracle on one sequence of the workload per step (score,
+    select and verify); keeps stepping until ``n_steps`` steps and at least
+    ``min_seconds`` are done.  Returns (per-step seconds, bytes per step)."""
+    from oracle import dustin_oracle as O
+    from synth import WORKLOADS, generate, to_bits
+    wl = WORKLOADS[WORKLOAD].with_(B=1)
+    x = generate(wl, device="cpu")
+    bits = lambda ts: [to_bits(t) for t in ts]
+    dq, kd, hq, K = bits(x.draft_q), bits(x.Kd), bits(x.hist_q), bits(x.K)
+    Q, V, Kb, Vb = to_bits(x.Q[0]), to_bits(x.V[0]), to_bits(x.Kb[0]), to_bits(x.Vb[0])
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < n_steps or time.perf_counter() - t_all < min_seconds:
+        t0 = time.perf_counter()
+        imp = O.score(dq, kd, hq, K, wl.srh, x.seq_len, wl.Lcap)
+        I, _ = O.select(imp, x.seq_len, wl.k, wl.sinks, wl.window, wl.m)
+        O.verify(Q, K[0], V, Kb, Vb, I, x.seq_len)
+        times.append(time.perf_counter() - t0)
+        if len(times) >= 64:
+            break
+    return times, algorithmic_bytes(wl, B=1)["step"]
+
+
+def run_oracle_subprocess(n_steps: int, min_seconds: float, threads: int):
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.oracle_steps_worker(%r, %r)))" % (ROOT, n_steps, min_seconds))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    times, nbytes = json.loads(r.stdout.strip().splitlines()[-1])
+    return times, nbytes
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "processor\t")):
+                    if "model name" in line.lower():
+                        return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    times, nbytes = run_oracle_subprocess(args.warmup + args.steps, 0.0, threads)
+    times = times[args.warmup:args.warmup + args.steps]
+    t = sum(times) / len(times)
+    value = nbytes / t / 1e9
+    sample = f"1 sequence of {WORKLOAD} per step (score+select+verify), fp64 numpy oracle"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(args),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample, "cpu": cpu_model()},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(args):
+    from synth import WORKLOADS
+    wl = WORKLOADS[WORKLOAD]
+    return {"workload": wl.name, "B": wl.B, "L": wl.L, "Lcap": wl.Lcap, "Hq": wl.Hq,
+            "Hkv": wl.Hkv, "d": wl.d, "gamma": wl.gamma, "k": wl.k, "sinks": wl.sinks,
+            "window": wl.window, "m": wl.m, "srh": "4 target (4 KV heads) + 4 draft (2 KV heads)",
+            "draft": f"Hq_d={wl.Hq_d} Hkv_d={wl.Hkv_d} d_d={wl.d_d}",
+            "l2": "inputs larger than L2 (KV 2.15 GB), no flush",
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def gpu_arm(args, rank, world, dist):
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as ge
+    import sparse_kv_verify_gb300 as dk
+    from synth import WORKLOADS, generate
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ge.build()
+    wl = WORKLOADS[WORKLOAD]
+    if rank:
+        wl = wl.with_(seed_id=wl.seed_id + 1000 * rank)
+    x = generate(wl, device=dev)
+    p = dk.Params(wl.B, wl.Lcap, wl.gamma, wl.sinks, wl.window, wl.m, wl.k)
+    seq = torch.as_tensor(x.seq_len, device=dev)
+    draft = dk.Signal(x.draft_q, x.Kd)
+    target = dk.Signal(x.hist_q, x.K)
+    layer = dk.VerifyLayer(x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0])
+    stream = torch.cuda.current_stream(dev)
+    call = dk.StepCall(p, draft, target, wl.srh, [layer], seq)
+    ab = algorithmic_bytes(wl)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # ---- device-resident timing with per-stage events
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    flags = dk.check(call.ws)
+    if flags:
+        raise RuntimeError(f"device flags {flags:#x} after warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    with sampler:
+        time.sleep(0.3)
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            call(events=ev[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    clocks = sampler.result()
+    barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    stage = {k: [] for k in ("score_kernel", "score_reduce", "select", "verify")}
+    for e in ev:
+        stage["score_kernel"].append(e[0].elapsed_time(e[1]))
+        stage["score_reduce"].append(e[1].elapsed_time(e[2]))
+        stage["select"].append(e[2].elapsed_time(e[3]))
+        stage["verify"].append(e[3].elapsed_time(e[4]))
+    step_ms = max_over_ranks(total_ms / args.steps, dist, dev)
+
+    # ---- dense comparator on the same inputs
+    ws_dense = dk.workspace(p, device=dev)
+    o_dense = torch.empty_like(call.layers[0].o)
+    for _ in range(2):
+        dk.dense_verify_attn(p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], seq, o=o_dense, ws=ws_dense)
+    torch.cuda.synchronize(dev)
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    nd = max(3, min(10, args.steps))
+    d0.record(stream)
+    for _ in range(nd):
+        dk.dense_verify_attn(p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], seq, o=o_dense, ws=ws_dense)
+    d1.record(stream)
+    torch.cuda.synchronize(dev)
+    dense_ms = d0.elapsed_time(d1) / nd
+
+    # ---- end to end through the public API: pinned host inputs -> step -> host O
+    host_in = [t.cpu().pin_memory() for t in (x.Q[0], x.hist_q[0], x.draft_q[0], x.Kb[0], x.Vb[0])]
+    dev_in = [x.Q[0], x.hist_q[0], x.draft_q[0], x.Kb[0], x.Vb[0]]
+    host_out = torch.empty(call.layers[0].o.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        call()
+        host_out.copy_(call.layers[0].o, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
+    flags = dk.check(call.ws)
+    if flags:
+        raise RuntimeError(f"device flags {flags:#x} after timing")
+    if rank != 0:
+        return 0
+
+    peak, peak_kind = peak_hbm()
+    sk_ms = statistics.mean(stage["score_kernel"])
+    achieved = ab["score_kernel"] / (sk_ms * 1e-3) / 1e9
+    stage_us = {k: statistics.mean(v) * 1e3 for k, v in stage.items()}
+    value = world * ab["step"] / (step_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_block(args),
+        "step_us": step_ms * 1e3,
+        "stage_us": stage_us,
+        "stage_gbs": {"score": ab["score"] / (stage_us["score_kernel"] + stage_us["score_reduce"]) / 1e3,
+                      "select": ab["select"] / stage_us["select"] / 1e3,
+                      "verify": ab["verify"] / stage_us["verify"] / 1e3},
+        "algorithmic_bytes_per_step": ab["step"],
+        "verified_tokens_per_s": world * wl.B * (wl.gamma + 1) / (step_ms * 1e-3),
+        "step_frac_of_hbm": (ab["step"] / (step_ms * 1e-3) / 1e9) / peak,
+        "dense": {"us": dense_ms * 1e3, "GB/s": ab["dense"] / (dense_ms * 1e-3) / 1e9,
+                  "frac_of_hbm": ab["dense"] / (dense_ms * 1e-3) / 1e9 / peak},
+        "speedup_vs_dense": {"attention_only": dense_ms / (stage_us["verify"] * 1e-3),
+                             "step": dense_ms / step_ms},
+        "roofline": {"kernel": "score_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": ab["score_kernel"]},
+        "e2e": {"value": world * ab["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        try:
+            times, nb = run_oracle_subprocess(1, args.cpu_seconds, threads)
+            dt, n = sum(times), len(times)
+            line["cpu_baseline"] = {"value": nb * n / dt / 1e9, "unit": "GB/s", "cores": threads,
+                                    "kind": "oracle", "cpu": cpu_model(),
+                                    "sample": f"{n} sequence(s) of {WORKLOAD} through score, "
+                                              f"select and verify ({dt:.1f} s, fp64 numpy)"}
+        except Exception as e:  # the GPU number stands without it
+            line["cpu_baseline"] = {"value": None, "error": str(e)[-300:]}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        return gpu_arm(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,427 @@
+// C-ABI layer: argument validation, launch planning, TMA descriptor encoding
+// and kernel launches for the calls declared in include/dustin.h.  Nothing
+// here allocates device memory; scratch lives in the caller's workspace:
+//   [0, 256)            header: the sticky device error word (int32 at 0)
+//   [256, ...)          per-slab partial importance maps, fp32 [n_slab][B][Lcap]
+//   [..., ...)          logits spill for caches too long for on-chip logits
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace dustin;
+
+namespace {
+
+constexpr size_t kHeader = 256;
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool params_ok(const dustin_params* p) {
+  if (!p) return false;
+  if (p->B < 1 || p->B > 65535) return false;
+  if (p->Lcap < 1 || p->Lcap > DUSTIN_MAX_LCAP) return false;
+  if (p->gamma < 0 || p->k < 1 || p->sinks < 0 || p->window < 0 || p->m < 0) return false;
+  if (int64_t(p->sinks) + p->window > p->k) return false;
+  return true;
+}
+
+bool kv_ok(const dustin_kv& v, int Lcap) {
+  if (!v.ptr || !aligned16(v.ptr)) return false;
+  if (v.d != 64 && v.d != 128) return false;
+  if (v.hkv < 1) return false;
+  if (v.sb <= 0 || v.sh <= 0 || v.sl <= 0) return false;
+  if ((v.sb % 8) || (v.sh % 8) || (v.sl % 8)) return false;
+  if (v.sl < v.d) return false;
+  return true;
+}
+
+bool ws_ok(const void* ws, size_t ws_bytes, size_t need) {
+  return ws && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0 && ws_bytes >= need;
+}
+
+int* err_word(void* ws) { return reinterpret_cast<int*>(ws); }
+
+// ----------------------------------------------------------- TMA encoding
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 4-D map over a cache view: dims (d, Lcap, hkv, B); box 64 x 64 x 1 x 1 with
+// the 128-byte swizzle that the score kernel's ldmatrix addressing expects.
+bool encode_cache_map(CUtensorMap* m, const dustin_kv& v, int Lcap, int B) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {cuuint64_t(v.d), cuuint64_t(Lcap), cuuint64_t(v.hkv), cuuint64_t(B)};
+  cuuint64_t strides[3] = {cuuint64_t(v.sl) * 2, cuuint64_t(v.sh) * 2, cuuint64_t(v.sb) * 2};
+  cuuint32_t box[4] = {64, 64, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v.ptr, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------- score plan
+
+struct ScorePlan {
+  int n_slab = 0;
+  int n_cache = 0;
+  int cache_channel[DUSTIN_MAX_SRH];
+  int cache_layer[DUSTIN_MAX_SRH];
+  ScoreSlab slab[DUSTIN_MAX_SRH];
+  int np_max = 0;
+  int d_max = 0;
+  ScoreLaunch launch{};
+  size_t part_off = 0, part_bytes = 0, spill_off = 0, spill_bytes = 0, total = 0;
+};
+
+const dustin_signal* sig_of(int ch, const dustin_signal* draft, const dustin_signal* target) {
+  return ch == 0 ? draft : target;
+}
+
+bool signal_ok(const dustin_signal* s, int Lcap) {
+  if (!s || s->n_layers < 1 || s->n_layers > 4096 || s->hq < 1 || s->nq < 1 || !s->q || !s->k)
+    return false;
+  (void)Lcap;
+  return true;
+}
+
+int build_score_plan(const dustin_params* p, const dustin_signal* draft,
+                     const dustin_signal* target, const dustin_srh* srh, int32_t n_srh,
+                     ScorePlan* pl) {
+  if (!params_ok(p)) return DUSTIN_EINVAL;
+  if (!srh || n_srh < 1) return DUSTIN_EINVAL;
+  if (n_srh > DUSTIN_MAX_SRH) return DUSTIN_ERANGE;
+  std::memset(pl, 0, sizeof(*pl));
+  for (int i = 0; i < n_srh; ++i) {
+    const dustin_srh& e = srh[i];
+    if (e.channel != 0 && e.channel != 1) return DUSTIN_EINVAL;
+    const dustin_signal* s = sig_of(e.channel, draft, target);
+    if (!signal_ok(s, p->Lcap)) return DUSTIN_EINVAL;
+    if (e.layer < 0 || e.layer >= s->n_layers) return DUSTIN_EINVAL;
+    if (e.q_head < 0 || e.q_head >= s->hq) return DUSTIN_EINVAL;
+    for (int j = 0; j < i; ++j)
+      if (srh[j].channel == e.channel && srh[j].layer == e.layer && srh[j].q_head == e.q_head)
+        return DUSTIN_EINVAL;   // duplicate SRH
+    const dustin_kv& kv = s->k[e.layer];
+    const void* q = s->q[e.layer];
+    if (!kv_ok(kv, p->Lcap) || !q || !aligned16(q)) return DUSTIN_EINVAL;
+    if (s->hq % kv.hkv) return DUSTIN_EINVAL;
+    const int g = e.q_head / (s->hq / kv.hkv);
+    // cache index
+    int ci = -1;
+    for (int c = 0; c < pl->n_cache; ++c)
+      if (pl->cache_channel[c] == e.channel && pl->cache_layer[c] == e.layer) ci = c;
+    if (ci < 0) {
+      ci = pl->n_cache++;
+      pl->cache_channel[ci] = e.channel;
+      pl->cache_layer[ci] = e.layer;
+    }
+    // slab index
+    int sj = -1;
+    for (int t = 0; t < pl->n_slab; ++t)
+      if (pl->slab[t].cache == ci && pl->slab[t].g == g) sj = t;
+    if (sj < 0) {
+      sj = pl->n_slab++;
+      ScoreSlab& S = pl->slab[sj];
+      S.channel = e.channel;
+      S.cache = ci;
+      S.g = g;
+      S.D = kv.d;
+      S.nq = s->nq;
+      S.hq = s->hq;
+      S.nheads = 0;
+      S.npairs = 0;
+      S.q = static_cast<const uint16_t*>(q);
+    }
+    ScoreSlab& S = pl->slab[sj];
+    if (S.npairs + s->nq > DUSTIN_MAX_PAIRS) return DUSTIN_ERANGE;
+    S.heads[S.nheads++] = e.q_head;
+    S.npairs += s->nq;
+  }
+  for (int t = 0; t < pl->n_slab; ++t) {
+    pl->np_max = pl->np_max > pl->slab[t].npairs ? pl->np_max : pl->slab[t].npairs;
+    pl->d_max = pl->d_max > pl->slab[t].D ? pl->d_max : pl->slab[t].D;
+  }
+  pl->launch = score_plan(p->Lcap, p->B, pl->n_slab, pl->np_max, pl->d_max);
+  pl->part_off = kHeader;
+  pl->part_bytes = round256(size_t(pl->n_slab) * p->B * p->Lcap * 4);
+  pl->spill_off = pl->part_off + pl->part_bytes;
+  pl->spill_bytes = pl->launch.smem_logits
+                        ? 0
+                        : round256(size_t(pl->n_slab) * p->B * pl->launch.C * pl->np_max *
+                                   size_t(pl->launch.LS) * 4);
+  pl->total = pl->spill_off + pl->spill_bytes;
+  return DUSTIN_OK;
+}
+
+int launch_score(const dustin_params* p, const dustin_signal* draft, const dustin_signal* target,
+                 const ScorePlan& pl, const int32_t* seq_len, float* importance, void* ws,
+                 cudaStream_t stream, cudaEvent_t mid = nullptr) {
+  static thread_local ScoreArgs a;   // large (tensor maps): keep it off the stack
+  std::memset(&a, 0, sizeof(a));
+  for (int c = 0; c < pl.n_cache; ++c) {
+    const dustin_signal* s = sig_of(pl.cache_channel[c], draft, target);
+    if (!encode_cache_map(&a.map[c], s->k[pl.cache_layer[c]], p->Lcap, p->B)) return DUSTIN_ECUDA;
+  }
+  for (int t = 0; t < pl.n_slab; ++t) a.slab[t] = pl.slab[t];
+  a.B = p->B;
+  a.Lcap = p->Lcap;
+  a.C = pl.launch.C;
+  a.P = pl.launch.P;
+  a.LS = pl.launch.LS;
+  a.n_slab = pl.n_slab;
+  a.np_max = pl.np_max;
+  a.seq_len = seq_len;
+  a.err = err_word(ws);
+  a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.part_off);
+  a.spill = pl.spill_bytes ? reinterpret_cast<float*>(static_cast<char*>(ws) + pl.spill_off) : nullptr;
+  if (score_launch(a, pl.launch, stream) != cudaSuccess) return DUSTIN_ECUDA;
+  if (mid && cudaEventRecord(mid, stream) != cudaSuccess) return DUSTIN_ECUDA;
+  ReduceArgs r{};
+  r.B = p->B;
+  r.Lcap = p->Lcap;
+  r.n_slab = pl.n_slab;
+  for (int t = 0; t < pl.n_slab; ++t) r.channel_of[t] = pl.slab[t].channel;
+  r.part = a.part;
+  r.seq_len = seq_len;
+  r.importance = importance;
+  if (score_reduce_launch(r, stream) != cudaSuccess) return DUSTIN_ECUDA;
+  return DUSTIN_OK;
+}
+
+// ----------------------------------------------------------- verify setup
+
+int check_verify_layer(const dustin_params* p, int32_t hq, const void* q, const dustin_kv& k,
+                       const dustin_kv& v, const void* kb, const void* vb, const float* o) {
+  if (!q || !kb || !vb || !o) return DUSTIN_EINVAL;
+  if (!aligned16(q) || !aligned16(kb) || !aligned16(vb) || !aligned16(o)) return DUSTIN_EINVAL;
+  if (!kv_ok(k, p->Lcap) || !kv_ok(v, p->Lcap)) return DUSTIN_EINVAL;
+  if (k.hkv != v.hkv || k.d != v.d) return DUSTIN_EINVAL;
+  if (hq < 1 || hq % k.hkv) return DUSTIN_EINVAL;
+  const int64_t nq = int64_t(p->gamma + 1) * (hq / k.hkv);
+  if (nq > DUSTIN_MAX_QROWS) return DUSTIN_ERANGE;
+  return DUSTIN_OK;
+}
+
+void fill_layer(VerifyLayerDev& L, const void* q, const dustin_kv& k, const dustin_kv& v,
+                const void* kb, const void* vb, float* o) {
+  L.q = static_cast<const uint16_t*>(q);
+  L.k = static_cast<const uint16_t*>(k.ptr);
+  L.v = static_cast<const uint16_t*>(v.ptr);
+  L.kb = static_cast<const uint16_t*>(kb);
+  L.vb = static_cast<const uint16_t*>(vb);
+  L.o = o;
+  L.ksb = k.sb; L.ksh = k.sh; L.ksl = k.sl;
+  L.vsb = v.sb; L.vsh = v.sh; L.vsl = v.sl;
+}
+
+int run_verify(const dustin_params* p, int32_t hq, int hkv, int D, int n_layers,
+               const VerifyLayerDev* layers, const int32_t* ivf, const int32_t* seq_len, int dense,
+               void* ws, cudaStream_t stream) {
+  static thread_local VerifyArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.B = p->B;
+  a.Lcap = p->Lcap;
+  a.T = p->gamma + 1;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.G = hq / hkv;
+  a.NQ = a.T * a.G;
+  a.k = p->k;
+  a.dense = dense;
+  a.n_layers = n_layers;
+  a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(D)));
+  a.ivf = ivf;
+  a.seq_len = seq_len;
+  a.err = err_word(ws);
+  for (int l = 0; l < n_layers; ++l) a.layer[l] = layers[l];
+  const int nkeys_cap = dense ? p->Lcap : p->k;
+  VerifyLaunch pl = verify_plan(D, a.NQ, nkeys_cap, p->B, hkv, n_layers, dense);
+  const int per = (nkeys_cap + pl.CS - 1) / pl.CS;
+  a.keys_per_split = ((per + 63) / 64) * 64;
+  if (verify_launch(a, pl, stream) != cudaSuccess) return DUSTIN_ECUDA;
+  return DUSTIN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dustin_version(void) { return "dustin-gb300 0.1 (sm_103a)"; }
+
+size_t dustin_workspace_bytes(const dustin_params* p, const dustin_signal* draft,
+                              const dustin_signal* target, const dustin_srh* srh, int32_t n_srh) {
+  if (!params_ok(p)) return 0;
+  if (n_srh == 0) return kHeader;
+  static thread_local ScorePlan pl;
+  if (build_score_plan(p, draft, target, srh, n_srh, &pl) != DUSTIN_OK) return 0;
+  return pl.total;
+}
+
+int dustin_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!ws_ok(ws, ws_bytes, kHeader)) return DUSTIN_EWORKSPACE;
+  return cudaMemsetAsync(ws, 0, kHeader, stream) == cudaSuccess ? DUSTIN_OK : DUSTIN_ECUDA;
+}
+
+int dustin_check(void* ws, cudaStream_t stream, int32_t* flags) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DUSTIN_EWORKSPACE;
+  int32_t h = 0;
+  if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return DUSTIN_ECUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DUSTIN_ECUDA;
+  if (flags) *flags = h;
+  if (h != 0) {
+    if (cudaMemsetAsync(ws, 0, sizeof(h), stream) != cudaSuccess) return DUSTIN_ECUDA;
+    return DUSTIN_EDEVICE;
+  }
+  return DUSTIN_OK;
+}
+
+int dustin_score(const dustin_params* p, const dustin_signal* draft, const dustin_signal* target,
+                 const dustin_srh* srh, int32_t n_srh, const int32_t* seq_len, float* importance,
+                 void* ws, size_t ws_bytes, cudaStream_t stream) {
+  static thread_local ScorePlan pl;
+  const int st = build_score_plan(p, draft, target, srh, n_srh, &pl);
+  if (st != DUSTIN_OK) return st;
+  if (!seq_len || !importance || !aligned16(importance)) return DUSTIN_EINVAL;
+  if (!ws_ok(ws, ws_bytes, pl.total)) return DUSTIN_EWORKSPACE;
+  return launch_score(p, draft, target, pl, seq_len, importance, ws, stream);
+}
+
+int dustin_select(const dustin_params* p, const float* importance, const int32_t* seq_len,
+                  int32_t* i_verify, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!params_ok(p)) return DUSTIN_EINVAL;
+  if (!importance || !seq_len || !i_verify) return DUSTIN_EINVAL;
+  if (!ws_ok(ws, ws_bytes, kHeader)) return DUSTIN_EWORKSPACE;
+  SelectArgs a{};
+  a.B = p->B;
+  a.Lcap = p->Lcap;
+  a.k = p->k;
+  a.sinks = p->sinks;
+  a.window = p->window;
+  a.m = p->m;
+  a.cache_keys = select_cache_keys(p->Lcap);
+  a.imp = importance;
+  a.seq_len = seq_len;
+  a.out = i_verify;
+  a.err = err_word(ws);
+  return select_launch(a, stream) == cudaSuccess ? DUSTIN_OK : DUSTIN_ECUDA;
+}
+
+int dustin_verify_attn(const dustin_params* p, int32_t hq, const void* q, dustin_kv k,
+                       dustin_kv v, const void* kb, const void* vb, const int32_t* i_verify,
+                       const int32_t* seq_len, float* o, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  if (!params_ok(p)) return DUSTIN_EINVAL;
+  const int st = check_verify_layer(p, hq, q, k, v, kb, vb, o);
+  if (st != DUSTIN_OK) return st;
+  if (!i_verify || !seq_len) return DUSTIN_EINVAL;
+  if (!ws_ok(ws, ws_bytes, kHeader)) return DUSTIN_EWORKSPACE;
+  VerifyLayerDev L;
+  fill_layer(L, q, k, v, kb, vb, o);
+  return run_verify(p, hq, k.hkv, k.d, 1, &L, i_verify, seq_len, 0, ws, stream);
+}
+
+int dense_verify_attn(const dustin_params* p, int32_t hq, const void* q, dustin_kv k, dustin_kv v,
+                      const void* kb, const void* vb, const int32_t* seq_len, float* o, void* ws,
+                      size_t ws_bytes, cudaStream_t stream) {
+  if (!params_ok(p)) return DUSTIN_EINVAL;
+  const int st = check_verify_layer(p, hq, q, k, v, kb, vb, o);
+  if (st != DUSTIN_OK) return st;
+  if (!seq_len) return DUSTIN_EINVAL;
+  if (!ws_ok(ws, ws_bytes, kHeader)) return DUSTIN_EWORKSPACE;
+  VerifyLayerDev L;
+  fill_layer(L, q, k, v, kb, vb, o);
+  return run_verify(p, hq, k.hkv, k.d, 1, &L, nullptr, seq_len, 1, ws, stream);
+}
+
+int dustin_kv_append(const dustin_params* p, int32_t n_layers, const dustin_kv* k,
+                     const dustin_kv* v, const void* const* kb, const void* const* vb,
+                     const int32_t* n_accept, int32_t* seq_len, void* ws, size_t ws_bytes,
+                     cudaStream_t stream) {
+  if (!params_ok(p)) return DUSTIN_EINVAL;
+  if (n_layers < 1) return DUSTIN_EINVAL;
+  if (n_layers > DUSTIN_MAX_LAYERS) return DUSTIN_ERANGE;
+  if (!k || !v || !kb || !vb || !n_accept || !seq_len) return DUSTIN_EINVAL;
+  if (!ws_ok(ws, ws_bytes, kHeader)) return DUSTIN_EWORKSPACE;
+  AppendArgs a{};
+  a.B = p->B;
+  a.Lcap = p->Lcap;
+  a.T = p->gamma + 1;
+  a.hkv = k[0].hkv;
+  a.D = k[0].d;
+  a.n_layers = n_layers;
+  a.n_accept = n_accept;
+  a.seq_len = seq_len;
+  a.err = err_word(ws);
+  for (int l = 0; l < n_layers; ++l) {
+    if (!kv_ok(k[l], p->Lcap) || !kv_ok(v[l], p->Lcap)) return DUSTIN_EINVAL;
+    if (k[l].hkv != a.hkv || v[l].hkv != a.hkv || k[l].d != a.D || v[l].d != a.D)
+      return DUSTIN_EINVAL;
+    if (!kb[l] || !vb[l] || !aligned16(kb[l]) || !aligned16(vb[l])) return DUSTIN_EINVAL;
+    AppendLayerDev& L = a.layer[l];
+    L.k = static_cast<uint16_t*>(k[l].ptr);
+    L.v = static_cast<uint16_t*>(v[l].ptr);
+    L.kb = static_cast<const uint16_t*>(kb[l]);
+    L.vb = static_cast<const uint16_t*>(vb[l]);
+    L.ksb = k[l].sb; L.ksh = k[l].sh; L.ksl = k[l].sl;
+    L.vsb = v[l].sb; L.vsh = v[l].sh; L.vsl = v[l].sl;
+  }
+  return append_launch(a, stream) == cudaSuccess ? DUSTIN_OK : DUSTIN_ECUDA;
+}
+
+int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!s) return DUSTIN_EINVAL;
+  const dustin_params* p = &s->p;
+  static thread_local ScorePlan pl;
+  int st = build_score_plan(p, s->draft, s->target, s->srh, s->n_srh, &pl);
+  if (st != DUSTIN_OK) return st;
+  if (!s->seq_len || !s->importance || !aligned16(s->importance) || !s->i_verify)
+    return DUSTIN_EINVAL;
+  if (s->n_layers < 1 || !s->layers) return DUSTIN_EINVAL;
+  if (s->n_layers > DUSTIN_MAX_LAYERS) return DUSTIN_ERANGE;
+  VerifyLayerDev layers[DUSTIN_MAX_LAYERS];
+  const int hkv = s->layers[0].k.hkv, D = s->layers[0].k.d;
+  for (int l = 0; l < s->n_layers; ++l) {
+    const dustin_verify_layer& V = s->layers[l];
+    st = check_verify_layer(p, s->hq, V.q, V.k, V.v, V.kb, V.vb, V.o);
+    if (st != DUSTIN_OK) return st;
+    if (V.k.hkv != hkv || V.k.d != D) return DUSTIN_EINVAL;
+    fill_layer(layers[l], V.q, V.k, V.v, V.kb, V.vb, V.o);
+  }
+  if (!ws_ok(ws, ws_bytes, pl.total)) return DUSTIN_EWORKSPACE;
+  cudaEvent_t* ev = s->stage_events;
+  if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return DUSTIN_ECUDA;
+  st = launch_score(p, s->draft, s->target, pl, s->seq_len, s->importance, ws, stream,
+                    ev ? ev[1] : nullptr);
+  if (st != DUSTIN_OK) return st;
+  if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return DUSTIN_ECUDA;
+  st = dustin_select(p, s->importance, s->seq_len, s->i_verify, ws, ws_bytes, stream);
+  if (st != DUSTIN_OK) return st;
+  if (ev && cudaEventRecord(ev[3], stream) != cudaSuccess) return DUSTIN_ECUDA;
+  st = run_verify(p, s->hq, hkv, D, s->n_layers, layers, s->i_verify, s->seq_len, 0, ws, stream);
+  if (st != DUSTIN_OK) return st;
+  if (ev && cudaEventRecord(ev[4], stream) != cudaSuccess) return DUSTIN_ECUDA;
+  return DUSTIN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,306 @@
+"""Parity of every CUDA stage with the fp64 oracle on seeded inputs.
+
+Small workloads (tiny, qwen72b-layer 8k) are compared element by element;
+the 32k batched workload runs in the launch configuration the benchmark
+times and is checked on samples the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU too
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+import sparse_kv_verify_gb300 as dk  # noqa: E402
+from oracle import dustin_oracle as O  # noqa: E402
+from synth import WORKLOADS, random_importance, to_bits  # noqa: E402
+
+from _cases import (Case, params_of, assert_importance, assert_attention,  # noqa: E402
+                    assert_select_near)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+
+
+# ------------------------------------------------------------------ score
+
+
+@pytest.mark.parametrize("name", ["tiny", "layer8k"])
+def test_score_parity(name):
+    c = Case(WORKLOADS[name])
+    ws = dk.workspace(c.p, c.draft, c.target, c.wl.srh)
+    imp = dk.dustin_score(c.p, c.draft, c.target, c.wl.srh, c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    assert_importance(imp, c.oracle_score(), c.x.seq_len)
+
+
+def test_score_ragged_lengths_multi_batch():
+    wl = WORKLOADS["tiny"].with_(B=3, L=1024)
+    c = Case(wl, seq_len=[1024, 777, 65])
+    imp = dk.dustin_score(c.p, c.draft, c.target, wl.srh, c.seq)
+    assert_importance(imp, c.oracle_score(), c.x.seq_len)
+
+
+def test_score_sixteen_cta_cluster_and_spill():
+    """Long caches: the plan moves to 16-CTA clusters, then to logits in the
+    workspace when they no longer fit on chip."""
+    for L in (40000, 140000):
+        wl = WORKLOADS["tiny"].with_(L=L, n_planted=16)
+        c = Case(wl)
+        imp = dk.dustin_score(c.p, c.draft, c.target, wl.srh, c.seq)
+        assert_importance(imp, c.oracle_score(), c.x.seq_len)
+
+
+def test_score_deterministic():
+    c = Case(WORKLOADS["layer8k"])
+    a = dk.dustin_score(c.p, c.draft, c.target, c.wl.srh, c.seq).clone()
+    b = dk.dustin_score(c.p, c.draft, c.target, c.wl.srh, c.seq)
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ select
+
+
+@pytest.mark.parametrize("ties", [False, True])
+@pytest.mark.parametrize("L,k,s,w,m", [(1024, 128, 4, 32, 32), (8192, 1024, 16, 128, 256),
+                                        (5000, 700, 0, 0, 700), (300, 299, 3, 5, 0),
+                                        (2000, 64, 16, 48, 512), (100, 128, 4, 8, 16)])
+def test_select_bit_exact_on_identical_keys(ties, L, k, s, w, m):
+    B, Lcap = 3, ((L + 64 + 63) // 64) * 64
+    keys = random_importance(L * 7 + k, B, Lcap, ties=ties)
+    seq = np.array([L, max(1, L // 2), max(1, L - 3)], dtype=np.int32)
+    p = dk.Params(B, Lcap, 4, s, w, m, k)
+    I = dk.dustin_select(p, torch.as_tensor(keys, device="cuda"), torch.as_tensor(seq, device="cuda"))
+    ref, _ = O.select(keys.astype(np.float64), seq, k, s, w, m)
+    assert np.array_equal(I.cpu().numpy(), ref)
+
+
+def test_select_long_cache_global_keys():
+    """Caches too long to stage keys on chip select from global memory."""
+    B, L, k = 2, 131072, 4096
+    Lcap = L + 64
+    keys = random_importance(5, B, Lcap, ties=True)
+    seq = np.array([L, 100000], dtype=np.int32)
+    p = dk.Params(B, Lcap, 4, 16, 512, 1024, k)
+    I = dk.dustin_select(p, torch.as_tensor(keys, device="cuda"), torch.as_tensor(seq, device="cuda"))
+    ref, _ = O.select(keys.astype(np.float64), seq, k, 16, 512, 1024)
+    assert np.array_equal(I.cpu().numpy(), ref)
+
+
+def test_select_nan_key_flagged():
+    B, L, Lcap = 1, 512, 576
+    keys = random_importance(9, B, Lcap)
+    keys[0, 0, 100] = np.nan
+    p = dk.Params(B, Lcap, 4, 4, 8, 16, 64)
+    ws = dk.workspace(p)
+    dk.dustin_select(p, torch.as_tensor(keys, device="cuda"),
+                     torch.as_tensor(np.array([L], np.int32), device="cuda"), ws=ws)
+    assert dk.check(ws) & dk.DEV_NAN
+
+
+@pytest.mark.parametrize("name", ["tiny", "layer8k"])
+def test_select_on_own_scores_vs_oracle_scores(name):
+    c = Case(WORKLOADS[name])
+    imp = dk.dustin_score(c.p, c.draft, c.target, c.wl.srh, c.seq)
+    I = dk.dustin_select(c.p, imp, c.seq)
+    wl = c.wl
+    assert_select_near(I, c.oracle_score(), c.x.seq_len, wl.k, wl.sinks, wl.window, wl.m)
+
+
+# ------------------------------------------------------------------ verify
+
+
+@pytest.mark.parametrize("name", ["tiny", "layer8k"])
+def test_verify_parity(name):
+    c = Case(WORKLOADS[name])
+    wl, x = c.wl, c.x
+    I_ref, _ = O.select(c.oracle_score(), x.seq_len, wl.k, wl.sinks, wl.window, wl.m)
+    I = torch.as_tensor(I_ref.astype(np.int32), device="cuda")
+    ws = dk.workspace(c.p)
+    o = dk.dustin_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], I, c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    assert_attention(o, c.oracle_verify(I_ref))
+
+
+@pytest.mark.parametrize("name", ["tiny", "layer8k"])
+def test_dense_parity(name):
+    c = Case(WORKLOADS[name])
+    x = c.x
+    ws = dk.workspace(c.p)
+    o = dk.dense_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    assert_attention(o, c.oracle_dense())
+
+
+@pytest.mark.parametrize("gamma", [0, 1, 2, 8, 15])
+def test_verify_gamma_range(gamma):
+    """gamma from 0 up to 15 (one to eight 16-row m-tiles of queries, G = 8)."""
+    wl = WORKLOADS["layer8k"].with_(gamma=gamma, L=2048, k=256, sinks=4, window=64, m=64,
+                                    n_planted=16)
+    c = Case(wl)
+    x = c.x
+    rng = np.random.default_rng(gamma)
+    I_ref = np.stack([np.sort(rng.choice(wl.L, wl.k, replace=False))]).astype(np.int64)
+    I = torch.as_tensor(I_ref.astype(np.int32), device="cuda")
+    o = dk.dustin_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], I, c.seq)
+    assert_attention(o, c.oracle_verify(I_ref))
+    od = dk.dense_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], c.seq)
+    assert_attention(od, c.oracle_dense())
+
+
+def test_verify_full_budget_matches_dense():
+    """k >= L: I_verify is every context row, so sparse equals dense."""
+    wl = WORKLOADS["tiny"].with_(k=1100)
+    c = Case(wl)
+    x = c.x
+    I = dk.dustin_select(c.p, dk.dustin_score(c.p, c.draft, c.target, wl.srh, c.seq), c.seq)
+    assert I[0, :wl.L].tolist() == list(range(wl.L)) and bool((I[0, wl.L:] == -1).all())
+    o_s = dk.dustin_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], I, c.seq)
+    o_d = dk.dense_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], c.seq)
+    assert torch.allclose(o_s, o_d, atol=2e-6, rtol=0)
+    assert_attention(o_d, c.oracle_dense())
+
+
+def test_verify_padding_and_bad_index():
+    """-1 entries are skipped silently; an index past the context is skipped
+    and flagged."""
+    c = Case(WORKLOADS["tiny"])
+    x, wl = c.x, c.wl
+    rng = np.random.default_rng(3)
+    I_ref = np.sort(rng.choice(wl.L, 100, replace=False))
+    I_pad = np.concatenate([I_ref, -np.ones(wl.k - 100, np.int64)])[None]
+    ws = dk.workspace(c.p)
+    o = dk.dustin_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0],
+                              torch.as_tensor(I_pad.astype(np.int32), device="cuda"), c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    assert_attention(o, c.oracle_verify(I_pad))
+    I_bad = I_pad.copy()
+    I_bad[0, 120] = wl.L + 5
+    o = dk.dustin_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0],
+                              torch.as_tensor(I_bad.astype(np.int32), device="cuda"), c.seq, ws=ws)
+    assert dk.check(ws) & dk.DEV_INDEX
+    assert_attention(o, c.oracle_verify(I_pad))
+
+
+def test_verify_ragged_lengths():
+    wl = WORKLOADS["tiny"].with_(B=3)
+    c = Case(wl, seq_len=[1024, 500, 90])
+    x = c.x
+    imp = dk.dustin_score(c.p, c.draft, c.target, wl.srh, c.seq)
+    I = dk.dustin_select(c.p, imp, c.seq)
+    I_np = I.cpu().numpy().astype(np.int64)
+    o = dk.dustin_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], I, c.seq)
+    assert_attention(o, c.oracle_verify(I_np))
+    od = dk.dense_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], c.seq)
+    assert_attention(od, c.oracle_dense())
+
+
+# ------------------------------------------------------------------ append
+
+
+def test_kv_append_and_overflow_flag():
+    wl = WORKLOADS["tiny"].with_(B=3, n_layers=2)
+    c = Case(wl, seq_len=[1000, 1010, wl.Lcap - 2])
+    x = c.x
+    before = [(to_bits(k).copy(), to_bits(v).copy()) for k, v in zip(x.K, x.V)]
+    n_acc = torch.tensor([3, 0, 4], dtype=torch.int32, device="cuda")
+    ws = dk.workspace(c.p)
+    dk.dustin_kv_append(c.p, x.K, x.V, x.Kb, x.Vb, n_acc, c.seq, ws=ws)
+    flags = dk.check(ws)
+    assert flags & dk.DEV_APPEND    # sequence 2 would pass the capacity
+    assert c.seq.cpu().tolist() == [1003, 1010, wl.Lcap - 2]
+    for l in range(2):
+        K2, V2, sl = O.kv_append(before[l][0][:2], before[l][1][:2], to_bits(x.Kb[l])[:2],
+                                 to_bits(x.Vb[l])[:2], [3, 0], [1000, 1010])
+        assert np.array_equal(to_bits(x.K[l])[:2], K2)
+        assert np.array_equal(to_bits(x.V[l])[:2], V2)
+        assert np.array_equal(to_bits(x.K[l])[2], before[l][0][2])
+
+
+# ------------------------------------------------------------------ fused step
+
+
+@pytest.mark.parametrize("name", ["tiny", "layer8k"])
+def test_verify_step_end_to_end(name):
+    c = Case(WORKLOADS[name])
+    wl, x = c.wl, c.x
+    layer = dk.VerifyLayer(x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0])
+    call = dk.StepCall(c.p, c.draft, c.target, wl.srh, [layer], c.seq)
+    imp, I, outs = call()
+    assert dk.check(call.ws) == 0
+    assert_importance(imp, c.oracle_score(), x.seq_len)
+    # selection is bit-exact on the GPU's own fp32 scores
+    I_ref, _ = O.select(imp.double().cpu().numpy(), x.seq_len, wl.k, wl.sinks, wl.window, wl.m)
+    assert np.array_equal(I.cpu().numpy(), I_ref)
+    assert_attention(outs[0], c.oracle_verify(I_ref))
+    # planted salient positions are recovered (sanity of the recipe)
+    assert np.isin(x.planted, I.cpu().numpy()).mean() > 0.99
+
+
+def test_verify_step_multi_layer_shared_selection():
+    wl = WORKLOADS["tiny"].with_(n_layers=3, srh=((1, 0, 0), (1, 2, 3), (0, 0, 1)))
+    c = Case(wl)
+    x = c.x
+    layers = [dk.VerifyLayer(x.Q[l], x.K[l], x.V[l], x.Kb[l], x.Vb[l]) for l in range(3)]
+    imp, I, outs = dk.dustin_verify_step(c.p, c.draft, c.target, wl.srh, layers, c.seq)
+    assert_importance(imp, c.oracle_score(), x.seq_len)
+    I_np = I.cpu().numpy().astype(np.int64)
+    for l in range(3):
+        assert_attention(outs[l], c.oracle_verify(I_np, layer=l))
+
+
+# ------------------------------------------------------------------ full size
+
+
+@pytest.fixture(scope="module")
+def big():
+    return Case(WORKLOADS["batched32k"])
+
+
+def test_full_size_step_sampled(big):
+    """The 32k batched workload in the launch configuration the benchmark
+    times: importance of two sequences in full, selection of every sequence
+    bit-exact on the GPU's scores, attention of sampled (sequence, KV head)
+    pairs against the oracle."""
+    c = big
+    wl, x = c.wl, c.x
+    layer = dk.VerifyLayer(x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0])
+    call = dk.StepCall(c.p, c.draft, c.target, wl.srh, [layer], c.seq)
+    imp, I, outs = call()
+    assert dk.check(call.ws) == 0
+    imp_np = imp.double().cpu().numpy()
+    for b in (0, wl.B - 1):
+        sub = lambda ts: [to_bits(t[b:b + 1]) for t in ts]
+        ref = O.score(sub(x.draft_q), sub(x.Kd), sub(x.hist_q), sub(x.K), wl.srh,
+                      x.seq_len[b:b + 1], wl.Lcap)
+        assert_importance(imp_np[b:b + 1], ref, x.seq_len[b:b + 1])
+    I_ref, _ = O.select(imp_np, x.seq_len, wl.k, wl.sinks, wl.window, wl.m)
+    I_np = I.cpu().numpy()
+    assert np.array_equal(I_np, I_ref)
+    G = wl.Hq // wl.Hkv
+    o = outs[0]
+    for (b, g) in [(0, 0), (5, 3), (wl.B - 1, wl.Hkv - 1)]:
+        hs = slice(g * G, (g + 1) * G)
+        ref = O.verify(to_bits(x.Q[0][b:b + 1, :, hs]), to_bits(x.K[0][b:b + 1, g:g + 1]),
+                       to_bits(x.V[0][b:b + 1, g:g + 1]), to_bits(x.Kb[0][b:b + 1, g:g + 1]),
+                       to_bits(x.Vb[0][b:b + 1, g:g + 1]), I_ref[b:b + 1].astype(np.int64),
+                       x.seq_len[b:b + 1])
+        assert_attention(o[b:b + 1, :, hs], ref)
+
+
+def test_full_size_dense_sampled(big):
+    c = big
+    wl, x = c.wl, c.x
+    o = dk.dense_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], c.seq)
+    G = wl.Hq // wl.Hkv
+    for (b, g) in [(0, 0), (wl.B - 1, 5)]:
+        hs = slice(g * G, (g + 1) * G)
+        ref = O.dense(to_bits(x.Q[0][b:b + 1, :, hs]), to_bits(x.K[0][b:b + 1, g:g + 1]),
+                      to_bits(x.V[0][b:b + 1, g:g + 1]), to_bits(x.Kb[0][b:b + 1, g:g + 1]),
+                      to_bits(x.Vb[0][b:b + 1, g:g + 1]), x.seq_len[b:b + 1])
+        assert_attention(o[b:b + 1, :, hs], ref)
