@@ -92,54 +92,94 @@ def peak_hbm():
 # --------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples SM clock and clock-event reasons during the timed region.
+
+    Reads NVML through ctypes (read-only queries) from a background thread
+    every ~2 ms; falls back to ``nvidia-smi -lms`` when NVML is unavailable.
+    """
+    # nvmlClocksEventReasons bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, index):
         self.index = index
+        self.samples = []
+        self.stop = False
+        self.thread = None
+        self.nvml = None
         self.proc = None
 
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            return None
+        return lib, h
+
+    def _loop(self):
+        import ctypes
+        lib, h = self.nvml
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop:
+            ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0          # NVML_CLOCK_SM
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            lib.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs))
+            if ok:
+                self.samples.append((clk.value, mx.value, rs.value))
+            time.sleep(0.002)
+
     def __enter__(self):
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.nvml = self._nvml_open()
         except Exception:
-            self.proc = None
+            self.nvml = None
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+        else:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.index}",
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception:
+                self.proc = None
         return self
 
     def __exit__(self, *a):
-        pass
+        self.stop = True
+        if self.thread is not None:
+            self.thread.join(timeout=2)
 
     def result(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except Exception:
-            self.proc.kill()
-            out = ""
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
+        if self.proc is not None:
+            self.proc.terminate()
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                out = ""
+            for line in out.strip().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    self.samples.append((float(f[0]), float(f[1]), int(f[2], 16)))
+                except (ValueError, IndexError):
+                    pass
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = set()
+        for _, _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(c for c, _, _ in self.samples),
+                "sm_max_mhz": max(m for _, m, _ in self.samples),
+                "reasons": sorted(reasons), "samples": len(self.samples),
+                "source": "nvml" if self.nvml is not None else "nvidia-smi"}
 
 
 # --------------------------------------------------------------------------
@@ -248,6 +288,8 @@ def gpu_arm(args, rank, world, dist):
     dev = torch.device("cuda", local)
     ge.build()
     wl = WORKLOADS[WORKLOAD]
+    if args.batch:
+        wl = wl.with_(B=args.batch)
     if rank:
         wl = wl.with_(seed_id=wl.seed_id + 1000 * rank)
     x = generate(wl, device=dev)
@@ -276,7 +318,7 @@ def gpu_arm(args, rank, world, dist):
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(local)
     with sampler:
-        time.sleep(0.3)
+        time.sleep(0.01)
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -294,6 +336,14 @@ def gpu_arm(args, rank, world, dist):
         stage["select"].append(e[2].elapsed_time(e[3]))
         stage["verify"].append(e[3].elapsed_time(e[4]))
     step_ms = max_over_ranks(total_ms / args.steps, dist, dev)
+
+    if args.profile:
+        # profiling run (ncu): warm-up and timed steps only
+        dk.check(call.ws)
+        if rank == 0:
+            print(json.dumps({"profile_run": True, "workload": wl.name, "B": wl.B,
+                              "step_us": step_ms * 1e3}), flush=True)
+        return 0
 
     # ---- dense comparator on the same inputs
     ws_dense = dk.workspace(p, device=dev)
@@ -396,6 +446,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the batch size (profiling of smaller cases)")
+    ap.add_argument("--profile", action="store_true",
+                    help="run warm-up and timed steps only (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

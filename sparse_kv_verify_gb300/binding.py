@@ -352,6 +352,9 @@ class StepCall:
         after select and after verify."""
         ev = events if events is not None else self.events
         if ev is not None:
+            for e in ev:
+                if not e.cuda_event:      # torch creates the CUDA event on first record
+                    e.record(stream if stream is not None else torch.cuda.current_stream())
             arr = (c_void_p * 5)(*[e.cuda_event for e in ev])
             self.step.stage_events = ctypes.cast(arr, POINTER(c_void_p))
         else:
