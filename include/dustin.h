@@ -211,6 +211,35 @@ int dustin_kv_append(const dustin_params* p, int32_t n_layers, const dustin_kv* 
 /* score -> select -> sparse verify of every layer, on one stream. */
 int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Bytes of the library-owned scratch array used by dustin_score_noalloc. */
+#define DUSTIN_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* dustin_score without a caller workspace.  The pages have no counterpart to
+ * this call: it exists for callers that cannot call cudaMalloc (or any other
+ * allocator) at the point where they score -- for example code running inside
+ * an allocator-free runtime, a host callback, or a component that must not
+ * touch the process's memory pools.  Results are the same as dustin_score's.
+ *
+ * Scratch lives in one file-scope device array of DUSTIN_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) inside the library; every GPU that loads the library holds it
+ * until the process exits.  The call allocates nothing: no cudaMalloc,
+ * cudaFree or allocating library routine.  The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture.
+ *
+ * Limits: the per-KV-head partial maps (number of distinct SRH KV heads x B x
+ * Lcap x 4 bytes, plus a 256-byte header) must fit in the array, and the
+ * logits must fit on chip (no spill); otherwise DUSTIN_ERANGE is returned and
+ * nothing is launched.  The device error word lives in the array too; it is
+ * cleared at the start of every call and cannot be read by the caller.
+ *
+ * All calls share the one array and it keeps the last call's contents: calls
+ * that overlap on the GPU (different streams, or different host threads
+ * without ordering) race on it and must be serialised by the caller. */
+int dustin_score_noalloc(const dustin_params* p, const dustin_signal* draft,
+                         const dustin_signal* target, const dustin_srh* srh, int32_t n_srh,
+                         const int32_t* seq_len, float* importance, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

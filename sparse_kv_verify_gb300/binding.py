@@ -106,6 +106,9 @@ def lib():
                                        POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_void_p,
                                        c_void_p, c_size_t, c_void_p]
         L.dustin_verify_step.argtypes = [POINTER(CStep), c_void_p, c_size_t, c_void_p]
+        L.dustin_score_noalloc.argtypes = [POINTER(CParams), POINTER(CSignal), POINTER(CSignal),
+                                           POINTER(CSRH), c_int32, c_void_p, c_void_p, c_void_p]
+        L.dustin_score_noalloc.restype = ctypes.c_int
         for f in EXPORTS[1:]:
             if f != "dustin_workspace_bytes":
                 getattr(L, f).restype = ctypes.c_int
@@ -245,6 +248,24 @@ def dustin_score(p: Params, draft: Signal, target: Signal, srh, seq_len: torch.T
                             _ptr(seq_len, torch.int32), _ptr(importance, torch.float32),
                             ws.ptr, ws.nbytes, _stream(stream))
     _check("dustin_score", st)
+    return importance
+
+
+def dustin_score_noalloc(p: Params, draft: Signal, target: Signal, srh, seq_len: torch.Tensor,
+                         importance: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """dustin_score with the library's own static scratch (no workspace).
+
+    For callers that cannot allocate device memory when they score; the
+    library keeps one 16 MiB scratch array per GPU, shared by all calls (calls
+    that overlap on the GPU race on it)."""
+    if importance is None:
+        raise ValueError("pass a preallocated importance tensor [B][2][Lcap] fp32")
+    d, t = draft.c(), target.c()
+    arr = _srh_array(srh)
+    st = lib().dustin_score_noalloc(ctypes.byref(p.c()), ctypes.byref(d), ctypes.byref(t), arr,
+                                    len(srh), _ptr(seq_len, torch.int32),
+                                    _ptr(importance, torch.float32), _stream(stream))
+    _check("dustin_score_noalloc", st)
     return importance
 
 

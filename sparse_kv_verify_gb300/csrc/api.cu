@@ -425,3 +425,50 @@ int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStre
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Scoring without a caller workspace (for callers that cannot allocate).
+// The scratch is this file-scope device array; host code must not use its
+// name as a device address, so the address is looked up per device.
+// ---------------------------------------------------------------------------
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DUSTIN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_noalloc_scratch on the current device (looked up once
+// per device, with that device current).
+int noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DUSTIN_ECUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DUSTIN_ECUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return DUSTIN_OK;
+}
+
+}  // namespace
+
+extern "C" int dustin_score_noalloc(const dustin_params* p, const dustin_signal* draft,
+                                    const dustin_signal* target, const dustin_srh* srh,
+                                    int32_t n_srh, const int32_t* seq_len, float* importance,
+                                    cudaStream_t stream) {
+  static thread_local ScorePlan pl;
+  const int st = build_score_plan(p, draft, target, srh, n_srh, &pl);
+  if (st != DUSTIN_OK) return st;
+  if (!seq_len || !importance || !aligned16(importance)) return DUSTIN_EINVAL;
+  if (pl.spill_bytes != 0 || pl.total > DUSTIN_NOALLOC_SCRATCH_BYTES) return DUSTIN_ERANGE;
+  void* ws = nullptr;
+  const int s2 = noalloc_scratch(&ws);
+  if (s2 != DUSTIN_OK) return s2;
+  if (cudaMemsetAsync(ws, 0, kHeader, stream) != cudaSuccess) return DUSTIN_ECUDA;
+  return launch_score(p, draft, target, pl, seq_len, importance, ws, stream);
+}
