@@ -346,7 +346,7 @@ def gpu_arm(args, rank, world, dist):
         return 0
 
     # ---- dense comparator on the same inputs
-    ws_dense = dk.workspace(p, device=dev)
+    ws_dense = dk.workspace(p, verify=(wl.Hq, wl.Hkv, wl.d, 1), device=dev)
     o_dense = torch.empty_like(call.layers[0].o)
     for _ in range(2):
         dk.dense_verify_attn(p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], seq, o=o_dense, ws=ws_dense)

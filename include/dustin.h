@@ -144,15 +144,20 @@ typedef struct {
 /* Library version string (static storage). */
 const char* dustin_version(void);
 
-/* Bytes of workspace needed by every call made with these arguments (score
- * sizes its per-KV-head partial maps from the SRH list).  Returns 0 if the
- * arguments are invalid.  Pass draft/target/srh = NULL, n_srh = 0 for calls
- * that do not score. */
+/* Bytes of workspace needed by every call made with these arguments: score
+ * sizes its per-KV-head partial maps from the SRH list, verification its
+ * per-unit partials from (hq, hkv, d, n_layers).  Pass n_srh = 0 (and NULL
+ * pointers) when nothing is scored and n_layers = 0 when nothing is verified.
+ * Returns 0 if the arguments are invalid.  Every workspace holds at least
+ * 256 + 65536 bytes (error word and the verify combine counters). */
 size_t dustin_workspace_bytes(const dustin_params* p, const dustin_signal* draft,
                               const dustin_signal* target, const dustin_srh* srh,
-                              int32_t n_srh);
+                              int32_t n_srh, int32_t hq, int32_t hkv, int32_t d,
+                              int32_t n_layers);
 
-/* Clears the error word of a workspace (asynchronously, on stream). */
+/* Clears the error word and the verify counters of a workspace
+ * (asynchronously, on stream).  Call it once before first use, and again
+ * after dustin_check has reported DUSTIN_DEV_TIMEOUT. */
 int dustin_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronises the stream, returns the error word in *flags (if non-NULL),

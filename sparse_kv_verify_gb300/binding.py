@@ -88,7 +88,8 @@ def lib():
         L.dustin_version.restype = c_char_p
         L.dustin_workspace_bytes.restype = c_size_t
         L.dustin_workspace_bytes.argtypes = [POINTER(CParams), POINTER(CSignal), POINTER(CSignal),
-                                             POINTER(CSRH), c_int32]
+                                             POINTER(CSRH), c_int32, c_int32, c_int32, c_int32,
+                                             c_int32]
         L.dustin_workspace_init.argtypes = [c_void_p, c_size_t, c_void_p]
         L.dustin_check.argtypes = [c_void_p, c_void_p, POINTER(c_int32)]
         L.dustin_score.argtypes = [POINTER(CParams), POINTER(CSignal), POINTER(CSignal),
@@ -203,23 +204,32 @@ class Workspace:
 
 
 def workspace_bytes(p: Params, draft: Optional[Signal] = None, target: Optional[Signal] = None,
-                    srh=()) -> int:
+                    srh=(), verify=None) -> int:
+    """Workspace bytes for scoring with ``srh`` and/or verifying with
+    ``verify = (hq, hkv, d, n_layers)``."""
     cp = p.c()
+    hq, hkv, d, nl = verify if verify is not None else (0, 0, 0, 0)
     if srh:
-        d = draft.c() if draft is not None else None
-        t = target.c() if target is not None else None
+        dc = draft.c() if draft is not None else None
+        tc = target.c() if target is not None else None
         arr = _srh_array(srh)
-        n = lib().dustin_workspace_bytes(ctypes.byref(cp), ctypes.byref(d) if d else None,
-                                         ctypes.byref(t) if t else None, arr, len(srh))
+        n = lib().dustin_workspace_bytes(ctypes.byref(cp), ctypes.byref(dc) if dc else None,
+                                         ctypes.byref(tc) if tc else None, arr, len(srh),
+                                         hq, hkv, d, nl)
     else:
-        n = lib().dustin_workspace_bytes(ctypes.byref(cp), None, None, None, 0)
+        n = lib().dustin_workspace_bytes(ctypes.byref(cp), None, None, None, 0, hq, hkv, d, nl)
     if n == 0:
         raise DustinError("dustin_workspace_bytes", -1)
     return int(n)
 
 
-def workspace(p: Params, draft=None, target=None, srh=(), device=None, stream=None) -> Workspace:
-    return Workspace(workspace_bytes(p, draft, target, srh), device=device, stream=stream)
+def workspace(p: Params, draft=None, target=None, srh=(), verify=None, device=None,
+              stream=None) -> Workspace:
+    return Workspace(workspace_bytes(p, draft, target, srh, verify), device=device, stream=stream)
+
+
+def _verify_shape(q, k, n_layers=1):
+    return (q.shape[2], k.shape[1], k.shape[3], n_layers)
 
 
 def check(ws: Workspace, stream=None) -> int:
@@ -293,7 +303,7 @@ def dustin_verify_attn(p: Params, q, k, v, kb, vb, i_verify, seq_len, o=None, ws
                        stream=None) -> torch.Tensor:
     o = _out(o, q)
     if ws is None:
-        ws = workspace(p, device=q.device, stream=stream)
+        ws = workspace(p, verify=_verify_shape(q, k), device=q.device, stream=stream)
     st = lib().dustin_verify_attn(ctypes.byref(p.c()), q.shape[2], _ptr(q, torch.bfloat16),
                                   kv_view(k), kv_view(v), _ptr(kb, torch.bfloat16),
                                   _ptr(vb, torch.bfloat16), _ptr(i_verify, torch.int32),
@@ -307,7 +317,7 @@ def dense_verify_attn(p: Params, q, k, v, kb, vb, seq_len, o=None, ws=None,
                       stream=None) -> torch.Tensor:
     o = _out(o, q)
     if ws is None:
-        ws = workspace(p, device=q.device, stream=stream)
+        ws = workspace(p, verify=_verify_shape(q, k), device=q.device, stream=stream)
     st = lib().dense_verify_attn(ctypes.byref(p.c()), q.shape[2], _ptr(q, torch.bfloat16),
                                  kv_view(k), kv_view(v), _ptr(kb, torch.bfloat16),
                                  _ptr(vb, torch.bfloat16), _ptr(seq_len, torch.int32),
@@ -354,7 +364,9 @@ class StepCall:
         for Lr in layers:
             Lr.o = _out(Lr.o, Lr.q)
         self.layers = list(layers)
-        self.ws = ws if ws is not None else workspace(p, draft, target, srh, device=dev, stream=stream)
+        self.ws = ws if ws is not None else workspace(
+            p, draft, target, srh, verify=_verify_shape(layers[0].q, layers[0].k, len(layers)),
+            device=dev, stream=stream)
         self._d, self._t = draft.c(), target.c()
         self._srh = _srh_array(srh)
         self._larr = (CVerifyLayer * len(layers))(*[

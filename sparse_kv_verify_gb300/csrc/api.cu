@@ -1,9 +1,13 @@
 // C-ABI layer: argument validation, launch planning, TMA descriptor encoding
 // and kernel launches for the calls declared in include/dustin.h.  Nothing
 // here allocates device memory; scratch lives in the caller's workspace:
-//   [0, 256)            header: the sticky device error word (int32 at 0)
-//   [256, ...)          per-slab partial importance maps, fp32 [n_slab][B][Lcap]
-//   [..., ...)          logits spill for caches too long for on-chip logits
+//   [0, 256)                 header: the sticky device error word (int32 at 0)
+//   [256, 256 + 64 KiB)      per-unit segment counters of the verify combine
+//                            (zero between calls; kept zero by the kernels)
+//   [kScratch, ...)          scratch shared by the stages of one call:
+//                            score: per-slab partial maps fp32 [n_slab][B][Lcap]
+//                                   (+ logits spill for very long caches)
+//                            verify: segment partials [units][max_seg][NQ][d+2]
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -18,6 +22,20 @@ using namespace dustin;
 namespace {
 
 constexpr size_t kHeader = 256;
+constexpr size_t kCounterBytes = 65536;             // verify units <= 16384
+constexpr size_t kScratch = kHeader + kCounterBytes;
+
+int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -106,7 +124,7 @@ bool signal_ok(const dustin_signal* s, int Lcap) {
 
 int build_score_plan(const dustin_params* p, const dustin_signal* draft,
                      const dustin_signal* target, const dustin_srh* srh, int32_t n_srh,
-                     ScorePlan* pl) {
+                     ScorePlan* pl, size_t scratch_off = kScratch) {
   if (!params_ok(p)) return DUSTIN_EINVAL;
   if (!srh || n_srh < 1) return DUSTIN_EINVAL;
   if (n_srh > DUSTIN_MAX_SRH) return DUSTIN_ERANGE;
@@ -162,7 +180,7 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
     pl->d_max = pl->d_max > pl->slab[t].D ? pl->d_max : pl->slab[t].D;
   }
   pl->launch = score_plan(p->Lcap, p->B, pl->n_slab, pl->np_max, pl->d_max);
-  pl->part_off = kHeader;
+  pl->part_off = scratch_off;
   pl->part_bytes = round256(size_t(pl->n_slab) * p->B * p->Lcap * 4);
   pl->spill_off = pl->part_off + pl->part_bytes;
   pl->spill_bytes = pl->launch.smem_logits
@@ -234,9 +252,34 @@ void fill_layer(VerifyLayerDev& L, const void* q, const dustin_kv& k, const dust
   L.vsb = v.sb; L.vsh = v.sh; L.vsl = v.sl;
 }
 
+struct VerifyShape {
+  int hq = 0, hkv = 0, d = 0, n_layers = 0;
+};
+
+VerifyLaunch plan_verify(const dustin_params* p, const VerifyShape& v, int dense) {
+  const int NQ = (p->gamma + 1) * (v.hq / v.hkv);
+  return verify_plan(v.d, NQ, dense ? p->Lcap : p->k, p->B, v.hkv, v.n_layers, dense, num_sms());
+}
+
+// Bytes of workspace the verification of this shape needs (0 if invalid).
+size_t verify_ws_bytes(const dustin_params* p, const VerifyShape& v, int dense) {
+  if (v.n_layers <= 0) return kScratch;
+  const VerifyLaunch pl = plan_verify(p, v, dense);
+  if (pl.units * 4 > (long long)kCounterBytes) return 0;
+  return kScratch + round256(verify_scratch_bytes(pl));
+}
+
 int run_verify(const dustin_params* p, int32_t hq, int hkv, int D, int n_layers,
                const VerifyLayerDev* layers, const int32_t* ivf, const int32_t* seq_len, int dense,
-               void* ws, cudaStream_t stream) {
+               void* ws, size_t ws_bytes, cudaStream_t stream) {
+  VerifyShape vs;
+  vs.hq = hq;
+  vs.hkv = hkv;
+  vs.d = D;
+  vs.n_layers = n_layers;
+  const VerifyLaunch pl = plan_verify(p, vs, dense);
+  if (pl.units * 4 > (long long)kCounterBytes) return DUSTIN_ERANGE;
+  if (!ws_ok(ws, ws_bytes, kScratch + verify_scratch_bytes(pl))) return DUSTIN_EWORKSPACE;
   static thread_local VerifyArgs a;
   std::memset(&a, 0, sizeof(a));
   a.B = p->B;
@@ -249,15 +292,18 @@ int run_verify(const dustin_params* p, int32_t hq, int hkv, int D, int n_layers,
   a.k = p->k;
   a.dense = dense;
   a.n_layers = n_layers;
+  a.ctx_tiles = pl.ctx_tiles;
+  a.tiles_u = pl.tiles_u;
+  a.total = pl.total;
+  a.max_seg = pl.max_seg;
+  a.slot_floats = pl.slot_floats;
   a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(D)));
   a.ivf = ivf;
   a.seq_len = seq_len;
   a.err = err_word(ws);
+  a.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + kHeader);
+  a.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kScratch);
   for (int l = 0; l < n_layers; ++l) a.layer[l] = layers[l];
-  const int nkeys_cap = dense ? p->Lcap : p->k;
-  VerifyLaunch pl = verify_plan(D, a.NQ, nkeys_cap, p->B, hkv, n_layers, dense);
-  const int per = (nkeys_cap + pl.CS - 1) / pl.CS;
-  a.keys_per_split = ((per + 63) / 64) * 64;
   if (verify_launch(a, pl, stream) != cudaSuccess) return DUSTIN_ECUDA;
   return DUSTIN_OK;
 }
@@ -269,17 +315,36 @@ extern "C" {
 const char* dustin_version(void) { return "dustin-gb300 0.1 (sm_103a)"; }
 
 size_t dustin_workspace_bytes(const dustin_params* p, const dustin_signal* draft,
-                              const dustin_signal* target, const dustin_srh* srh, int32_t n_srh) {
+                              const dustin_signal* target, const dustin_srh* srh, int32_t n_srh,
+                              int32_t hq, int32_t hkv, int32_t d, int32_t n_layers) {
   if (!params_ok(p)) return 0;
-  if (n_srh == 0) return kHeader;
-  static thread_local ScorePlan pl;
-  if (build_score_plan(p, draft, target, srh, n_srh, &pl) != DUSTIN_OK) return 0;
-  return pl.total;
+  size_t need = kScratch;
+  if (n_srh != 0) {
+    static thread_local ScorePlan pl;
+    if (build_score_plan(p, draft, target, srh, n_srh, &pl) != DUSTIN_OK) return 0;
+    need = pl.total > need ? pl.total : need;
+  }
+  if (n_layers != 0) {
+    if (n_layers < 0 || n_layers > DUSTIN_MAX_LAYERS || hkv < 1 || hq < 1 || hq % hkv ||
+        (d != 64 && d != 128) || int64_t(p->gamma + 1) * (hq / hkv) > DUSTIN_MAX_QROWS)
+      return 0;
+    VerifyShape vs;
+    vs.hq = hq;
+    vs.hkv = hkv;
+    vs.d = d;
+    vs.n_layers = n_layers;
+    for (int dense = 0; dense < 2; ++dense) {
+      const size_t v = verify_ws_bytes(p, vs, dense);
+      if (v == 0) return 0;
+      need = v > need ? v : need;
+    }
+  }
+  return need;
 }
 
 int dustin_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
-  if (!ws_ok(ws, ws_bytes, kHeader)) return DUSTIN_EWORKSPACE;
-  return cudaMemsetAsync(ws, 0, kHeader, stream) == cudaSuccess ? DUSTIN_OK : DUSTIN_ECUDA;
+  if (!ws_ok(ws, ws_bytes, kScratch)) return DUSTIN_EWORKSPACE;
+  return cudaMemsetAsync(ws, 0, kScratch, stream) == cudaSuccess ? DUSTIN_OK : DUSTIN_ECUDA;
 }
 
 int dustin_check(void* ws, cudaStream_t stream, int32_t* flags) {
@@ -311,7 +376,7 @@ int dustin_select(const dustin_params* p, const float* importance, const int32_t
                   int32_t* i_verify, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (!params_ok(p)) return DUSTIN_EINVAL;
   if (!importance || !seq_len || !i_verify) return DUSTIN_EINVAL;
-  if (!ws_ok(ws, ws_bytes, kHeader)) return DUSTIN_EWORKSPACE;
+  if (!ws_ok(ws, ws_bytes, kScratch)) return DUSTIN_EWORKSPACE;
   SelectArgs a{};
   a.B = p->B;
   a.Lcap = p->Lcap;
@@ -335,10 +400,10 @@ int dustin_verify_attn(const dustin_params* p, int32_t hq, const void* q, dustin
   const int st = check_verify_layer(p, hq, q, k, v, kb, vb, o);
   if (st != DUSTIN_OK) return st;
   if (!i_verify || !seq_len) return DUSTIN_EINVAL;
-  if (!ws_ok(ws, ws_bytes, kHeader)) return DUSTIN_EWORKSPACE;
+  if (!ws_ok(ws, ws_bytes, kScratch)) return DUSTIN_EWORKSPACE;
   VerifyLayerDev L;
   fill_layer(L, q, k, v, kb, vb, o);
-  return run_verify(p, hq, k.hkv, k.d, 1, &L, i_verify, seq_len, 0, ws, stream);
+  return run_verify(p, hq, k.hkv, k.d, 1, &L, i_verify, seq_len, 0, ws, ws_bytes, stream);
 }
 
 int dense_verify_attn(const dustin_params* p, int32_t hq, const void* q, dustin_kv k, dustin_kv v,
@@ -348,10 +413,10 @@ int dense_verify_attn(const dustin_params* p, int32_t hq, const void* q, dustin_
   const int st = check_verify_layer(p, hq, q, k, v, kb, vb, o);
   if (st != DUSTIN_OK) return st;
   if (!seq_len) return DUSTIN_EINVAL;
-  if (!ws_ok(ws, ws_bytes, kHeader)) return DUSTIN_EWORKSPACE;
+  if (!ws_ok(ws, ws_bytes, kScratch)) return DUSTIN_EWORKSPACE;
   VerifyLayerDev L;
   fill_layer(L, q, k, v, kb, vb, o);
-  return run_verify(p, hq, k.hkv, k.d, 1, &L, nullptr, seq_len, 1, ws, stream);
+  return run_verify(p, hq, k.hkv, k.d, 1, &L, nullptr, seq_len, 1, ws, ws_bytes, stream);
 }
 
 int dustin_kv_append(const dustin_params* p, int32_t n_layers, const dustin_kv* k,
@@ -362,7 +427,7 @@ int dustin_kv_append(const dustin_params* p, int32_t n_layers, const dustin_kv* 
   if (n_layers < 1) return DUSTIN_EINVAL;
   if (n_layers > DUSTIN_MAX_LAYERS) return DUSTIN_ERANGE;
   if (!k || !v || !kb || !vb || !n_accept || !seq_len) return DUSTIN_EINVAL;
-  if (!ws_ok(ws, ws_bytes, kHeader)) return DUSTIN_EWORKSPACE;
+  if (!ws_ok(ws, ws_bytes, kScratch)) return DUSTIN_EWORKSPACE;
   AppendArgs a{};
   a.B = p->B;
   a.Lcap = p->Lcap;
@@ -408,7 +473,14 @@ int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStre
     if (V.k.hkv != hkv || V.k.d != D) return DUSTIN_EINVAL;
     fill_layer(layers[l], V.q, V.k, V.v, V.kb, V.vb, V.o);
   }
-  if (!ws_ok(ws, ws_bytes, pl.total)) return DUSTIN_EWORKSPACE;
+  VerifyShape vs;
+  vs.hq = s->hq;
+  vs.hkv = hkv;
+  vs.d = D;
+  vs.n_layers = s->n_layers;
+  const size_t vneed = verify_ws_bytes(p, vs, 0);
+  if (vneed == 0) return DUSTIN_ERANGE;
+  if (!ws_ok(ws, ws_bytes, pl.total > vneed ? pl.total : vneed)) return DUSTIN_EWORKSPACE;
   cudaEvent_t* ev = s->stage_events;
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return DUSTIN_ECUDA;
   st = launch_score(p, s->draft, s->target, pl, s->seq_len, s->importance, ws, stream,
@@ -418,7 +490,8 @@ int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStre
   st = dustin_select(p, s->importance, s->seq_len, s->i_verify, ws, ws_bytes, stream);
   if (st != DUSTIN_OK) return st;
   if (ev && cudaEventRecord(ev[3], stream) != cudaSuccess) return DUSTIN_ECUDA;
-  st = run_verify(p, s->hq, hkv, D, s->n_layers, layers, s->i_verify, s->seq_len, 0, ws, stream);
+  st = run_verify(p, s->hq, hkv, D, s->n_layers, layers, s->i_verify, s->seq_len, 0, ws, ws_bytes,
+                  stream);
   if (st != DUSTIN_OK) return st;
   if (ev && cudaEventRecord(ev[4], stream) != cudaSuccess) return DUSTIN_ECUDA;
   return DUSTIN_OK;
@@ -462,7 +535,7 @@ extern "C" int dustin_score_noalloc(const dustin_params* p, const dustin_signal*
                                     int32_t n_srh, const int32_t* seq_len, float* importance,
                                     cudaStream_t stream) {
   static thread_local ScorePlan pl;
-  const int st = build_score_plan(p, draft, target, srh, n_srh, &pl);
+  const int st = build_score_plan(p, draft, target, srh, n_srh, &pl, kHeader);
   if (st != DUSTIN_OK) return st;
   if (!seq_len || !importance || !aligned16(importance)) return DUSTIN_EINVAL;
   if (pl.spill_bytes != 0 || pl.total > DUSTIN_NOALLOC_SCRATCH_BYTES) return DUSTIN_ERANGE;

@@ -25,21 +25,33 @@ struct VerifyArgs {
   int B, Lcap, T, hq, hkv, G, NQ;
   int k;                // budget (sparse); unused for dense
   int dense;            // 1: keys are positions 0..seq_len-1
-  int keys_per_split;   // multiple of 64
   int n_layers;
+  int ctx_tiles;        // 64-key tiles of context per unit
+  int tiles_u;          // ctx_tiles + 1 (the draft-block tile)
+  long long total;      // units * tiles_u
+  int max_seg;          // partial slots per unit
+  long long slot_floats;  // floats per partial slot (multiple of 4)
   float scale_log2;     // log2(e) / sqrt(D)
   const int32_t* ivf;   // [B][k] (sparse)
   const int32_t* seq_len;
   int* err;
+  float* partial;       // [units][max_seg][slot_floats]: O [NQ][D], m [NQ], l [NQ]
+  int* counters;        // [units], zero between launches
   VerifyLayerDev layer[DUSTIN_MAX_LAYERS];
 };
 
 struct VerifyLaunch {
-  int D, MT, NST, CS;
+  int D, MT, NST;
+  int ctx_tiles, tiles_u, grid, max_seg;
+  long long units, total, slot_floats;
   size_t smem;
 };
 
-VerifyLaunch verify_plan(int D, int NQ, int nkeys_cap, int B, int hkv, int n_layers, int dense);
+// Grid sizes never exceed kVerifyGridMax, which bounds the partial slots.
+constexpr int kVerifyGridMax = 256;
+VerifyLaunch verify_plan(int D, int NQ, int nkeys_cap, int B, int hkv, int n_layers, int dense,
+                         int num_sms);
+size_t verify_scratch_bytes(const VerifyLaunch& pl);
 cudaError_t verify_launch(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t stream);
 
 // ------------------------------------------------------------------- score

@@ -45,7 +45,8 @@ def test_workspace_sizing(L):
     from sparse_kv_verify_gb300 import binding as bd
     p = bd.CParams(2, 1024, 4, 4, 32, 32, 128)
     lib = L.lib()
-    assert lib.dustin_workspace_bytes(ctypes.byref(p), None, None, None, 0) == 256
+    base = 256 + 65536          # error word + verify combine counters
+    assert lib.dustin_workspace_bytes(ctypes.byref(p), None, None, None, 0, 0, 0, 0, 0) == base
     kv_t = (bd.CKV * 1)(bd.CKV(0x10000, 2, 128, 2 * 1024 * 128, 1024 * 128, 128))
     kv_d = (bd.CKV * 1)(bd.CKV(0x20000, 1, 64, 1024 * 64, 1024 * 64, 64))
     qt = (ctypes.c_void_p * 1)(0x30000)
@@ -53,16 +54,25 @@ def test_workspace_sizing(L):
     tgt = bd.CSignal(1, 8, 5, qt, kv_t)
     dft = bd.CSignal(1, 2, 4, qd, kv_d)
     srh = (bd.CSRH * 3)(bd.CSRH(1, 0, 0), bd.CSRH(1, 0, 7), bd.CSRH(0, 0, 1))
-    n = lib.dustin_workspace_bytes(ctypes.byref(p), ctypes.byref(dft), ctypes.byref(tgt), srh, 3)
+    n = lib.dustin_workspace_bytes(ctypes.byref(p), ctypes.byref(dft), ctypes.byref(tgt), srh, 3,
+                                   0, 0, 0, 0)
     # 3 slabs (target heads 0 and 7 sit in different KV groups) x B x Lcap fp32 partial maps
-    assert n == 256 + 3 * 2 * 1024 * 4
+    assert n == base + 3 * 2 * 1024 * 4
+    # verification adds per-unit partial slots [units][max_seg][NQ][d + 2]
+    nv = lib.dustin_workspace_bytes(ctypes.byref(p), None, None, None, 0, 8, 2, 128, 1)
+    assert nv > base
+    assert lib.dustin_workspace_bytes(ctypes.byref(p), None, None, None, 0, 8, 3, 128, 1) == 0
+    assert lib.dustin_workspace_bytes(ctypes.byref(p), None, None, None, 0, 8, 2, 96, 1) == 0
+    assert lib.dustin_workspace_bytes(ctypes.byref(p), None, None, None, 0, 8, 2, 128, 17) == 0
     # duplicate SRH, bad channel, head out of range -> 0 (invalid)
     for bad in [(1, 0, 0), ]:
         srh2 = (bd.CSRH * 2)(bd.CSRH(1, 0, 0), bd.CSRH(*bad))
-        assert lib.dustin_workspace_bytes(ctypes.byref(p), ctypes.byref(dft), ctypes.byref(tgt), srh2, 2) == 0
+        assert lib.dustin_workspace_bytes(ctypes.byref(p), ctypes.byref(dft), ctypes.byref(tgt), srh2, 2,
+                                          0, 0, 0, 0) == 0
     for bad in [(2, 0, 0), (1, 0, 8), (1, 1, 0), (0, 0, 2)]:
         srh2 = (bd.CSRH * 1)(bd.CSRH(*bad))
-        assert lib.dustin_workspace_bytes(ctypes.byref(p), ctypes.byref(dft), ctypes.byref(tgt), srh2, 1) == 0
+        assert lib.dustin_workspace_bytes(ctypes.byref(p), ctypes.byref(dft), ctypes.byref(tgt), srh2, 1,
+                                          0, 0, 0, 0) == 0
 
 
 def test_invalid_params_rejected(L):
@@ -77,7 +87,7 @@ def test_invalid_params_rejected(L):
         d.update(over)
         p = bd.CParams(*[d[f] for f in ("B", "Lcap", "gamma", "sinks", "window", "m", "k")])
         assert lib.dustin_select(ctypes.byref(p), 0x1000, 0x2000, 0x3000, ws, 1 << 20, None) == -1
-        assert lib.dustin_workspace_bytes(ctypes.byref(p), None, None, None, 0) == 0
+        assert lib.dustin_workspace_bytes(ctypes.byref(p), None, None, None, 0, 0, 0, 0, 0) == 0
     p = bd.CParams(*good.values())
     assert lib.dustin_select(ctypes.byref(p), None, 0x2000, 0x3000, ws, 1 << 20, None) == -1
     assert lib.dustin_select(ctypes.byref(p), 0x1000, 0x2000, 0x3000, None, 1 << 20, None) == -5

@@ -121,7 +121,7 @@ def test_verify_parity(name):
     wl, x = c.wl, c.x
     I_ref, _ = O.select(c.oracle_score(), x.seq_len, wl.k, wl.sinks, wl.window, wl.m)
     I = torch.as_tensor(I_ref.astype(np.int32), device="cuda")
-    ws = dk.workspace(c.p)
+    ws = dk.workspace(c.p, verify=(wl.Hq, wl.Hkv, wl.d, 1))
     o = dk.dustin_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], I, c.seq, ws=ws)
     assert dk.check(ws) == 0
     assert_attention(o, c.oracle_verify(I_ref))
@@ -131,7 +131,7 @@ def test_verify_parity(name):
 def test_dense_parity(name):
     c = Case(WORKLOADS[name])
     x = c.x
-    ws = dk.workspace(c.p)
+    ws = dk.workspace(c.p, verify=(c.wl.Hq, c.wl.Hkv, c.wl.d, 1))
     o = dk.dense_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], c.seq, ws=ws)
     assert dk.check(ws) == 0
     assert_attention(o, c.oracle_dense())
@@ -174,7 +174,7 @@ def test_verify_padding_and_bad_index():
     rng = np.random.default_rng(3)
     I_ref = np.sort(rng.choice(wl.L, 100, replace=False))
     I_pad = np.concatenate([I_ref, -np.ones(wl.k - 100, np.int64)])[None]
-    ws = dk.workspace(c.p)
+    ws = dk.workspace(c.p, verify=(wl.Hq, wl.Hkv, wl.d, 1))
     o = dk.dustin_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0],
                               torch.as_tensor(I_pad.astype(np.int32), device="cuda"), c.seq, ws=ws)
     assert dk.check(ws) == 0
