@@ -232,10 +232,10 @@ int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStre
  * looks up the array's device address (cudaGetSymbolAddress, with that device
  * current); make that first call before any stream capture.
  *
- * Limits: the per-KV-head partial maps (number of distinct SRH KV heads x B x
- * Lcap x 4 bytes, plus a 256-byte header) must fit in the array, and the
- * logits must fit on chip (no spill); otherwise DUSTIN_ERANGE is returned and
- * nothing is launched.  The device error word lives in the array too; it is
+ * Limits: the scratch of at least one sequence -- its logits (SRH pairs x
+ * Lcap x 4 bytes) and their statistics, plus a 256-byte header -- must fit in
+ * the array; larger batches are scored in groups of sequences that fit.
+ * Otherwise DUSTIN_ERANGE is returned and nothing is launched.  The device error word lives in the array too; it is
  * cleared at the start of every call and cannot be read by the caller.
  *
  * All calls share the one array and it keeps the last call's contents: calls

@@ -5,9 +5,10 @@
 //   [256, 256 + 64 KiB)      per-unit segment counters of the verify combine
 //                            (zero between calls; kept zero by the kernels)
 //   [kScratch, ...)          scratch shared by the stages of one call:
-//                            score: per-slab partial maps fp32 [n_slab][B][Lcap]
-//                                   (+ logits spill for very long caches)
-//                            verify: segment partials [units][max_seg][NQ][d+2]
+//                            score: logits of one group of sequences
+//                                   [n_slab][nb][pairs][LSP] (kept in L2) and
+//                                   per-segment (max, sum) statistics
+//                            verify: segment partials [units][max_seg][slot]
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -82,14 +83,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 4-D map over a cache view: dims (d, Lcap, hkv, B); box 64 x 64 x 1 x 1 with
+// 4-D map over a cache view: dims (d, Lcap, hkv, B); box 64 x 128 x 1 x 1 with
 // the 128-byte swizzle that the score kernel's ldmatrix addressing expects.
 bool encode_cache_map(CUtensorMap* m, const dustin_kv& v, int Lcap, int B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {cuuint64_t(v.d), cuuint64_t(Lcap), cuuint64_t(v.hkv), cuuint64_t(B)};
   cuuint64_t strides[3] = {cuuint64_t(v.sl) * 2, cuuint64_t(v.sh) * 2, cuuint64_t(v.sb) * 2};
-  cuuint32_t box[4] = {64, 64, 1, 1};
+  cuuint32_t box[4] = {64, 128, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v.ptr, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -99,6 +100,10 @@ bool encode_cache_map(CUtensorMap* m, const dustin_kv& v, int Lcap, int B) {
 
 // ------------------------------------------------------------- score plan
 
+// Logits of one group of sequences are kept under this size so that they stay
+// in L2 between the stream and the normalise kernels.
+constexpr size_t kScoreL2Budget = size_t(48) << 20;
+
 struct ScorePlan {
   int n_slab = 0;
   int n_cache = 0;
@@ -106,25 +111,33 @@ struct ScorePlan {
   int cache_layer[DUSTIN_MAX_SRH];
   ScoreSlab slab[DUSTIN_MAX_SRH];
   int np_max = 0;
-  int d_max = 0;
+  int LSP = 0;           // logits row stride (floats, multiple of 32)
+  int nb = 0;            // sequences per group
+  int max_seg = 0;
   ScoreLaunch launch{};
-  size_t part_off = 0, part_bytes = 0, spill_off = 0, spill_bytes = 0, total = 0;
+  size_t logits_off = 0, logits_bytes = 0, stats_off = 0, stats_bytes = 0, total = 0;
 };
 
 const dustin_signal* sig_of(int ch, const dustin_signal* draft, const dustin_signal* target) {
   return ch == 0 ? draft : target;
 }
 
-bool signal_ok(const dustin_signal* s, int Lcap) {
-  if (!s || s->n_layers < 1 || s->n_layers > 4096 || s->hq < 1 || s->nq < 1 || !s->q || !s->k)
-    return false;
-  (void)Lcap;
-  return true;
+bool signal_ok(const dustin_signal* s) {
+  return s && s->n_layers >= 1 && s->n_layers <= 4096 && s->hq >= 1 && s->nq >= 1 && s->q && s->k;
 }
 
+long long group_tiles(const ScorePlan& pl, int nb) {
+  long long t = 0;
+  for (int i = 0; i < pl.n_slab; ++i) t += (long long)nb * pl.slab[i].tiles;
+  return t;
+}
+
+// Validates the SRH list and plans the score launches.  scratch_off is where
+// the scratch begins in the workspace and scratch_max bounds it (0: no bound
+// beyond the L2 budget).
 int build_score_plan(const dustin_params* p, const dustin_signal* draft,
                      const dustin_signal* target, const dustin_srh* srh, int32_t n_srh,
-                     ScorePlan* pl, size_t scratch_off = kScratch) {
+                     ScorePlan* pl, size_t scratch_off = kScratch, size_t scratch_max = 0) {
   if (!params_ok(p)) return DUSTIN_EINVAL;
   if (!srh || n_srh < 1) return DUSTIN_EINVAL;
   if (n_srh > DUSTIN_MAX_SRH) return DUSTIN_ERANGE;
@@ -133,7 +146,7 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
     const dustin_srh& e = srh[i];
     if (e.channel != 0 && e.channel != 1) return DUSTIN_EINVAL;
     const dustin_signal* s = sig_of(e.channel, draft, target);
-    if (!signal_ok(s, p->Lcap)) return DUSTIN_EINVAL;
+    if (!signal_ok(s)) return DUSTIN_EINVAL;
     if (e.layer < 0 || e.layer >= s->n_layers) return DUSTIN_EINVAL;
     if (e.q_head < 0 || e.q_head >= s->hq) return DUSTIN_EINVAL;
     for (int j = 0; j < i; ++j)
@@ -144,7 +157,6 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
     if (!kv_ok(kv, p->Lcap) || !q || !aligned16(q)) return DUSTIN_EINVAL;
     if (s->hq % kv.hkv) return DUSTIN_EINVAL;
     const int g = e.q_head / (s->hq / kv.hkv);
-    // cache index
     int ci = -1;
     for (int c = 0; c < pl->n_cache; ++c)
       if (pl->cache_channel[c] == e.channel && pl->cache_layer[c] == e.layer) ci = c;
@@ -153,7 +165,6 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
       pl->cache_channel[ci] = e.channel;
       pl->cache_layer[ci] = e.layer;
     }
-    // slab index
     int sj = -1;
     for (int t = 0; t < pl->n_slab; ++t)
       if (pl->slab[t].cache == ci && pl->slab[t].g == g) sj = t;
@@ -168,6 +179,8 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
       S.hq = s->hq;
       S.nheads = 0;
       S.npairs = 0;
+      S.rows = score_rows_per_tile(kv.d);
+      S.tiles = (p->Lcap + S.rows - 1) / S.rows;
       S.q = static_cast<const uint16_t*>(q);
     }
     ScoreSlab& S = pl->slab[sj];
@@ -175,19 +188,47 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
     S.heads[S.nheads++] = e.q_head;
     S.npairs += s->nq;
   }
+  pl->LSP = (p->Lcap + 31) / 32 * 32;
+  size_t per_b = 0;   // logits bytes of one sequence
   for (int t = 0; t < pl->n_slab; ++t) {
     pl->np_max = pl->np_max > pl->slab[t].npairs ? pl->np_max : pl->slab[t].npairs;
-    pl->d_max = pl->d_max > pl->slab[t].D ? pl->d_max : pl->slab[t].D;
+    per_b += size_t(pl->slab[t].npairs) * pl->LSP * 4;
   }
-  pl->launch = score_plan(p->Lcap, p->B, pl->n_slab, pl->np_max, pl->d_max);
-  pl->part_off = scratch_off;
-  pl->part_bytes = round256(size_t(pl->n_slab) * p->B * p->Lcap * 4);
-  pl->spill_off = pl->part_off + pl->part_bytes;
-  pl->spill_bytes = pl->launch.smem_logits
-                        ? 0
-                        : round256(size_t(pl->n_slab) * p->B * pl->launch.C * pl->np_max *
-                                   size_t(pl->launch.LS) * 4);
-  pl->total = pl->spill_off + pl->spill_bytes;
+  // sequences per group: logits within the L2 budget (and the scratch bound)
+  size_t budget = kScoreL2Budget;
+  if (scratch_max) {
+    const size_t avail = scratch_max > scratch_off ? scratch_max - scratch_off : 0;
+    budget = avail < budget ? avail : budget;
+  }
+  long long nb = (long long)(budget / (per_b + 1));
+  for (;;) {
+    if (nb > p->B) nb = p->B;
+    if (nb < 1) {
+      if (scratch_max) return DUSTIN_ERANGE;   // a hard scratch bound: refuse
+      nb = 1;                                  // one sequence at a time, past the L2 budget
+    }
+    // statistics slots: the smallest group has the fewest tiles per CTA
+    const int last = int(p->B % nb ? p->B % nb : nb);
+    const long long per = group_tiles(*pl, last) / kScoreGridMax;
+    int tmax = 0;
+    for (int t = 0; t < pl->n_slab; ++t) tmax = tmax > pl->slab[t].tiles ? tmax : pl->slab[t].tiles;
+    pl->max_seg = int(tmax / (per > 0 ? per : 1)) + 2;
+    pl->nb = int(nb);
+    pl->logits_bytes = round256(per_b * nb);
+    pl->stats_bytes = round256(size_t(pl->n_slab) * nb * pl->max_seg * pl->np_max * 2 * 4);
+    pl->logits_off = scratch_off;
+    pl->stats_off = pl->logits_off + pl->logits_bytes;
+    pl->total = pl->stats_off + pl->stats_bytes;
+    if (!scratch_max || pl->total <= scratch_max) break;
+    --nb;
+  }
+  long long off = 0;
+  for (int t = 0; t < pl->n_slab; ++t) {
+    pl->slab[t].logit_off = off;
+    off += (long long)pl->nb * pl->slab[t].npairs * pl->LSP;
+  }
+  pl->launch.NT = (pl->np_max + 7) / 8;
+  pl->launch.smem = score_stream_smem();
   return DUSTIN_OK;
 }
 
@@ -203,26 +244,32 @@ int launch_score(const dustin_params* p, const dustin_signal* draft, const dusti
   for (int t = 0; t < pl.n_slab; ++t) a.slab[t] = pl.slab[t];
   a.B = p->B;
   a.Lcap = p->Lcap;
-  a.C = pl.launch.C;
-  a.P = pl.launch.P;
-  a.LS = pl.launch.LS;
+  a.LSP = pl.LSP;
   a.n_slab = pl.n_slab;
   a.np_max = pl.np_max;
+  a.max_seg = pl.max_seg;
   a.seq_len = seq_len;
   a.err = err_word(ws);
-  a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.part_off);
-  a.spill = pl.spill_bytes ? reinterpret_cast<float*>(static_cast<char*>(ws) + pl.spill_off) : nullptr;
-  if (score_launch(a, pl.launch, stream) != cudaSuccess) return DUSTIN_ECUDA;
+  a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.logits_off);
+  a.stats = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.stats_off);
+  a.importance = importance;
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  for (int b0 = 0; b0 < p->B; b0 += pl.nb) {
+    a.b0 = b0;
+    a.nb = p->B - b0 < pl.nb ? p->B - b0 : pl.nb;
+    long long acc = 0;
+    for (int t = 0; t < pl.n_slab; ++t) {
+      a.slab_start[t] = acc;
+      acc += (long long)a.nb * pl.slab[t].tiles;
+    }
+    a.slab_start[pl.n_slab] = acc;
+    a.total = acc;
+    long long grid = sms < kScoreGridMax ? sms : kScoreGridMax;
+    if (grid > a.total) grid = a.total;
+    a.grid = int(grid);
+    if (score_launch(a, pl.launch, stream) != cudaSuccess) return DUSTIN_ECUDA;
+  }
   if (mid && cudaEventRecord(mid, stream) != cudaSuccess) return DUSTIN_ECUDA;
-  ReduceArgs r{};
-  r.B = p->B;
-  r.Lcap = p->Lcap;
-  r.n_slab = pl.n_slab;
-  for (int t = 0; t < pl.n_slab; ++t) r.channel_of[t] = pl.slab[t].channel;
-  r.part = a.part;
-  r.seq_len = seq_len;
-  r.importance = importance;
-  if (score_reduce_launch(r, stream) != cudaSuccess) return DUSTIN_ECUDA;
   return DUSTIN_OK;
 }
 
@@ -535,10 +582,11 @@ extern "C" int dustin_score_noalloc(const dustin_params* p, const dustin_signal*
                                     int32_t n_srh, const int32_t* seq_len, float* importance,
                                     cudaStream_t stream) {
   static thread_local ScorePlan pl;
-  const int st = build_score_plan(p, draft, target, srh, n_srh, &pl, kHeader);
+  const int st = build_score_plan(p, draft, target, srh, n_srh, &pl, kHeader,
+                                  DUSTIN_NOALLOC_SCRATCH_BYTES);
   if (st != DUSTIN_OK) return st;
   if (!seq_len || !importance || !aligned16(importance)) return DUSTIN_EINVAL;
-  if (pl.spill_bytes != 0 || pl.total > DUSTIN_NOALLOC_SCRATCH_BYTES) return DUSTIN_ERANGE;
+  if (pl.total > DUSTIN_NOALLOC_SCRATCH_BYTES) return DUSTIN_ERANGE;
   void* ws = nullptr;
   const int s2 = noalloc_scratch(&ws);
   if (s2 != DUSTIN_OK) return s2;

@@ -26,7 +26,7 @@ struct VerifyArgs {
   int k;                // budget (sparse); unused for dense
   int dense;            // 1: keys are positions 0..seq_len-1
   int n_layers;
-  int ctx_tiles;        // 64-key tiles of context per unit
+  int ctx_tiles;        // 32-key tiles of context per unit
   int tiles_u;          // ctx_tiles + 1 (the draft-block tile)
   long long total;      // units * tiles_u
   int max_seg;          // partial slots per unit
@@ -48,7 +48,7 @@ struct VerifyLaunch {
 };
 
 // Grid sizes never exceed kVerifyGridMax, which bounds the partial slots.
-constexpr int kVerifyGridMax = 256;
+constexpr int kVerifyGridMax = 1024;
 VerifyLaunch verify_plan(int D, int NQ, int nkeys_cap, int B, int hkv, int n_layers, int dense,
                          int num_sms);
 size_t verify_scratch_bytes(const VerifyLaunch& pl);
@@ -66,37 +66,37 @@ struct ScoreSlab {
   int npairs;    // heads.size() * nq
   int nheads;
   int heads[DUSTIN_MAX_PAIRS];
-  const uint16_t* q;  // [B][nq][hq][D]
+  int rows;      // positions per tile (128 for d = 128, 256 for d = 64)
+  int tiles;     // tiles per sequence: ceil(Lcap / rows)
+  long long logit_off;   // float offset of this slab's logits [nb][npairs][LSP]
+  const uint16_t* q;     // [B][nq][hq][D]
 };
 
 struct ScoreArgs {
-  CUtensorMap map[DUSTIN_MAX_SRH];   // one per (channel, layer) cache
+  CUtensorMap map[DUSTIN_MAX_SRH];   // one per (channel, layer) cache; box 64 x 128
   ScoreSlab slab[DUSTIN_MAX_SRH];
-  int B, Lcap, C, P, LS, n_slab, np_max;
+  long long slab_start[DUSTIN_MAX_SRH + 1];   // first flattened tile of each slab
+  long long total;                            // tiles of this group
+  int B, Lcap, LSP, n_slab, np_max;
+  int b0, nb;            // the group of sequences handled by this launch
+  int grid;              // CTAs of the stream kernel
+  int max_seg;           // statistics slots per (slab, sequence)
   const int32_t* seq_len;
   int* err;
-  float* part;          // [n_slab][B][Lcap]
-  float* spill;         // logits in global memory when they do not fit on chip
+  float* logits;         // scratch, stays in L2 between the two kernels
+  float* stats;          // [n_slab][nb][max_seg][np_max][2]
+  float* importance;     // [B][2][Lcap]
 };
 
 struct ScoreLaunch {
-  int C, P, LS, NT, np_max;
-  bool smem_logits;
+  int NT;
   size_t smem;
-  size_t spill_bytes;
 };
 
-ScoreLaunch score_plan(int Lcap, int B, int n_slab, int np_max, int d_max);
+constexpr int kScoreGridMax = 256;
+size_t score_stream_smem();
+int score_rows_per_tile(int D);
 cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream);
-
-struct ReduceArgs {
-  int B, Lcap, n_slab;
-  int channel_of[DUSTIN_MAX_SRH];
-  const float* part;
-  const int32_t* seq_len;
-  float* importance;   // [B][2][Lcap]
-};
-cudaError_t score_reduce_launch(const ReduceArgs& a, cudaStream_t stream);
 
 // ------------------------------------------------------------------ select
 

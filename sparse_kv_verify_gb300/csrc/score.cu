@@ -2,116 +2,90 @@
 // Dustin", section 1 "Hybrid Attention Aggregation" and section 2 "Efficient
 // Estimation via Semantic Retrieval Heads").
 //
-// Work unit: a "slab" = one (channel, layer, KV head g) of one sequence b,
-// together with every (SRH head of group g, query row) pair that reads it.
-// A thread-block cluster of C CTAs covers the slab; CTA r owns positions
-// [r*P, (r+1)*P) and
-//   phase 1  streams its K rows once with 4-D TMA tiles (64 rows x 64 columns,
-//            128-byte swizzle) through a 4-stage mbarrier ring, computes
-//            logits l = q.k * log2(e)/sqrt(d) for all pairs at once as bf16
-//            m16n8k16 MMAs (positions x pairs), keeps them in shared memory
-//            and tracks per-pair maxima;
-//   exchange the CTAs swap per-pair maxima, then per-pair sums of
-//            exp2(l - M), through distributed shared memory;
-//   phase 2  writes sum_pairs exp2(l - M_pair) / S_pair for each position: the
-//            softmax normalisation and the sum over heads and query rows are
-//            fused, and no attention tensor is ever written.
-// A deterministic reduce then sums the per-slab maps of each channel in slab
-// order into importance[B][2][Lcap].
-#include <cooperative_groups.h>
-
+// A "slab" is one (channel, layer, KV head g): every (SRH head of group g,
+// query row) pair of that channel reads the same K rows.  For each sequence b
+// the importance of position i in channel c is
+//     sum over the slabs of c, sum over their pairs p of
+//         exp(l_p,i - M_p) / S_p,   l = q.k / sqrt(d) (kept in the log2 domain)
+// where M_p, S_p are the max and the sum of exp over the whole context.
+//
+// Kernel A (stream): the tiles of all (slab, sequence) pairs of a group of
+// sequences form one sequence that is split evenly over one CTA per SM.  Each
+// CTA streams its K rows once with 2-D TMA boxes (64 columns x 128 rows,
+// 128-byte swizzle; 32 KB per tile) through a 6-stage mbarrier ring, computes
+// the logits of all pairs at once with bf16 m16n8k16 MMAs (positions x
+// pairs), writes them to a scratch buffer that stays in L2, and keeps an online
+// (max, sum of exp) per pair for each contiguous segment of its range.
+//
+// Kernel B (normalise): per sequence, merges the segment statistics into
+// M_p, S_p, then reads the logits back from L2, applies exp2(l - M_p) / S_p,
+// sums over pairs and over the slabs of each channel and writes importance.
+// It then discards the scratch lines from L2 so that they are never written
+// back to HBM.  No attention tensor is materialised and K is read once.
 #include "common.cuh"
 #include "kernels.h"
-
-namespace cg = cooperative_groups;
 
 namespace dustin {
 
 namespace {
 
-constexpr int kRows = 64;              // positions per tile
-constexpr int kBox = 64;               // bf16 columns per TMA box (128 bytes)
-constexpr int kBoxBytes = kRows * kBox * 2;
-constexpr int kStages = 4;
-constexpr int kStageBytes = 2 * kBoxBytes;   // room for d = 128
-constexpr int kConsumers = 4;          // 4 warps x 16 rows = one 64-row tile
+constexpr int kBoxCols = 64;
+constexpr int kBoxRows = 128;
+constexpr int kBoxBytes = kBoxCols * kBoxRows * 2;   // 16 KB
+constexpr int kTileBytes = 2 * kBoxBytes;            // 128 rows x 128 or 256 rows x 64
+constexpr int kStages = 6;
+constexpr int kConsumers = 8;                        // 8 warps x 16 rows = 128 rows
 constexpr int kThreads = 32 * (kConsumers + 1);
-constexpr int kMaxKs = 8;              // d / 16 for d = 128
+constexpr int kMaxKs = 8;                            // d / 16 for d = 128
+constexpr int kNormChunk = 1024;                     // positions per normalise CTA
 
-struct ScoreSmemLayout {
-  size_t ring = 0;                      // 1024-aligned
-  size_t logits = 0;
-  size_t small = 0;
-  size_t total = 0;
-};
-
-__host__ __device__ inline ScoreSmemLayout score_layout(int np_max, int LS, bool smem_logits) {
-  ScoreSmemLayout s;
-  s.ring = 0;
-  s.logits = size_t(kStages) * kStageBytes;
-  const size_t lg = smem_logits ? size_t(np_max) * LS * 4 : 0;
-  s.small = s.logits + lg;
-  // red[4][32] | stat_m[32] | stat_s[32] | Mg[32] | inv[32] | full[4] | empty[4] | abort
-  // +1024: the ring is aligned to 1024 bytes (128-byte swizzle atom) at run time
-  s.total = s.small + (kConsumers * 32 + 4 * 32) * 4 + kStages * 16 + 16 + 1024;
-  return s;
+__device__ __forceinline__ uint32_t tile_addr(uint32_t st, int D, int r, int c) {
+  // element (row r, column c) of a tile stored as two TMA boxes of
+  // [128 rows][128 bytes] with the 128-byte swizzle (chunk ^= row % 8)
+  const int box = (D == 128) ? (c >> 6) : (r >> 7);
+  const int chunk = (c & 63) >> 3;
+  return st + box * kBoxBytes + (r & 127) * 128 + ((chunk ^ (r & 7)) << 4) + ((c & 7) << 1);
 }
 
-__device__ __forceinline__ uint32_t swz128(uint32_t stage, int row, int col) {
-  // element (row, col) of a tile stored as d/64 boxes of [64 rows][128 bytes]
-  // with the TMA 128-byte swizzle (16-byte chunk index XOR row % 8)
-  const int box = col >> 6;
-  const int chunk = (col & 63) >> 3;
-  return stage + box * kBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4) + ((col & 7) << 1);
+__device__ __forceinline__ int cta_of(long long x, long long total, int G) {
+  return int(((x + 1) * G + total - 1) / total) - 1;
 }
 
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-template <int NT, bool SMEM_LOGITS>
-__global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ ScoreArgs A) {
+__device__ __forceinline__ void stat_merge(float& m, float& s, float m2, float s2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  s = (m == -INFINITY ? 0.f : s * exp2f(m - M)) + (m2 == -INFINITY ? 0.f : s2 * exp2f(m2 - M));
+  m = M;
+}
+
+// Slab and sequence of flattened tile t of the group.
+__device__ __forceinline__ void decode_tile(const ScoreArgs& A, long long t, int& s, int& bl,
+                                            int& tile) {
+  s = 0;
+  while (s + 1 < A.n_slab && A.slab_start[s + 1] <= t) ++s;
+  const long long off = t - A.slab_start[s];
+  bl = int(off / A.slab[s].tiles);
+  tile = int(off - (long long)bl * A.slab[s].tiles);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_constant__ ScoreArgs A) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const ScoreSmemLayout lay = score_layout(A.np_max, A.LS, SMEM_LOGITS);
-  unsigned char* ring = smem + lay.ring;
-  float* red = reinterpret_cast<float*>(smem + lay.small);
-  float* stat_m = red + kConsumers * 32;
-  float* stat_s = stat_m + 32;
-  float* Mg = stat_s + 32;
-  float* inv = Mg + 32;
-  uint64_t* full = reinterpret_cast<uint64_t*>(inv + 32);
+  unsigned char* ring = smem;
+  float* red = reinterpret_cast<float*>(smem + size_t(kStages) * kTileBytes);   // [8][32][2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + kConsumers * 32 * 2);
   uint64_t* empty = full + kStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
 
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = static_cast<int>(cluster.num_blocks());
-  const int r = static_cast<int>(cluster.block_rank());
-  const int si = blockIdx.y;
-  const int b = blockIdx.z;
-  const ScoreSlab& S = A.slab[si];
-  const int D = S.D;
-  const int nks = D >> 4;
-  const int npairs = S.npairs;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  float* lg = SMEM_LOGITS
-                  ? reinterpret_cast<float*>(smem + lay.logits)
-                  : A.spill + ((size_t(si) * A.B + b) * C + r) * size_t(A.np_max) * A.LS;
-
-  int L = A.seq_len[b];
-  if (L < 0 || L > A.Lcap) {
-    if (threadIdx.x == 0 && r == 0 && si == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
-    L = 0;
-  }
-  const int p0 = r * A.P;
-  const int p1 = min(p0 + A.P, L);
-  const int npos = max(0, p1 - p0);
-  const int n_tiles = (npos + kRows - 1) / kRows;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x;
+  const long long t0 = (long long)blockIdx.x * A.total / G;
+  const long long t1 = (long long)(blockIdx.x + 1) * A.total / G;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -123,242 +97,270 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   }
   __syncthreads();
 
-  const float scale = kLog2e * rsqrtf(float(D));
-
   if (warp == kConsumers) {
     // ----------------------------------------------------------- TMA producer
-    if (lane == 0 && n_tiles > 0) {
-      const CUtensorMap* map = &A.map[S.cache];
-      prefetch_tensormap(map);
+    if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      const uint32_t bytes = uint32_t(D / kBox) * kBoxBytes;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int s = i % kStages;
+      for (long long t = t0; t < t1; ++t) {
+        const int i = int(t - t0);
+        const int st = i % kStages;
         if (i >= kStages) {
-          if (!mbar_wait(&empty[s], ((i / kStages) - 1) & 1, A.err, abort_flag)) break;
+          if (!mbar_wait(&empty[st], ((i / kStages) - 1) & 1, A.err, abort_flag)) break;
         }
-        mbar_arrive_expect_tx(&full[s], bytes);
-        unsigned char* st = ring + size_t(s) * kStageBytes;
-        for (int h = 0; h < D / kBox; ++h)
-          tma_load_4d(st + h * kBoxBytes, map, h * kBox, p0 + i * kRows, S.g, b, &full[s], pol);
+        int s, bl, tile;
+        decode_tile(A, t, s, bl, tile);
+        const ScoreSlab& S = A.slab[s];
+        const int b = A.b0 + bl;
+        int L = A.seq_len[b];
+        if (L < 0 || L > A.Lcap) L = 0;
+        const int r0 = tile * S.rows;
+        if (r0 >= L) {
+          mbar_arrive(&full[st]);   // nothing to load: an empty tile
+          continue;
+        }
+        const CUtensorMap* map = &A.map[S.cache];
+        unsigned char* dst = ring + size_t(st) * kTileBytes;
+        if (S.D == 128) {
+          mbar_arrive_expect_tx(&full[st], 2 * kBoxBytes);
+          tma_load_4d(dst, map, 0, r0, S.g, b, &full[st], pol);
+          tma_load_4d(dst + kBoxBytes, map, 64, r0, S.g, b, &full[st], pol);
+        } else {
+          const bool two = r0 + kBoxRows < L;
+          mbar_arrive_expect_tx(&full[st], two ? 2 * kBoxBytes : kBoxBytes);
+          tma_load_4d(dst, map, 0, r0, S.g, b, &full[st], pol);
+          if (two) tma_load_4d(dst + kBoxBytes, map, 0, r0 + kBoxRows, S.g, b, &full[st], pol);
+        }
       }
     }
   } else {
     // -------------------------------------------------------------- consumers
-    // B fragments of Q^T (d x pairs), loaded once: pair n = 8j + lane/4.
     uint32_t qb[NT][kMaxKs][2];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const int p = 8 * j + (lane >> 2);
-      const uint16_t* qrow = nullptr;
-      if (p < npairs) {
-        const int hi = p / S.nq, t = p % S.nq;
-        qrow = S.q + ((size_t(b) * S.nq + t) * S.hq + S.heads[hi]) * D;
+    float rm[NT][2], rs[NT][2];   // online (max, sum) per pair column
+    int cur_s = -1, cur_bl = -1;
+    for (long long t = t0; t < t1; ++t) {
+      const int i = int(t - t0);
+      const int st = i % kStages;
+      int s, bl, tile;
+      decode_tile(A, t, s, bl, tile);
+      const ScoreSlab& S = A.slab[s];
+      const int D = S.D;
+      const int b = A.b0 + bl;
+      int L = A.seq_len[b];
+      if (L < 0 || L > A.Lcap) {
+        if (lane == 0 && warp == 0 && tile == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
+        L = 0;
       }
+      if (s != cur_s || bl != cur_bl) {
+        // new segment: load Q^T fragments (d x pairs) of this slab and sequence
+        cur_s = s;
+        cur_bl = bl;
 #pragma unroll
-      for (int ks = 0; ks < kMaxKs; ++ks) {
-        uint32_t v0 = 0, v1 = 0;
-        if (qrow && ks < nks) {
-          v0 = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * (lane & 3));
-          v1 = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * (lane & 3));
+        for (int j = 0; j < NT; ++j) {
+          const int p = 8 * j + (lane >> 2);
+          const uint16_t* qrow = nullptr;
+          if (p < S.npairs) {
+            const int hi = p / S.nq, tq = p - (p / S.nq) * S.nq;
+            qrow = S.q + ((size_t(b) * S.nq + tq) * S.hq + S.heads[hi]) * D;
+          }
+#pragma unroll
+          for (int ks = 0; ks < kMaxKs; ++ks) {
+            uint32_t v0 = 0, v1 = 0;
+            if (qrow && ks < (D >> 4)) {
+              v0 = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * (lane & 3));
+              v1 = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * (lane & 3));
+            }
+            qb[j][ks][0] = v0;
+            qb[j][ks][1] = v1;
+          }
+          rm[j][0] = rm[j][1] = -INFINITY;
+          rs[j][0] = rs[j][1] = 0.f;
         }
-        qb[j][ks][0] = v0;
-        qb[j][ks][1] = v1;
       }
-    }
-    float runmax[NT][2];
+      // on a give-up the loop keeps running without work so that every warp
+      // still reaches every named barrier below
+      const bool ok = mbar_wait(&full[st], (i / kStages) & 1, A.err, abort_flag);
+      const int r0 = tile * S.rows;
+      if (ok && r0 < L) {
+        const uint32_t sb = smem_u32(ring + size_t(st) * kTileBytes);
+        const int nmt = (D == 128) ? 1 : 2;
+        const float scale = kLog2e * rsqrtf(float(D));
+        float* lrow = A.logits + S.logit_off + size_t(bl) * S.npairs * A.LSP;
 #pragma unroll
-    for (int j = 0; j < NT; ++j) runmax[j][0] = runmax[j][1] = -INFINITY;
-
-    for (int i = 0; i < n_tiles; ++i) {
-      const int s = i % kStages;
-      if (!mbar_wait(&full[s], (i / kStages) & 1, A.err, abort_flag)) break;
-      const uint32_t st = smem_u32(ring + size_t(s) * kStageBytes);
-      float c[NT][4];
+        for (int mi = 0; mi < 2; ++mi) {
+          if (mi >= nmt) break;
+          const int rb = 16 * warp + kBoxRows * mi;
+          float c[NT][4];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
-      const int arow = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1);
+          for (int j = 0; j < NT; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+          const int arow = rb + (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
-      for (int ks = 0; ks < kMaxKs; ++ks) {
-        if (ks < nks) {
-          uint32_t a0, a1, a2, a3;
-          ldmatrix_x4(a0, a1, a2, a3, swz128(st, arow, 16 * ks + 8 * (lane >> 4)));
+          for (int ks = 0; ks < kMaxKs; ++ks) {
+            if (ks < (D >> 4)) {
+              uint32_t a0, a1, a2, a3;
+              ldmatrix_x4(a0, a1, a2, a3, tile_addr(sb, D, arow, 16 * ks + 8 * (lane >> 4)));
 #pragma unroll
-          for (int j = 0; j < NT; ++j) mma_bf16_16816(c[j], a0, a1, a2, a3, qb[j][ks][0], qb[j][ks][1]);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      // logits of positions lo = row lane/4 and hi = row lane/4 + 8 of this warp
-      const int loc_lo = i * kRows + 16 * warp + (lane >> 2);
+              for (int j = 0; j < NT; ++j)
+                mma_bf16_16816(c[j], a0, a1, a2, a3, qb[j][ks][0], qb[j][ks][1]);
+            }
+          }
+          const int pos_lo = r0 + rb + (lane >> 2);
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
+          for (int j = 0; j < NT; ++j) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int pair = 8 * j + 2 * (lane & 3) + (e & 1);
-          const int loc = loc_lo + ((e >> 1) << 3);
-          const float v = (loc < npos) ? c[j][e] * scale : -INFINITY;
-          if (pair < npairs) {
-            lg[size_t(pair) * A.LS + loc] = v;
-            runmax[j][e & 1] = fmaxf(runmax[j][e & 1], v);
+            for (int e = 0; e < 4; ++e) {
+              const int pair = 8 * j + 2 * (lane & 3) + (e & 1);
+              const int pos = pos_lo + ((e >> 1) << 3);
+              if (pair < S.npairs && pos < L) {
+                const float v = c[j][e] * scale;
+                lrow[size_t(pair) * A.LSP + pos] = v;
+                float& m = rm[j][e & 1];
+                float& sm = rs[j][e & 1];
+                if (v > m) {
+                  sm = sm * exp2f(m - v) + 1.f;
+                  m = v;
+                } else {
+                  sm += exp2f(v - m);
+                }
+              }
+            }
           }
         }
       }
-    }
-    // per-pair CTA maxima: lanes sharing lane%4 hold the same pairs
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+
+      // end of segment: reduce the statistics and write them out
+      bool seg_end = (t + 1 == t1);
+      if (!seg_end) {
+        int s2, bl2, tile2;
+        decode_tile(A, t + 1, s2, bl2, tile2);
+        seg_end = (s2 != s || bl2 != bl);
+      }
+      if (seg_end) {
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
+        for (int j = 0; j < NT; ++j) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float v = runmax[j][e];
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-        const int pair = 8 * j + 2 * lane + e;
-        if (lane < 4 && pair < 32) red[warp * 32 + pair] = v;
+          for (int e = 0; e < 2; ++e) {
+            float m = rm[j][e], sm = rs[j][e];
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+              const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+              const float s2 = __shfl_xor_sync(0xffffffffu, sm, o);
+              stat_merge(m, sm, m2, s2);
+            }
+            const int pair = 8 * j + 2 * lane + e;
+            if (lane < 4) {
+              red[(warp * 32 + pair) * 2] = m;
+              red[(warp * 32 + pair) * 2 + 1] = sm;
+            }
+          }
+        }
+        named_bar(1, 32 * kConsumers);
+        if (warp == 0 && lane < S.npairs) {
+          float m = -INFINITY, sm = 0.f;
+          for (int w = 0; w < kConsumers; ++w)
+            stat_merge(m, sm, red[(w * 32 + lane) * 2], red[(w * 32 + lane) * 2 + 1]);
+          const long long first = A.slab_start[s] + (long long)bl * S.tiles;
+          const int seg = int(blockIdx.x) - cta_of(first, A.total, G);
+          float* slot = A.stats + ((size_t(s) * A.nb + bl) * A.max_seg + seg) * size_t(A.np_max) * 2;
+          slot[lane * 2] = m;
+          slot[lane * 2 + 1] = sm;
+        }
+        named_bar(1, 32 * kConsumers);
       }
     }
   }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    const int p = threadIdx.x;
-    float v = -INFINITY;
-    if (p < npairs)
-      for (int w = 0; w < kConsumers; ++w) v = fmaxf(v, red[w * 32 + p]);
-    stat_m[p] = v;
-  }
-  cluster.sync();  // exchange 1: maxima
-  if (threadIdx.x < 32) {
-    const int p = threadIdx.x;
-    float M = -INFINITY;
-    if (p < npairs)
-      for (int q = 0; q < C; ++q) M = fmaxf(M, *cluster.map_shared_rank(stat_m + p, q));
-    Mg[p] = M;
-  }
-  __syncthreads();
-  // exponentiate in place and sum per pair (warp w takes pairs w, w+5, ...)
-  for (int p = warp; p < npairs; p += kConsumers + 1) {
-    const float M = Mg[p];
-    float* row = lg + size_t(p) * A.LS;
-    float acc = 0.f;
-    for (int loc = lane; loc < npos; loc += 32) {
-      const float e = (M == -INFINITY) ? 0.f : exp2f(row[loc] - M);
-      row[loc] = e;
-      acc += e;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) stat_s[p] = acc;
-  }
-  __syncthreads();
-  cluster.sync();  // exchange 2: sums
-  if (threadIdx.x < 32) {
-    const int p = threadIdx.x;
-    float Ssum = 0.f;
-    if (p < npairs)
-      for (int q = 0; q < C; ++q) Ssum += *cluster.map_shared_rank(stat_s + p, q);
-    inv[p] = Ssum > 0.f ? 1.f / Ssum : 0.f;
-  }
-  cluster_arrive();  // remote reads of this CTA are done once everyone arrives
-  __syncthreads();
-  float* part = A.part + (size_t(si) * A.B + b) * A.Lcap + p0;
-  for (int loc = threadIdx.x; loc < npos; loc += kThreads) {
-    float acc = 0.f;
-    for (int p = 0; p < npairs; ++p) acc += lg[size_t(p) * A.LS + loc] * inv[p];
-    part[loc] = acc;
-  }
-  cluster_wait();
 }
 
-template <int NT, bool SM>
-cudaError_t launch_t(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream) {
-  auto kern = score_kernel<NT, SM>;
+__global__ void __launch_bounds__(256) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
+  __shared__ float Mg[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
+  __shared__ float Ig[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
+  const int bl = blockIdx.y;
+  const int b = A.b0 + bl;
+  int L = A.seq_len[b];
+  if (L < 0 || L > A.Lcap) L = 0;
+  const int G = A.grid;
+  for (int q = threadIdx.x; q < A.n_slab * DUSTIN_MAX_PAIRS; q += blockDim.x) {
+    const int s = q / DUSTIN_MAX_PAIRS, p = q - s * DUSTIN_MAX_PAIRS;
+    const ScoreSlab& S = A.slab[s];
+    float m = -INFINITY, sm = 0.f;
+    if (p < S.npairs) {
+      const long long first = A.slab_start[s] + (long long)bl * S.tiles;
+      const int n_seg = cta_of(first + S.tiles - 1, A.total, G) - cta_of(first, A.total, G) + 1;
+      const float* slots = A.stats + (size_t(s) * A.nb + bl) * A.max_seg * size_t(A.np_max) * 2;
+      for (int g = 0; g < n_seg; ++g)
+        stat_merge(m, sm, __ldcg(slots + (size_t(g) * A.np_max + p) * 2),
+                   __ldcg(slots + (size_t(g) * A.np_max + p) * 2 + 1));
+    }
+    Mg[q] = m;
+    Ig[q] = sm > 0.f ? 1.f / sm : 0.f;
+  }
+  __syncthreads();
+  const int base = blockIdx.x * kNormChunk;
+  for (int c = 0; c < 2; ++c) {
+    float* out = A.importance + (size_t(b) * 2 + c) * A.Lcap;
+    for (int pos = base + threadIdx.x; pos < base + kNormChunk && pos < A.Lcap; pos += blockDim.x) {
+      float acc = 0.f;
+      if (pos < L) {
+        for (int s = 0; s < A.n_slab; ++s) {
+          const ScoreSlab& S = A.slab[s];
+          if (S.channel != c) continue;
+          const float* lrow = A.logits + S.logit_off + size_t(bl) * S.npairs * A.LSP + pos;
+          for (int p = 0; p < S.npairs; ++p) {
+            const float l = __ldcs(lrow + size_t(p) * A.LSP);
+            acc += exp2f(l - Mg[s * DUSTIN_MAX_PAIRS + p]) * Ig[s * DUSTIN_MAX_PAIRS + p];
+          }
+        }
+      }
+      out[pos] = acc;
+    }
+  }
+  // the logits of this chunk are dead: drop them from L2 without write-back
+  __syncthreads();
+  const int lines_per_row = kNormChunk * 4 / 128;
+  int nrows = 0;
+  for (int s = 0; s < A.n_slab; ++s) nrows += A.slab[s].npairs;
+  for (int q = threadIdx.x; q < nrows * lines_per_row; q += blockDim.x) {
+    int r = q / lines_per_row;
+    const int ln = q - r * lines_per_row;
+    int s = 0;
+    while (r >= A.slab[s].npairs) r -= A.slab[s++].npairs;
+    const ScoreSlab& S = A.slab[s];
+    const size_t off = S.logit_off + (size_t(bl) * S.npairs + r) * A.LSP + base + ln * 32;
+    if (base + ln * 32 < A.LSP)
+      asm volatile("discard.global.L2 [%0], 128;" ::"l"(A.logits + off) : "memory");
+  }
+}
+
+template <int NT>
+cudaError_t launch_stream(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream) {
+  auto kern = score_stream_kernel<NT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem));
   if (e != cudaSuccess) return e;
-  if (pl.C > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.C, a.n_slab, a.B);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = pl.smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = pl.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a);
-}
-
-template <bool SM>
-cudaError_t launch_nt(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream) {
-  switch (pl.NT) {
-    case 1: return launch_t<1, SM>(a, pl, stream);
-    case 2: return launch_t<2, SM>(a, pl, stream);
-    case 3: return launch_t<3, SM>(a, pl, stream);
-    case 4: return launch_t<4, SM>(a, pl, stream);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-__global__ void score_reduce_kernel(const __grid_constant__ ReduceArgs R) {
-  const int c = blockIdx.y;
-  const int b = blockIdx.z;
-  const int pos = blockIdx.x * blockDim.x + threadIdx.x;
-  if (pos >= R.Lcap) return;
-  int L = R.seq_len[b];
-  if (L < 0 || L > R.Lcap) L = 0;
-  float v = 0.f;
-  if (pos < L) {
-    for (int s = 0; s < R.n_slab; ++s)
-      if (R.channel_of[s] == c) v += R.part[(size_t(s) * R.B + b) * R.Lcap + pos];
-  }
-  R.importance[(size_t(b) * 2 + c) * R.Lcap + pos] = v;
+  kern<<<a.grid, kThreads, pl.smem, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-ScoreLaunch score_plan(int Lcap, int B, int n_slab, int np_max, int d_max) {
-  (void)B;
-  (void)n_slab;
-  (void)d_max;
-  ScoreLaunch pl{};
-  pl.np_max = np_max;
-  pl.NT = (np_max + 7) / 8;
-  const size_t budget = 220 * 1024;
-  for (int C : {8, 16}) {
-    const int per = (Lcap + C - 1) / C;
-    const int P = ((per + kRows - 1) / kRows) * kRows;
-    const int LS = P + 4;
-    const ScoreSmemLayout l = score_layout(np_max, LS, true);
-    pl.C = C;
-    pl.P = P;
-    pl.LS = LS;
-    if (l.total <= budget) {
-      pl.smem_logits = true;
-      pl.smem = l.total;
-      pl.spill_bytes = 0;
-      return pl;
-    }
-  }
-  // logits too large for shared memory: keep them in a global scratch slice
-  pl.smem_logits = false;
-  pl.smem = score_layout(np_max, pl.LS, false).total;
-  pl.spill_bytes = 0;  // caller multiplies per slab/sequence/CTA
-  return pl;
+size_t score_stream_smem() {
+  return size_t(kStages) * kTileBytes + kConsumers * 32 * 2 * 4 + kStages * 16 + 16 + 1024;
 }
+
+int score_rows_per_tile(int D) { return D == 128 ? kBoxRows : 2 * kBoxRows; }
 
 cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream) {
-  return pl.smem_logits ? launch_nt<true>(a, pl, stream) : launch_nt<false>(a, pl, stream);
-}
-
-cudaError_t score_reduce_launch(const ReduceArgs& a, cudaStream_t stream) {
-  dim3 grid((a.Lcap + 255) / 256, 2, a.B);
-  score_reduce_kernel<<<grid, 256, 0, stream>>>(a);
+  cudaError_t e;
+  switch (pl.NT) {
+    case 1: e = launch_stream<1>(a, pl, stream); break;
+    case 2: e = launch_stream<2>(a, pl, stream); break;
+    case 3: e = launch_stream<3>(a, pl, stream); break;
+    case 4: e = launch_stream<4>(a, pl, stream); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Lcap + kNormChunk - 1) / kNormChunk, a.nb);
+  score_norm_kernel<<<grid, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -7,17 +7,19 @@
 // entries of I_verify; dense: positions 0..seq_len-1) plus the gamma+1
 // draft-block rows under the causal mask u <= t.
 //
-// Schedule (stream-K): each unit is cut into 64-key tiles followed by one
+// Schedule (stream-K): each unit is cut into 32-key tiles followed by one
 // block tile; all units' tiles form one sequence that is split evenly over a
 // grid sized to the GPU's resident capacity, so every CTA moves the same
 // number of bytes whatever B, Hkv and k are.  A CTA walks its range one unit
 // segment at a time.
 //
 // Data path: every warp issues 16-byte cp.async gathers (zero-filled for
-// padding / out-of-context rows) into a 4-stage ring of padded shared-memory
-// rows (2*d + 16 bytes, so ldmatrix is bank-conflict free); the index list
-// runs one stage ahead through shared memory.  Two warps share each 16-row
-// m-tile of queries and take one half of every 64-key tile: S = Q K^T and
+// padding / out-of-context rows) into a 3-stage ring of 32-key tiles in padded
+// shared-memory rows (2*d + 16 bytes, so ldmatrix is bank-conflict free); the
+// index list runs one stage ahead through shared memory.  The ring is small so
+// that several CTAs share an SM: cp.async reaches HBM bandwidth only with many
+// resident warps.  Two warps share each 16-row m-tile of queries and take one
+// half of every key tile: S = Q K^T and
 // O += P V are bf16 m16n8k16 tensor-core MMAs with fp32 accumulation, with an
 // online softmax in the log2 domain.
 //
@@ -32,7 +34,9 @@ namespace dustin {
 
 namespace {
 
-constexpr int TK = 64;  // keys per tile
+constexpr int TK = 32;  // keys per tile: small stages so that ~3 CTAs share an SM
+constexpr int NSTAGE = 3;
+constexpr int TKH = TK / 2;   // keys per warp (each m-tile has two warps)
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
@@ -69,7 +73,7 @@ __device__ __forceinline__ int cta_of(long long x, long long total, int G) {
 }
 
 template <int D, int MT, int NST>
-__global__ void __launch_bounds__(64 * MT, 1) verify_kernel(const __grid_constant__ VerifyArgs A) {
+__global__ void __launch_bounds__(64 * MT) verify_kernel(const __grid_constant__ VerifyArgs A) {
   using Ly = Lay<D, MT, NST>;
   constexpr int NTH = 64 * MT;
   constexpr int RS = Ly::RS;
@@ -209,13 +213,14 @@ __global__ void __launch_bounds__(64 * MT, 1) verify_kernel(const __grid_constan
       const uint32_t Vt = Kt + TK * RS;
       const int* slot = idxs + (i % (NST + 1)) * TK;
       const bool blk = (ta + i) >= ctx_tiles;
-      const int kb0 = 32 * half;   // first key of this warp's half
+      const int kb0 = TKH * half;   // first key of this warp's half
+      constexpr int NJ = TKH / 8;   // 8-key n-tiles per warp
 
-      float sacc[4][4];
+      float sacc[NJ][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+      for (int j = 0; j < NJ; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < NJ; ++j) {
 #pragma unroll
         for (int ks = 0; ks < NKS; ks += 2) {
           uint32_t b0, b1, b2, b3;
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(64 * MT, 1) verify_kernel(const __grid_constan
         }
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < NJ; ++j) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int key = kb0 + 8 * j + 2 * (lane & 3) + (e & 1);
@@ -240,7 +245,7 @@ __global__ void __launch_bounds__(64 * MT, 1) verify_kernel(const __grid_constan
       for (int hi = 0; hi < 2; ++hi) {
         float mx = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fmaxf(sacc[j][2 * hi], sacc[j][2 * hi + 1]));
+        for (int j = 0; j < NJ; ++j) mx = fmaxf(mx, fmaxf(sacc[j][2 * hi], sacc[j][2 * hi + 1]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         const float mnew = fmaxf(mrow[hi], mx);
@@ -249,7 +254,7 @@ __global__ void __launch_bounds__(64 * MT, 1) verify_kernel(const __grid_constan
         mrow[hi] = mnew;
         float ls = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < NJ; ++j) {
 #pragma unroll
           for (int e = 2 * hi; e < 2 * hi + 2; ++e) {
             const float p = bf16_round(exp2f(sacc[j][e] - basev));
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(64 * MT, 1) verify_kernel(const __grid_constan
         }
       }
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
+      for (int kk = 0; kk < NJ / 2; ++kk) {
         const uint32_t a0 = pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]);
         const uint32_t a1 = pack_bf16(sacc[2 * kk][2], sacc[2 * kk][3]);
         const uint32_t a2 = pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
@@ -388,13 +393,42 @@ __global__ void __launch_bounds__(64 * MT, 1) verify_kernel(const __grid_constan
 
 template <int D, int MT>
 cudaError_t launch_t(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t stream) {
-  constexpr int NST = 4;
-  auto kern = verify_kernel<D, MT, NST>;
-  const size_t smem = Lay<D, MT, NST>::total;
+  auto kern = verify_kernel<D, MT, NSTAGE>;
+  const size_t smem = Lay<D, MT, NSTAGE>::total;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   kern<<<pl.grid, 64 * MT, smem, stream>>>(a);
   return cudaGetLastError();
+}
+
+template <int D, int MT>
+int occupancy_t() {
+  int n = 0;
+  auto kern = verify_kernel<D, MT, NSTAGE>;
+  const size_t smem = Lay<D, MT, NSTAGE>::total;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    return 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 64 * MT, smem) != cudaSuccess) return 1;
+  return n > 0 ? n : 1;
+}
+
+template <int D>
+int occupancy_mt(int MT) {
+  static int cache[9] = {};
+  if (MT < 1 || MT > 8) return 1;
+  if (!cache[MT]) {
+    switch (MT) {
+      case 1: cache[MT] = occupancy_t<D, 1>(); break;
+      case 2: cache[MT] = occupancy_t<D, 2>(); break;
+      case 3: cache[MT] = occupancy_t<D, 3>(); break;
+      case 4: cache[MT] = occupancy_t<D, 4>(); break;
+      case 5: cache[MT] = occupancy_t<D, 5>(); break;
+      case 6: cache[MT] = occupancy_t<D, 6>(); break;
+      case 7: cache[MT] = occupancy_t<D, 7>(); break;
+      default: cache[MT] = occupancy_t<D, 8>(); break;
+    }
+  }
+  return cache[MT];
 }
 
 template <int D>
@@ -420,13 +454,15 @@ VerifyLaunch verify_plan(int D, int NQ, int nkeys_cap, int B, int hkv, int n_lay
   VerifyLaunch pl{};
   pl.D = D;
   pl.MT = (NQ + 15) / 16;
-  pl.NST = 4;
+  pl.NST = NSTAGE;
   pl.ctx_tiles = (nkeys_cap + TK - 1) / TK;
   pl.tiles_u = pl.ctx_tiles + 1;
   pl.units = (long long)B * hkv * n_layers;
   pl.total = pl.units * pl.tiles_u;
-  // one CTA per SM (about 150 KB of shared memory each)
-  long long grid = num_sms > 0 ? num_sms : kVerifyGridMax;
+  // as many CTAs as can be resident (several per SM)
+  int occ = 1;
+  if (num_sms > 0) occ = (D == 128) ? occupancy_mt<128>(pl.MT) : occupancy_mt<64>(pl.MT);
+  long long grid = num_sms > 0 ? (long long)num_sms * occ : kVerifyGridMax;
   if (grid > kVerifyGridMax) grid = kVerifyGridMax;
   if (grid > pl.total) grid = pl.total;
   pl.grid = int(grid);

@@ -46,12 +46,12 @@ def test_score_ragged_lengths_multi_batch():
     assert_importance(imp, c.oracle_score(), c.x.seq_len)
 
 
-def test_score_sixteen_cta_cluster_and_spill():
-    """Long caches: the plan moves to 16-CTA clusters, then to logits in the
-    workspace when they no longer fit on chip."""
-    for L in (40000, 140000):
-        wl = WORKLOADS["tiny"].with_(L=L, n_planted=16)
-        c = Case(wl)
+def test_score_long_caches_in_sequence_groups():
+    """Long caches and batches whose logits exceed the L2 budget are scored in
+    groups of sequences (here 5 sequences of up to 2^20 - 64 positions)."""
+    for L, B in ((40000, 1), (140000, 2), ((1 << 20) - 64, 5)):
+        wl = WORKLOADS["tiny"].with_(L=L, B=B, n_planted=16)
+        c = Case(wl, seq_len=[L - 777 * i for i in range(B)])
         imp = dk.dustin_score(c.p, c.draft, c.target, wl.srh, c.seq)
         assert_importance(imp, c.oracle_score(), c.x.seq_len)
 

@@ -48,12 +48,11 @@ def test_noalloc_matches_workspace_score_twice(name):
 
 
 def test_noalloc_rejects_oversize():
-    """Scratch beyond the array's 16 MiB (here 2 KV-head partial maps x 4
-    sequences x 2^20 positions x 4 bytes = 32 MiB) is refused with
-    DUSTIN_ERANGE before any launch."""
+    """Scratch beyond the array's 16 MiB is refused with DUSTIN_ERANGE before
+    any launch: here one sequence alone needs 18 pairs x 2^20 positions x 4
+    bytes = 72 MiB of logits."""
     c = Case(WORKLOADS["tiny"])
     big = dk.Params(1, 1 << 20, 4, 4, 32, 32, 128)
-    big.B = 4
     imp = torch.empty((1, 2, 16), dtype=torch.float32, device="cuda")
     with pytest.raises(dk.DustinError) as e:
         dk.dustin_score_noalloc(big, c.draft, c.target, c.wl.srh, c.seq, importance=imp)
