@@ -174,4 +174,12 @@ __device__ __forceinline__ float bf16_round(float x) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// 2^x with the hardware approximation (ex2.approx.ftz: relative error about
+// 2^-22, flushes denormal results to zero; ex2(-inf) = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 }  // namespace dustin

@@ -55,6 +55,7 @@ __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// Merges two (reference, sum of 2^(x - reference)) statistics.
 __device__ __forceinline__ void stat_merge(float& m, float& s, float m2, float s2) {
   const float M = fmaxf(m, m2);
   if (M == -INFINITY) return;
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
     // ----------------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
+      int cached_bl = -1, L = 0;    // seq_len is read once per sequence, not per tile
       for (long long t = t0; t < t1; ++t) {
         const int i = int(t - t0);
         const int st = i % kStages;
@@ -111,8 +113,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
         decode_tile(A, t, s, bl, tile);
         const ScoreSlab& S = A.slab[s];
         const int b = A.b0 + bl;
-        int L = A.seq_len[b];
-        if (L < 0 || L > A.Lcap) L = 0;
+        if (bl != cached_bl) {
+          cached_bl = bl;
+          L = A.seq_len[b];
+          if (L < 0 || L > A.Lcap) L = 0;
+        }
         const int r0 = tile * S.rows;
         if (r0 >= L) {
           mbar_arrive(&full[st]);   // nothing to load: an empty tile
@@ -136,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
     // -------------------------------------------------------------- consumers
     uint32_t qb[NT][kMaxKs][2];
     float rm[NT][2], rs[NT][2];   // online (max, sum) per pair column
-    int cur_s = -1, cur_bl = -1;
+    int cur_s = -1, cur_bl = -1, L = 0;
     for (long long t = t0; t < t1; ++t) {
       const int i = int(t - t0);
       const int st = i % kStages;
@@ -145,15 +150,15 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
       const ScoreSlab& S = A.slab[s];
       const int D = S.D;
       const int b = A.b0 + bl;
-      int L = A.seq_len[b];
-      if (L < 0 || L > A.Lcap) {
-        if (lane == 0 && warp == 0 && tile == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
-        L = 0;
-      }
       if (s != cur_s || bl != cur_bl) {
-        // new segment: load Q^T fragments (d x pairs) of this slab and sequence
+        // new segment: length, and Q^T fragments (d x pairs) of this slab and sequence
         cur_s = s;
         cur_bl = bl;
+        L = A.seq_len[b];
+        if (L < 0 || L > A.Lcap) {
+          if (lane == 0 && warp == 0 && tile == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
+          L = 0;
+        }
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           const int p = 8 * j + (lane >> 2);
@@ -183,7 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
       if (ok && r0 < L) {
         const uint32_t sb = smem_u32(ring + size_t(st) * kTileBytes);
         const int nmt = (D == 128) ? 1 : 2;
+        const int nt = (S.npairs + 7) >> 3;          // n-tiles this slab needs
         const float scale = kLog2e * rsqrtf(float(D));
+        const bool full_tile = r0 + S.rows <= L;
         float* lrow = A.logits + S.logit_off + size_t(bl) * S.npairs * A.LSP;
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi) {
@@ -200,27 +207,30 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
               ldmatrix_x4(a0, a1, a2, a3, tile_addr(sb, D, arow, 16 * ks + 8 * (lane >> 4)));
 #pragma unroll
               for (int j = 0; j < NT; ++j)
-                mma_bf16_16816(c[j], a0, a1, a2, a3, qb[j][ks][0], qb[j][ks][1]);
+                if (j < nt) mma_bf16_16816(c[j], a0, a1, a2, a3, qb[j][ks][0], qb[j][ks][1]);
             }
           }
           const int pos_lo = r0 + rb + (lane >> 2);
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
+            if (j >= nt) break;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int pair = 8 * j + 2 * (lane & 3) + (e & 1);
               const int pos = pos_lo + ((e >> 1) << 3);
-              if (pair < S.npairs && pos < L) {
+              if (pair < S.npairs && (full_tile || pos < L)) {
                 const float v = c[j][e] * scale;
                 lrow[size_t(pair) * A.LSP + pos] = v;
+                // online sum of 2^(v - m) with a lazily raised reference m:
+                // the reference only moves when v passes it by more than 8,
+                // so the common path is one ex2 and one add
                 float& m = rm[j][e & 1];
                 float& sm = rs[j][e & 1];
-                if (v > m) {
-                  sm = sm * exp2f(m - v) + 1.f;
+                if (v > m + 8.f) {
+                  sm *= fast_exp2(m - v);
                   m = v;
-                } else {
-                  sm += exp2f(v - m);
                 }
+                sm += fast_exp2(v - m);
               }
             }
           }
@@ -273,62 +283,87 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
 }
 
 __global__ void __launch_bounds__(256) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
+  // one row per (slab, pair): logits offset, merged max M and 1 / sum
+  __shared__ long long roff[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
   __shared__ float Mg[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
   __shared__ float Ig[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
+  __shared__ int nrow[2];
   const int bl = blockIdx.y;
   const int b = A.b0 + bl;
   int L = A.seq_len[b];
   if (L < 0 || L > A.Lcap) L = 0;
   const int G = A.grid;
+  if (threadIdx.x < 2) {
+    int n = 0;
+    for (int s = 0; s < A.n_slab; ++s)
+      if (A.slab[s].channel == int(threadIdx.x)) n += A.slab[s].npairs;
+    nrow[threadIdx.x] = n;
+  }
   for (int q = threadIdx.x; q < A.n_slab * DUSTIN_MAX_PAIRS; q += blockDim.x) {
     const int s = q / DUSTIN_MAX_PAIRS, p = q - s * DUSTIN_MAX_PAIRS;
     const ScoreSlab& S = A.slab[s];
-    float m = -INFINITY, sm = 0.f;
-    if (p < S.npairs) {
-      const long long first = A.slab_start[s] + (long long)bl * S.tiles;
-      const int n_seg = cta_of(first + S.tiles - 1, A.total, G) - cta_of(first, A.total, G) + 1;
-      const float* slots = A.stats + (size_t(s) * A.nb + bl) * A.max_seg * size_t(A.np_max) * 2;
-      for (int g = 0; g < n_seg; ++g)
-        stat_merge(m, sm, __ldcg(slots + (size_t(g) * A.np_max + p) * 2),
-                   __ldcg(slots + (size_t(g) * A.np_max + p) * 2 + 1));
+    if (p >= S.npairs) continue;
+    // row index: channel-major, slabs in order, then pairs
+    int r = 0;
+    for (int s2 = 0; s2 < A.n_slab; ++s2) {
+      if (A.slab[s2].channel < S.channel || (A.slab[s2].channel == S.channel && s2 < s))
+        r += A.slab[s2].npairs;
     }
-    Mg[q] = m;
-    Ig[q] = sm > 0.f ? 1.f / sm : 0.f;
+    r += p;
+    float m = -INFINITY, sm = 0.f;
+    const long long first = A.slab_start[s] + (long long)bl * S.tiles;
+    const int n_seg = cta_of(first + S.tiles - 1, A.total, G) - cta_of(first, A.total, G) + 1;
+    const float* slots = A.stats + (size_t(s) * A.nb + bl) * A.max_seg * size_t(A.np_max) * 2;
+    for (int g = 0; g < n_seg; ++g)
+      stat_merge(m, sm, __ldcg(slots + (size_t(g) * A.np_max + p) * 2),
+                 __ldcg(slots + (size_t(g) * A.np_max + p) * 2 + 1));
+    roff[r] = S.logit_off + (long long)(size_t(bl) * S.npairs + p) * A.LSP;
+    Mg[r] = m;
+    Ig[r] = sm > 0.f ? 1.f / sm : 0.f;
   }
   __syncthreads();
   const int base = blockIdx.x * kNormChunk;
+  // each thread: 4 consecutive positions (one float4 per logits row; rows are
+  // padded to a multiple of 32 floats, so the loads are aligned and in bounds)
+  const int pos = base + 4 * threadIdx.x;
+  constexpr int kBatch = 8;
+  int r0 = 0;
   for (int c = 0; c < 2; ++c) {
-    float* out = A.importance + (size_t(b) * 2 + c) * A.Lcap;
-    for (int pos = base + threadIdx.x; pos < base + kNormChunk && pos < A.Lcap; pos += blockDim.x) {
-      float acc = 0.f;
-      if (pos < L) {
-        for (int s = 0; s < A.n_slab; ++s) {
-          const ScoreSlab& S = A.slab[s];
-          if (S.channel != c) continue;
-          const float* lrow = A.logits + S.logit_off + size_t(bl) * S.npairs * A.LSP + pos;
-          for (int p = 0; p < S.npairs; ++p) {
-            const float l = __ldcs(lrow + size_t(p) * A.LSP);
-            acc += exp2f(l - Mg[s * DUSTIN_MAX_PAIRS + p]) * Ig[s * DUSTIN_MAX_PAIRS + p];
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int rn = nrow[c];
+    if (pos < L) {
+      for (int r = 0; r < rn; r += kBatch) {
+        float4 l[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+          if (r + u < rn) l[u] = __ldcs(reinterpret_cast<const float4*>(A.logits + roff[r0 + r + u] + pos));
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (r + u < rn) {
+            const float M = Mg[r0 + r + u], I = Ig[r0 + r + u];
+            acc[0] += fast_exp2(l[u].x - M) * I;
+            acc[1] += fast_exp2(l[u].y - M) * I;
+            acc[2] += fast_exp2(l[u].z - M) * I;
+            acc[3] += fast_exp2(l[u].w - M) * I;
           }
         }
       }
-      out[pos] = acc;
     }
+    r0 += rn;
+    float* out = A.importance + (size_t(b) * 2 + c) * A.Lcap;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (pos + e < A.Lcap) out[pos + e] = (pos + e < L) ? acc[e] : 0.f;
   }
   // the logits of this chunk are dead: drop them from L2 without write-back
   __syncthreads();
   const int lines_per_row = kNormChunk * 4 / 128;
-  int nrows = 0;
-  for (int s = 0; s < A.n_slab; ++s) nrows += A.slab[s].npairs;
+  const int nrows = nrow[0] + nrow[1];
   for (int q = threadIdx.x; q < nrows * lines_per_row; q += blockDim.x) {
-    int r = q / lines_per_row;
+    const int r = q / lines_per_row;
     const int ln = q - r * lines_per_row;
-    int s = 0;
-    while (r >= A.slab[s].npairs) r -= A.slab[s++].npairs;
-    const ScoreSlab& S = A.slab[s];
-    const size_t off = S.logit_off + (size_t(bl) * S.npairs + r) * A.LSP + base + ln * 32;
     if (base + ln * 32 < A.LSP)
-      asm volatile("discard.global.L2 [%0], 128;" ::"l"(A.logits + off) : "memory");
+      asm volatile("discard.global.L2 [%0], 128;" ::"l"(A.logits + roff[r] + base + ln * 32) : "memory");
   }
 }
 

@@ -5,12 +5,19 @@
 // signal).
 //
 // One 1024-thread CTA per sequence.  Importance values are non-negative fp32,
-// so their bit patterns order like the values; each tier is a radix select of
-// the threshold key T over four 8-bit digits (per-digit histograms built with
-// warp-aggregated shared-memory atomics), followed by an order-preserving
-// compaction that takes every key > T and the lowest-index keys == T until the
-// tier is full.  Keys are staged in shared memory when the cache capacity
-// allows; the draft tier is recorded in a bitmap that the target tier skips.
+// so their bit patterns order like the values.  Each tier finds the exact
+// threshold key T of its top-cnt (descending key, ties to the lower index):
+//   1. a 4096-bin histogram of the top 12 bits (sign, exponent, 3 mantissa
+//      bits) of every candidate key -- fine enough that the shared-memory
+//      atomics rarely collide -- gives the bin that holds the cnt-th key;
+//   2. the keys of that bin are gathered into a small list and two 10-bit
+//      radix passes over the list give T and how many keys equal to T to take;
+//   3. an order-preserving compaction writes every key > T and the
+//      lowest-index keys == T, ascending.
+// If the threshold bin holds more keys than the list can take (heavy ties), the
+// refinement runs over all candidates instead.  Keys are staged in shared
+// memory when the cache capacity allows; the draft tier is recorded in a
+// bitmap that the target tier skips.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -20,13 +27,19 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+constexpr int kBins1 = 4096;      // top 12 bits
+constexpr int kBins2 = 1024;      // 10 bits
+constexpr int kCandCap = 8192;
 constexpr size_t kSmemBudget = 200 * 1024;
 
 struct SelShared {
-  int hist[256];
+  int hist[kBins1];
+  uint32_t cand[kCandCap];
+  int wsum[kWarps];
   int wgt[kWarps];
   int weq[kWarps];
-  int digit;
+  int ncand;
+  int bin;
   int need;
 };
 
@@ -52,70 +65,111 @@ struct KeySrc {
   }
 };
 
-// Selects the top `cnt` candidates of [u0, u1) (minus bits set in `excl`) by
-// (key descending, index ascending), writes them ascending to out[0..cnt) and
-// sets their bits in `setbits` when given.  Whole-block call.
+__device__ __forceinline__ bool excluded(const uint32_t* excl, int i) {
+  return excl && ((excl[i >> 5] >> (i & 31)) & 1u);
+}
+
+// Over the histogram in descending bin order: the bin holding the need-th key
+// and how many keys of that bin are still needed.  Whole-block call.
+__device__ void find_bin(SelShared& sh, int nbins, int need) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = nbins / kThreads;   // bins per thread (4 or 1)
+  int local = 0;
+  for (int k = 0; k < q; ++k) local += sh.hist[nbins - 1 - (tid * q + k)];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sh.wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = sh.wsum[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    sh.wsum[lane] = wi - w;   // exclusive prefix of the warp sums
+  }
+  __syncthreads();
+  const int before = sh.wsum[warp] + incl - local;
+  if (before < need && need <= before + local) {
+    int acc = before;
+    for (int k = 0; k < q; ++k) {
+      const int bin = nbins - 1 - (tid * q + k);
+      const int h = sh.hist[bin];
+      if (acc + h >= need) {
+        sh.bin = bin;
+        sh.need = need - acc;
+        break;
+      }
+      acc += h;
+    }
+  }
+  __syncthreads();
+}
+
+// Top `cnt` candidates of [u0, u1) minus `excl` by (key desc, index asc):
+// written ascending to out[0..cnt), bits set in `setbits` when given.
 __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* excl, int cnt,
                             int32_t* out, uint32_t* setbits, SelShared& sh) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (cnt <= 0 || u1 <= u0) return;
-  uint32_t prefix = 0, pmask = 0;
-  int need = cnt;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    if (tid < 256) sh.hist[tid] = 0;
-    __syncthreads();
-    for (int base = u0; base < u1; base += kThreads) {
-      const int i = base + tid;
-      bool c = i < u1 && !(excl && ((excl[i >> 5] >> (i & 31)) & 1u));
-      uint32_t kv = 0;
-      if (c) {
-        kv = key(i);
-        c = (kv & pmask) == prefix;
-      }
-      const uint32_t dg = c ? ((kv >> shift) & 255u) : 256u;
-      const uint32_t peers = __match_any_sync(0xffffffffu, dg);
-      if (c && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[dg], __popc(peers));
+
+  // 1. top-12-bit histogram
+  for (int b = tid; b < kBins1; b += kThreads) sh.hist[b] = 0;
+  if (tid == 0) sh.ncand = 0;
+  __syncthreads();
+  for (int i = u0 + tid; i < u1; i += kThreads)
+    if (!excluded(excl, i)) atomicAdd(&sh.hist[key(i) >> 20], 1);
+  __syncthreads();
+  find_bin(sh, kBins1, cnt);
+  const uint32_t b1 = uint32_t(sh.bin);
+  int need = sh.need;
+
+  // 2. gather the keys of the threshold bin
+  for (int i = u0 + tid; i < u1; i += kThreads) {
+    if (excluded(excl, i)) continue;
+    const uint32_t kv = key(i);
+    if ((kv >> 20) == b1) {
+      const int slot = atomicAdd(&sh.ncand, 1);
+      if (slot < kCandCap) sh.cand[slot] = kv;
     }
+  }
+  __syncthreads();
+  const int ncand = sh.ncand;
+  const bool listed = ncand <= kCandCap;
+  uint32_t prefix = b1 << 20;
+  // two 10-bit passes over the list (or over all candidates when it overflowed)
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = 10 - 10 * pass;
+    const uint32_t hi_mask = 0xFFFFFFFFu << (shift + 10);
     __syncthreads();
-    if (warp == 0) {
-      // lane l covers digits 255-8l down to 248-8l
-      int cnt8[8];
-      int local = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        cnt8[q] = sh.hist[255 - 8 * lane - q];
-        local += cnt8[q];
+    for (int b = tid; b < kBins2; b += kThreads) sh.hist[b] = 0;
+    __syncthreads();
+    if (listed) {
+      for (int c = tid; c < ncand; c += kThreads) {
+        const uint32_t kv = sh.cand[c];
+        if ((kv & hi_mask) == prefix) atomicAdd(&sh.hist[(kv >> shift) & 1023u], 1);
       }
-      int incl = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int before = incl - local;
-      if (before < need && need <= incl) {
-        int acc = before;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (acc + cnt8[q] >= need) {
-            sh.digit = 255 - 8 * lane - q;
-            sh.need = need - acc;
-            break;
-          }
-          acc += cnt8[q];
-        }
+    } else {
+      for (int i = u0 + tid; i < u1; i += kThreads) {
+        if (excluded(excl, i)) continue;
+        const uint32_t kv = key(i);
+        if ((kv & hi_mask) == prefix) atomicAdd(&sh.hist[(kv >> shift) & 1023u], 1);
       }
     }
     __syncthreads();
-    prefix |= uint32_t(sh.digit) << shift;
-    pmask |= 255u << shift;
+    find_bin(sh, kBins2, need);
+    prefix |= uint32_t(sh.bin) << shift;
     need = sh.need;
-    __syncthreads();
   }
   const uint32_t T = prefix;
 
-  // order-preserving compaction over 32-aligned warp chunks
+  // 3. order-preserving compaction over 32-aligned warp chunks
   const int a0 = u0 & ~31;
   const int span = u1 - a0;
   const int chunk = (((span + kWarps - 1) / kWarps) + 31) & ~31;
@@ -124,8 +178,8 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
   int ngt = 0, neq = 0;
   for (int g0 = w0; g0 < w1; g0 += 32) {
     const int i = g0 + lane;
-    bool c = i >= u0 && i < w1 && !(excl && ((excl[i >> 5] >> (i & 31)) & 1u));
-    uint32_t kv = c ? key(i) : 0u;
+    const bool c = i >= u0 && i < w1 && !excluded(excl, i);
+    const uint32_t kv = c ? key(i) : 0u;
     ngt += __popc(__ballot_sync(0xffffffffu, c && kv > T));
     neq += __popc(__ballot_sync(0xffffffffu, c && kv == T));
   }
@@ -144,8 +198,8 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
   const uint32_t lt = (1u << lane) - 1u;
   for (int g0 = w0; g0 < w1; g0 += 32) {
     const int i = g0 + lane;
-    bool c = i >= u0 && i < w1 && !(excl && ((excl[i >> 5] >> (i & 31)) & 1u));
-    uint32_t kv = c ? key(i) : 0u;
+    const bool c = i >= u0 && i < w1 && !excluded(excl, i);
+    const uint32_t kv = c ? key(i) : 0u;
     const bool isgt = c && kv > T;
     const bool iseq = c && kv == T;
     const uint32_t eqb = __ballot_sync(0xffffffffu, iseq);
@@ -160,8 +214,9 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
 }
 
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_constant__ SelectArgs A) {
-  __shared__ SelShared sh;
   extern __shared__ __align__(16) unsigned char dsm[];
+  SelShared& sh = *reinterpret_cast<SelShared*>(dsm);
+  unsigned char* rest = dsm + ((sizeof(SelShared) + 15) & ~size_t(15));
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   int32_t* out = A.out + size_t(b) * A.k;
@@ -183,8 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   for (int j = tid; j < nP; j += kThreads) out[j] = j < s_eff ? j : w0 + (j - s_eff);
 
   const int nwords = (A.Lcap + 31) >> 5;
-  uint32_t* keys = A.cache_keys ? reinterpret_cast<uint32_t*>(dsm) : nullptr;
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(dsm + (A.cache_keys ? size_t(A.Lcap) * 4 : 0));
+  uint32_t* keys = A.cache_keys ? reinterpret_cast<uint32_t*>(rest) : nullptr;
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(rest + (A.cache_keys ? size_t(A.Lcap) * 4 : 0));
   for (int w = tid; w < nwords; w += kThreads) bitmap[w] = 0u;
 
   for (int ch = 0; ch < 2; ++ch) {
@@ -203,12 +258,13 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
 }  // namespace
 
 int select_cache_keys(int Lcap) {
-  const size_t need = size_t(Lcap) * 4 + size_t((Lcap + 31) / 32) * 4;
+  const size_t need = sizeof(SelShared) + 16 + size_t(Lcap) * 4 + size_t((Lcap + 31) / 32) * 4;
   return need <= kSmemBudget ? 1 : 0;
 }
 
 size_t select_smem_bytes(int Lcap, int cache_keys) {
-  return (cache_keys ? size_t(Lcap) * 4 : 0) + size_t((Lcap + 31) / 32) * 4;
+  return ((sizeof(SelShared) + 15) & ~size_t(15)) + (cache_keys ? size_t(Lcap) * 4 : 0) +
+         size_t((Lcap + 31) / 32) * 4;
 }
 
 cudaError_t select_launch(const SelectArgs& a, cudaStream_t stream) {

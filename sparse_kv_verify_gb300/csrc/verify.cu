@@ -250,14 +250,14 @@ __global__ void __launch_bounds__(64 * MT) verify_kernel(const __grid_constant__
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         const float mnew = fmaxf(mrow[hi], mx);
         const float basev = (mnew == -INFINITY) ? 0.f : mnew;
-        const float alpha = exp2f(mrow[hi] - basev);
+        const float alpha = fast_exp2(mrow[hi] - basev);
         mrow[hi] = mnew;
         float ls = 0.f;
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
 #pragma unroll
           for (int e = 2 * hi; e < 2 * hi + 2; ++e) {
-            const float p = bf16_round(exp2f(sacc[j][e] - basev));
+            const float p = bf16_round(fast_exp2(sacc[j][e] - basev));
             sacc[j][e] = p;
             ls += p;
           }
