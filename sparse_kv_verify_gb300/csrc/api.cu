@@ -83,18 +83,36 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 4-D map over a cache view: dims (d, Lcap, hkv, B); box 64 x 128 x 1 x 1 with
-// the 128-byte swizzle that the score kernel's ldmatrix addressing expects.
-bool encode_cache_map(CUtensorMap* m, const dustin_kv& v, int Lcap, int B) {
+// TMA map over a cache view with box 64 columns x 128 rows and the 128-byte
+// swizzle that the score kernel's ldmatrix addressing expects.  A densely
+// packed cache [B][hkv][Lcap][d] is described as 2-D rows [B*hkv*Lcap][d]
+// (rows of a box that run past one head's Lcap positions are past seq_len and
+// masked); any other strides use a 4-D map (d, Lcap, hkv, B).  *rank is 2 or 4.
+bool encode_cache_map(CUtensorMap* m, const dustin_kv& v, int Lcap, int B, int* rank) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[4] = {cuuint64_t(v.d), cuuint64_t(Lcap), cuuint64_t(v.hkv), cuuint64_t(B)};
-  cuuint64_t strides[3] = {cuuint64_t(v.sl) * 2, cuuint64_t(v.sh) * 2, cuuint64_t(v.sb) * 2};
-  cuuint32_t box[4] = {64, 128, 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v.ptr, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const bool packed = v.sl == v.d && v.sh == int64_t(Lcap) * v.d && v.sb == int64_t(v.hkv) * v.sh &&
+                      int64_t(B) * v.hkv * Lcap < (int64_t(1) << 31) - 256;
+  CUresult r;
+  if (packed) {
+    cuuint64_t dims[2] = {cuuint64_t(v.d), cuuint64_t(B) * v.hkv * Lcap};
+    cuuint64_t strides[1] = {cuuint64_t(v.sl) * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v.ptr, dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    *rank = 2;
+  } else {
+    cuuint64_t dims[4] = {cuuint64_t(v.d), cuuint64_t(Lcap), cuuint64_t(v.hkv), cuuint64_t(B)};
+    cuuint64_t strides[3] = {cuuint64_t(v.sl) * 2, cuuint64_t(v.sh) * 2, cuuint64_t(v.sb) * 2};
+    cuuint32_t box[4] = {64, 128, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v.ptr, dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    *rank = 4;
+  }
   return r == CUDA_SUCCESS;
 }
 
@@ -237,11 +255,17 @@ int launch_score(const dustin_params* p, const dustin_signal* draft, const dusti
                  cudaStream_t stream, cudaEvent_t mid = nullptr) {
   static thread_local ScoreArgs a;   // large (tensor maps): keep it off the stack
   std::memset(&a, 0, sizeof(a));
+  int rank[DUSTIN_MAX_SRH];
   for (int c = 0; c < pl.n_cache; ++c) {
     const dustin_signal* s = sig_of(pl.cache_channel[c], draft, target);
-    if (!encode_cache_map(&a.map[c], s->k[pl.cache_layer[c]], p->Lcap, p->B)) return DUSTIN_ECUDA;
+    if (!encode_cache_map(&a.map[c], s->k[pl.cache_layer[c]], p->Lcap, p->B, &rank[c]))
+      return DUSTIN_ECUDA;
   }
-  for (int t = 0; t < pl.n_slab; ++t) a.slab[t] = pl.slab[t];
+  for (int t = 0; t < pl.n_slab; ++t) {
+    a.slab[t] = pl.slab[t];
+    const dustin_signal* s = sig_of(pl.slab[t].channel, draft, target);
+    a.slab[t].row2d = rank[pl.slab[t].cache] == 2 ? s->k[pl.cache_layer[pl.slab[t].cache]].hkv : 0;
+  }
   a.B = p->B;
   a.Lcap = p->Lcap;
   a.LSP = pl.LSP;

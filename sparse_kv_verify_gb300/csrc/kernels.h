@@ -69,6 +69,7 @@ struct ScoreSlab {
   int rows;      // positions per tile (128 for d = 128, 256 for d = 64)
   int tiles;     // tiles per sequence: ceil(Lcap / rows)
   long long logit_off;   // float offset of this slab's logits [nb][npairs][LSP]
+  int row2d;     // 0: 4-D map; else 2-D map over packed rows, value = hkv of the cache
   const uint16_t* q;     // [B][nq][hq][D]
 };
 

@@ -63,7 +63,8 @@ __device__ __forceinline__ void stat_merge(float& m, float& s, float m2, float s
   m = M;
 }
 
-// Slab and sequence of flattened tile t of the group.
+// Slab, sequence and tile of flattened tile t of the group (one division:
+// called once per CTA; the walk then advances incrementally).
 __device__ __forceinline__ void decode_tile(const ScoreArgs& A, long long t, int& s, int& bl,
                                             int& tile) {
   s = 0;
@@ -71,6 +72,74 @@ __device__ __forceinline__ void decode_tile(const ScoreArgs& A, long long t, int
   const long long off = t - A.slab_start[s];
   bl = int(off / A.slab[s].tiles);
   tile = int(off - (long long)bl * A.slab[s].tiles);
+}
+
+template <int D, int NTU, int NT>
+__device__ __forceinline__ void consume_segment(const uint32_t (&qb)[NT][kMaxKs][2], float (&rm)[NT][2],
+                                                float (&rs)[NT][2], unsigned char* ring,
+                                                uint64_t* full, uint64_t* empty, int i0, int n,
+                                                int r0, int L, int npairs, float* lrow, int LSP,
+                                                int* err, volatile int* abort_flag) {
+  constexpr int ROWS = (D == 128) ? kBoxRows : 2 * kBoxRows;
+  constexpr int NMT = (D == 128) ? 1 : 2;
+  constexpr int NKS = D / 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float scale = kLog2e * rsqrtf(float(D));
+  for (int k = 0; k < n; ++k, r0 += ROWS) {
+    const int i = i0 + k;
+    const int st = i % kStages;
+    const bool ok = mbar_wait(&full[st], (i / kStages) & 1, err, abort_flag);
+    if (ok && r0 < L) {
+      const uint32_t sb = smem_u32(ring + size_t(st) * kTileBytes);
+      const bool full_tile = r0 + ROWS <= L;
+#pragma unroll
+      for (int mi = 0; mi < NMT; ++mi) {
+        const int rb = 16 * warp + kBoxRows * mi;
+        float c[NTU][4];
+#pragma unroll
+        for (int j = 0; j < NTU; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+        const int arow = rb + (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+        for (int ks = 0; ks < NKS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4(a0, a1, a2, a3, tile_addr(sb, D, arow, 16 * ks + 8 * (lane >> 4)));
+#pragma unroll
+          for (int j = 0; j < NTU; ++j)
+            mma_bf16_16816(c[j], a0, a1, a2, a3, qb[j][ks][0], qb[j][ks][1]);
+        }
+        if (mi == NMT - 1) {   // the tile's shared memory is no longer read
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        const int pos_lo = r0 + rb + (lane >> 2);
+#pragma unroll
+        for (int j = 0; j < NTU; ++j) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int pair = 8 * j + 2 * (lane & 3) + (e & 1);
+            const int pos = pos_lo + ((e >> 1) << 3);
+            if (pair < npairs && (full_tile || pos < L)) {
+              const float v = c[j][e] * scale;
+              lrow[size_t(pair) * LSP + pos] = v;
+              // online sum of 2^(v - m) with a lazily raised reference m: the
+              // reference only moves when v passes it by more than 8, so the
+              // common path is one ex2 and one add
+              float& m = rm[j][e & 1];
+              float& sm = rs[j][e & 1];
+              if (v > m + 8.f) {
+                sm *= fast_exp2(m - v);
+                m = v;
+              }
+              sm += fast_exp2(v - m);
+            }
+          }
+        }
+      }
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+  }
 }
 
 template <int NT>
@@ -97,186 +166,159 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
     fence_barrier_init();
   }
   __syncthreads();
+  if (t0 >= t1) return;
+
+  // The CTA's range as segments: (slab s, sequence bl, first tile, count).
+  int s0, bl0, tile0;
+  decode_tile(A, t0, s0, bl0, tile0);
 
   if (warp == kConsumers) {
     // ----------------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int cached_bl = -1, L = 0;    // seq_len is read once per sequence, not per tile
-      for (long long t = t0; t < t1; ++t) {
-        const int i = int(t - t0);
-        const int st = i % kStages;
-        if (i >= kStages) {
-          if (!mbar_wait(&empty[st], ((i / kStages) - 1) & 1, A.err, abort_flag)) break;
-        }
-        int s, bl, tile;
-        decode_tile(A, t, s, bl, tile);
+      int s = s0, bl = bl0, tile = tile0;
+      int i = 0;
+      for (long long t = t0; t < t1;) {
         const ScoreSlab& S = A.slab[s];
+        const int n = int(min((long long)(S.tiles - tile), t1 - t));
         const int b = A.b0 + bl;
-        if (bl != cached_bl) {
-          cached_bl = bl;
-          L = A.seq_len[b];
-          if (L < 0 || L > A.Lcap) L = 0;
-        }
-        const int r0 = tile * S.rows;
-        if (r0 >= L) {
-          mbar_arrive(&full[st]);   // nothing to load: an empty tile
-          continue;
-        }
+        int L = A.seq_len[b];
+        if (L < 0 || L > A.Lcap) L = 0;
+        const int D = S.D, rows = S.rows, g = S.g, row2d = S.row2d;
         const CUtensorMap* map = &A.map[S.cache];
-        unsigned char* dst = ring + size_t(st) * kTileBytes;
-        if (S.D == 128) {
-          mbar_arrive_expect_tx(&full[st], 2 * kBoxBytes);
-          tma_load_4d(dst, map, 0, r0, S.g, b, &full[st], pol);
-          tma_load_4d(dst + kBoxBytes, map, 64, r0, S.g, b, &full[st], pol);
-        } else {
-          const bool two = r0 + kBoxRows < L;
-          mbar_arrive_expect_tx(&full[st], two ? 2 * kBoxBytes : kBoxBytes);
-          tma_load_4d(dst, map, 0, r0, S.g, b, &full[st], pol);
-          if (two) tma_load_4d(dst + kBoxBytes, map, 0, r0 + kBoxRows, S.g, b, &full[st], pol);
+        const int rbase = row2d ? (b * row2d + g) * A.Lcap : 0;
+        int r0 = tile * rows;
+        bool stop = false;
+        for (int k = 0; k < n; ++k, ++i, r0 += rows) {
+          const int st = i % kStages;
+          if (i >= kStages) {
+            if (!mbar_wait(&empty[st], ((i / kStages) - 1) & 1, A.err, abort_flag)) {
+              stop = true;
+              break;
+            }
+          }
+          if (r0 >= L) {
+            mbar_arrive(&full[st]);   // nothing to load: an empty tile
+            continue;
+          }
+          unsigned char* dst = ring + size_t(st) * kTileBytes;
+          auto load = [&](unsigned char* d, int x, int r) {
+            if (row2d) tma_load_2d(d, map, x, rbase + r, &full[st], pol);
+            else tma_load_4d(d, map, x, r, g, b, &full[st], pol);
+          };
+          if (D == 128) {
+            mbar_arrive_expect_tx(&full[st], 2 * kBoxBytes);
+            load(dst, 0, r0);
+            load(dst + kBoxBytes, 64, r0);
+          } else {
+            const bool two = r0 + kBoxRows < L;
+            mbar_arrive_expect_tx(&full[st], two ? 2 * kBoxBytes : kBoxBytes);
+            load(dst, 0, r0);
+            if (two) load(dst + kBoxBytes, 0, r0 + kBoxRows);
+          }
+        }
+        if (stop) break;
+        t += n;
+        tile = 0;
+        if (++bl == A.nb) {
+          bl = 0;
+          ++s;
         }
       }
     }
   } else {
     // -------------------------------------------------------------- consumers
     uint32_t qb[NT][kMaxKs][2];
-    float rm[NT][2], rs[NT][2];   // online (max, sum) per pair column
-    int cur_s = -1, cur_bl = -1, L = 0;
-    for (long long t = t0; t < t1; ++t) {
-      const int i = int(t - t0);
-      const int st = i % kStages;
-      int s, bl, tile;
-      decode_tile(A, t, s, bl, tile);
+    float rm[NT][2], rs[NT][2];
+    int s = s0, bl = bl0, tile = tile0;
+    int i = 0;
+    for (long long t = t0; t < t1;) {
       const ScoreSlab& S = A.slab[s];
-      const int D = S.D;
+      const int n = int(min((long long)(S.tiles - tile), t1 - t));
       const int b = A.b0 + bl;
-      if (s != cur_s || bl != cur_bl) {
-        // new segment: length, and Q^T fragments (d x pairs) of this slab and sequence
-        cur_s = s;
-        cur_bl = bl;
-        L = A.seq_len[b];
-        if (L < 0 || L > A.Lcap) {
-          if (lane == 0 && warp == 0 && tile == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
-          L = 0;
-        }
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const int p = 8 * j + (lane >> 2);
-          const uint16_t* qrow = nullptr;
-          if (p < S.npairs) {
-            const int hi = p / S.nq, tq = p - (p / S.nq) * S.nq;
-            qrow = S.q + ((size_t(b) * S.nq + tq) * S.hq + S.heads[hi]) * D;
-          }
-#pragma unroll
-          for (int ks = 0; ks < kMaxKs; ++ks) {
-            uint32_t v0 = 0, v1 = 0;
-            if (qrow && ks < (D >> 4)) {
-              v0 = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * (lane & 3));
-              v1 = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * (lane & 3));
-            }
-            qb[j][ks][0] = v0;
-            qb[j][ks][1] = v1;
-          }
-          rm[j][0] = rm[j][1] = -INFINITY;
-          rs[j][0] = rs[j][1] = 0.f;
-        }
+      const int D = S.D, npairs = S.npairs;
+      int L = A.seq_len[b];
+      if (L < 0 || L > A.Lcap) {
+        if (lane == 0 && warp == 0 && tile == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
+        L = 0;
       }
-      // on a give-up the loop keeps running without work so that every warp
-      // still reaches every named barrier below
-      const bool ok = mbar_wait(&full[st], (i / kStages) & 1, A.err, abort_flag);
+      // Q^T fragments (d x pairs) of this slab and sequence; fresh statistics
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const int p = 8 * j + (lane >> 2);
+        const uint16_t* qrow = nullptr;
+        if (p < npairs) {
+          const int hi = p / S.nq, tq = p - (p / S.nq) * S.nq;
+          qrow = S.q + ((size_t(b) * S.nq + tq) * S.hq + S.heads[hi]) * D;
+        }
+#pragma unroll
+        for (int ks = 0; ks < kMaxKs; ++ks) {
+          uint32_t v0 = 0, v1 = 0;
+          if (qrow && ks < (D >> 4)) {
+            v0 = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * (lane & 3));
+            v1 = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * (lane & 3));
+          }
+          qb[j][ks][0] = v0;
+          qb[j][ks][1] = v1;
+        }
+        rm[j][0] = rm[j][1] = -INFINITY;
+        rs[j][0] = rs[j][1] = 0.f;
+      }
+      float* lrow = A.logits + S.logit_off + size_t(bl) * npairs * A.LSP;
+      const int ntu = (npairs + 7) >> 3;
       const int r0 = tile * S.rows;
-      if (ok && r0 < L) {
-        const uint32_t sb = smem_u32(ring + size_t(st) * kTileBytes);
-        const int nmt = (D == 128) ? 1 : 2;
-        const int nt = (S.npairs + 7) >> 3;          // n-tiles this slab needs
-        const float scale = kLog2e * rsqrtf(float(D));
-        const bool full_tile = r0 + S.rows <= L;
-        float* lrow = A.logits + S.logit_off + size_t(bl) * S.npairs * A.LSP;
+#define DUSTIN_SEG(DD, NN)                                                                     \
+  consume_segment<DD, NN, NT>(qb, rm, rs, ring, full, empty, i, n, r0, L, npairs, lrow, A.LSP, \
+                              A.err, abort_flag)
+      if (D == 128) {
+        if (ntu <= 1) DUSTIN_SEG(128, 1);
+        else if (ntu == 2 || NT < 3) DUSTIN_SEG(128, (NT < 2 ? NT : 2));
+        else if (ntu == 3 || NT < 4) DUSTIN_SEG(128, (NT < 3 ? NT : 3));
+        else DUSTIN_SEG(128, NT);
+      } else {
+        if (ntu <= 1) DUSTIN_SEG(64, 1);
+        else if (ntu == 2 || NT < 3) DUSTIN_SEG(64, (NT < 2 ? NT : 2));
+        else if (ntu == 3 || NT < 4) DUSTIN_SEG(64, (NT < 3 ? NT : 3));
+        else DUSTIN_SEG(64, NT);
+      }
+#undef DUSTIN_SEG
+      i += n;
+      // segment statistics: reduce over lanes and warps, write one slot
 #pragma unroll
-        for (int mi = 0; mi < 2; ++mi) {
-          if (mi >= nmt) break;
-          const int rb = 16 * warp + kBoxRows * mi;
-          float c[NT][4];
+      for (int j = 0; j < NT; ++j) {
 #pragma unroll
-          for (int j = 0; j < NT; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
-          const int arow = rb + (lane & 7) + 8 * ((lane >> 3) & 1);
+        for (int e = 0; e < 2; ++e) {
+          float m = rm[j][e], sm = rs[j][e];
 #pragma unroll
-          for (int ks = 0; ks < kMaxKs; ++ks) {
-            if (ks < (D >> 4)) {
-              uint32_t a0, a1, a2, a3;
-              ldmatrix_x4(a0, a1, a2, a3, tile_addr(sb, D, arow, 16 * ks + 8 * (lane >> 4)));
-#pragma unroll
-              for (int j = 0; j < NT; ++j)
-                if (j < nt) mma_bf16_16816(c[j], a0, a1, a2, a3, qb[j][ks][0], qb[j][ks][1]);
-            }
+          for (int o = 4; o < 32; o <<= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const float s2 = __shfl_xor_sync(0xffffffffu, sm, o);
+            stat_merge(m, sm, m2, s2);
           }
-          const int pos_lo = r0 + rb + (lane >> 2);
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            if (j >= nt) break;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int pair = 8 * j + 2 * (lane & 3) + (e & 1);
-              const int pos = pos_lo + ((e >> 1) << 3);
-              if (pair < S.npairs && (full_tile || pos < L)) {
-                const float v = c[j][e] * scale;
-                lrow[size_t(pair) * A.LSP + pos] = v;
-                // online sum of 2^(v - m) with a lazily raised reference m:
-                // the reference only moves when v passes it by more than 8,
-                // so the common path is one ex2 and one add
-                float& m = rm[j][e & 1];
-                float& sm = rs[j][e & 1];
-                if (v > m + 8.f) {
-                  sm *= fast_exp2(m - v);
-                  m = v;
-                }
-                sm += fast_exp2(v - m);
-              }
-            }
+          const int pair = 8 * j + 2 * lane + e;
+          if (lane < 4) {
+            red[(warp * 32 + pair) * 2] = m;
+            red[(warp * 32 + pair) * 2 + 1] = sm;
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-
-      // end of segment: reduce the statistics and write them out
-      bool seg_end = (t + 1 == t1);
-      if (!seg_end) {
-        int s2, bl2, tile2;
-        decode_tile(A, t + 1, s2, bl2, tile2);
-        seg_end = (s2 != s || bl2 != bl);
+      named_bar(1, 32 * kConsumers);
+      if (warp == 0 && lane < npairs) {
+        float m = -INFINITY, sm = 0.f;
+        for (int w = 0; w < kConsumers; ++w)
+          stat_merge(m, sm, red[(w * 32 + lane) * 2], red[(w * 32 + lane) * 2 + 1]);
+        const long long first = A.slab_start[s] + (long long)bl * S.tiles;
+        const int seg = int(blockIdx.x) - cta_of(first, A.total, G);
+        float* slot = A.stats + ((size_t(s) * A.nb + bl) * A.max_seg + seg) * size_t(A.np_max) * 2;
+        slot[lane * 2] = m;
+        slot[lane * 2 + 1] = sm;
       }
-      if (seg_end) {
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float m = rm[j][e], sm = rs[j][e];
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-              const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-              const float s2 = __shfl_xor_sync(0xffffffffu, sm, o);
-              stat_merge(m, sm, m2, s2);
-            }
-            const int pair = 8 * j + 2 * lane + e;
-            if (lane < 4) {
-              red[(warp * 32 + pair) * 2] = m;
-              red[(warp * 32 + pair) * 2 + 1] = sm;
-            }
-          }
-        }
-        named_bar(1, 32 * kConsumers);
-        if (warp == 0 && lane < S.npairs) {
-          float m = -INFINITY, sm = 0.f;
-          for (int w = 0; w < kConsumers; ++w)
-            stat_merge(m, sm, red[(w * 32 + lane) * 2], red[(w * 32 + lane) * 2 + 1]);
-          const long long first = A.slab_start[s] + (long long)bl * S.tiles;
-          const int seg = int(blockIdx.x) - cta_of(first, A.total, G);
-          float* slot = A.stats + ((size_t(s) * A.nb + bl) * A.max_seg + seg) * size_t(A.np_max) * 2;
-          slot[lane * 2] = m;
-          slot[lane * 2 + 1] = sm;
-        }
-        named_bar(1, 32 * kConsumers);
+      named_bar(1, 32 * kConsumers);
+      t += n;
+      tile = 0;
+      if (++bl == A.nb) {
+        bl = 0;
+        ++s;
       }
     }
   }

@@ -69,6 +69,28 @@ __device__ __forceinline__ bool excluded(const uint32_t* excl, int i) {
   return excl && ((excl[i >> 5] >> (i & 31)) & 1u);
 }
 
+constexpr int kBatch = 8;   // independent key loads in flight per thread
+
+// Calls f(i, key, valid) for every i in [u0, u1), block-strided, with kBatch
+// loads issued before any is used (so global-memory keys do not serialise on
+// latency).  Every lane of every warp makes the same number of calls.
+template <typename F>
+__device__ __forceinline__ void for_keys(const KeySrc& key, int u0, int u1, const uint32_t* excl,
+                                         F f) {
+  for (int base = u0; base < u1; base += kThreads * kBatch) {
+    uint32_t kv[kBatch];
+    bool ok[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kThreads + int(threadIdx.x);
+      ok[u] = i < u1 && !excluded(excl, i);
+      kv[u] = ok[u] ? key(i) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) f(base + u * kThreads + int(threadIdx.x), kv[u], ok[u]);
+  }
+}
+
 // Over the histogram in descending bin order: the bin holding the need-th key
 // and how many keys of that bin are still needed.  Whole-block call.
 __device__ void find_bin(SelShared& sh, int nbins, int need) {
@@ -123,22 +145,26 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
   for (int b = tid; b < kBins1; b += kThreads) sh.hist[b] = 0;
   if (tid == 0) sh.ncand = 0;
   __syncthreads();
-  for (int i = u0 + tid; i < u1; i += kThreads)
-    if (!excluded(excl, i)) atomicAdd(&sh.hist[key(i) >> 20], 1);
+  for_keys(key, u0, u1, excl, [&](int, uint32_t kv, bool ok) {
+    if (ok) atomicAdd(&sh.hist[kv >> 20], 1);
+  });
   __syncthreads();
   find_bin(sh, kBins1, cnt);
   const uint32_t b1 = uint32_t(sh.bin);
   int need = sh.need;
 
-  // 2. gather the keys of the threshold bin
-  for (int i = u0 + tid; i < u1; i += kThreads) {
-    if (excluded(excl, i)) continue;
-    const uint32_t kv = key(i);
-    if ((kv >> 20) == b1) {
-      const int slot = atomicAdd(&sh.ncand, 1);
-      if (slot < kCandCap) sh.cand[slot] = kv;
+  // 2. gather the keys of the threshold bin (one atomic per warp)
+  for_keys(key, u0, u1, excl, [&](int, uint32_t kv, bool ok) {
+    const bool hit = ok && (kv >> 20) == b1;
+    const uint32_t ball = __ballot_sync(0xffffffffu, hit);
+    if (ball) {
+      int slot0 = 0;
+      if (lane == 0) slot0 = atomicAdd(&sh.ncand, __popc(ball));
+      slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+      const int slot = slot0 + __popc(ball & ((1u << lane) - 1u));
+      if (hit && slot < kCandCap) sh.cand[slot] = kv;
     }
-  }
+  });
   __syncthreads();
   const int ncand = sh.ncand;
   const bool listed = ncand <= kCandCap;
@@ -156,11 +182,9 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
         if ((kv & hi_mask) == prefix) atomicAdd(&sh.hist[(kv >> shift) & 1023u], 1);
       }
     } else {
-      for (int i = u0 + tid; i < u1; i += kThreads) {
-        if (excluded(excl, i)) continue;
-        const uint32_t kv = key(i);
-        if ((kv & hi_mask) == prefix) atomicAdd(&sh.hist[(kv >> shift) & 1023u], 1);
-      }
+      for_keys(key, u0, u1, excl, [&](int, uint32_t kv, bool ok) {
+        if (ok && (kv & hi_mask) == prefix) atomicAdd(&sh.hist[(kv >> shift) & 1023u], 1);
+      });
     }
     __syncthreads();
     find_bin(sh, kBins2, need);
@@ -176,12 +200,20 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
   const int w0 = a0 + warp * chunk;
   const int w1 = min(w0 + chunk, u1);
   int ngt = 0, neq = 0;
-  for (int g0 = w0; g0 < w1; g0 += 32) {
-    const int i = g0 + lane;
-    const bool c = i >= u0 && i < w1 && !excluded(excl, i);
-    const uint32_t kv = c ? key(i) : 0u;
-    ngt += __popc(__ballot_sync(0xffffffffu, c && kv > T));
-    neq += __popc(__ballot_sync(0xffffffffu, c && kv == T));
+  for (int gb = w0; gb < w1; gb += 32 * kBatch) {
+    uint32_t kv[kBatch];
+    bool cv[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = gb + 32 * u + lane;
+      cv[u] = i >= u0 && i < w1 && !excluded(excl, i);
+      kv[u] = cv[u] ? key(i) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      ngt += __popc(__ballot_sync(0xffffffffu, cv[u] && kv[u] > T));
+      neq += __popc(__ballot_sync(0xffffffffu, cv[u] && kv[u] == T));
+    }
   }
   if (lane == 0) {
     sh.wgt[warp] = ngt;
@@ -196,19 +228,29 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
   int pos = gt_before + min(eq_before, need);
   int eq_run = eq_before;
   const uint32_t lt = (1u << lane) - 1u;
-  for (int g0 = w0; g0 < w1; g0 += 32) {
-    const int i = g0 + lane;
-    const bool c = i >= u0 && i < w1 && !excluded(excl, i);
-    const uint32_t kv = c ? key(i) : 0u;
-    const bool isgt = c && kv > T;
-    const bool iseq = c && kv == T;
-    const uint32_t eqb = __ballot_sync(0xffffffffu, iseq);
-    const bool sel = isgt || (iseq && (eq_run + __popc(eqb & lt)) < need);
-    const uint32_t selb = __ballot_sync(0xffffffffu, sel);
-    if (sel) out[pos + __popc(selb & lt)] = i;
-    if (setbits && lane == 0) setbits[g0 >> 5] |= selb;
-    pos += __popc(selb);
-    eq_run += __popc(eqb);
+  for (int gb = w0; gb < w1; gb += 32 * kBatch) {
+    uint32_t kv[kBatch];
+    bool cv[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = gb + 32 * u + lane;
+      cv[u] = i >= u0 && i < w1 && !excluded(excl, i);
+      kv[u] = cv[u] ? key(i) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int g0 = gb + 32 * u;
+      const int i = g0 + lane;
+      const bool isgt = cv[u] && kv[u] > T;
+      const bool iseq = cv[u] && kv[u] == T;
+      const uint32_t eqb = __ballot_sync(0xffffffffu, iseq);
+      const bool sel = isgt || (iseq && (eq_run + __popc(eqb & lt)) < need);
+      const uint32_t selb = __ballot_sync(0xffffffffu, sel);
+      if (sel) out[pos + __popc(selb & lt)] = i;
+      if (setbits && lane == 0 && g0 < w1) setbits[g0 >> 5] |= selb;
+      pos += __popc(selb);
+      eq_run += __popc(eqb);
+    }
   }
   __syncthreads();
 }
@@ -245,7 +287,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   for (int ch = 0; ch < 2; ++ch) {
     const float* row = A.imp + (size_t(b) * 2 + ch) * A.Lcap;
     if (keys) {
-      for (int i = s_eff + tid; i < w0; i += kThreads) keys[i] = key_of(row[i], A.err);
+      for (int base = s_eff; base < w0; base += kThreads * kBatch) {
+        float v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int i = base + u * kThreads + tid;
+          v[u] = i < w0 ? row[i] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int i = base + u * kThreads + tid;
+          if (i < w0) keys[i] = key_of(v[u], A.err);
+        }
+      }
     }
     __syncthreads();
     KeySrc src{keys, row, A.err};

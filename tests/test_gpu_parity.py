@@ -56,6 +56,19 @@ def test_score_long_caches_in_sequence_groups():
         assert_importance(imp, c.oracle_score(), c.x.seq_len)
 
 
+def test_score_strided_cache_views():
+    """Caches that are views with padded strides (not densely packed) are read
+    through the general 4-D tensor maps; results are unchanged."""
+    wl = WORKLOADS["tiny"].with_(B=2)
+    c = Case(wl, seq_len=[1024, 700])
+    x = c.x
+    pad = lambda t: torch.cat([t, torch.zeros_like(t[:, :, :96])], dim=2)[:, :, : t.shape[2]]
+    K2, Kd2 = [pad(t) for t in x.K], [pad(t) for t in x.Kd]
+    assert K2[0].stride(1) != K2[0].shape[2] * K2[0].shape[3]
+    imp = dk.dustin_score(c.p, dk.Signal(x.draft_q, Kd2), dk.Signal(x.hist_q, K2), wl.srh, c.seq)
+    assert_importance(imp, c.oracle_score(), c.x.seq_len)
+
+
 def test_score_deterministic():
     c = Case(WORKLOADS["layer8k"])
     a = dk.dustin_score(c.p, c.draft, c.target, c.wl.srh, c.seq).clone()
