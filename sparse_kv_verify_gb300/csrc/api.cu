@@ -198,6 +198,7 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
       S.nheads = 0;
       S.npairs = 0;
       S.rows = score_rows_per_tile(kv.d);
+      S.cost = 0;
       S.tiles = (p->Lcap + S.rows - 1) / S.rows;
       S.q = static_cast<const uint16_t*>(q);
     }
@@ -206,6 +207,8 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
     S.heads[S.nheads++] = e.q_head;
     S.npairs += s->nq;
   }
+  for (int t = 0; t < pl->n_slab; ++t)
+    pl->slab[t].cost = score_tile_cost(pl->slab[t].D, pl->slab[t].npairs);
   pl->LSP = (p->Lcap + 31) / 32 * 32;
   size_t per_b = 0;   // logits bytes of one sequence
   for (int t = 0; t < pl->n_slab; ++t) {
@@ -225,12 +228,16 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
       if (scratch_max) return DUSTIN_ERANGE;   // a hard scratch bound: refuse
       nb = 1;                                  // one sequence at a time, past the L2 budget
     }
-    // statistics slots: the smallest group has the fewest tiles per CTA
-    const int last = int(p->B % nb ? p->B % nb : nb);
-    const long long per = group_tiles(*pl, last) / kScoreGridMax;
-    int tmax = 0;
-    for (int t = 0; t < pl->n_slab; ++t) tmax = tmax > pl->slab[t].tiles ? tmax : pl->slab[t].tiles;
-    pl->max_seg = int(tmax / (per > 0 ? per : 1)) + 2;
+    // statistics slots: a CTA's share of the cost is at least the cheapest
+    // tile's cost (the grid never exceeds the tile count), so a run of `tiles`
+    // tiles spans at most tiles * cost_max / cost_min + 2 CTA indices
+    int tmax = 0, wmin = 1 << 30, wmax = 0;
+    for (int t = 0; t < pl->n_slab; ++t) {
+      tmax = tmax > pl->slab[t].tiles ? tmax : pl->slab[t].tiles;
+      wmin = wmin < pl->slab[t].cost ? wmin : pl->slab[t].cost;
+      wmax = wmax > pl->slab[t].cost ? wmax : pl->slab[t].cost;
+    }
+    pl->max_seg = int((long long)tmax * wmax / wmin) + 3;
     pl->nb = int(nb);
     pl->logits_bytes = round256(per_b * nb);
     pl->stats_bytes = round256(size_t(pl->n_slab) * nb * pl->max_seg * pl->np_max * 2 * 4);
@@ -281,13 +288,17 @@ int launch_score(const dustin_params* p, const dustin_signal* draft, const dusti
   for (int b0 = 0; b0 < p->B; b0 += pl.nb) {
     a.b0 = b0;
     a.nb = p->B - b0 < pl.nb ? p->B - b0 : pl.nb;
-    long long acc = 0;
+    long long acc = 0, cost = 0;
     for (int t = 0; t < pl.n_slab; ++t) {
       a.slab_start[t] = acc;
+      a.cost_start[t] = cost;
       acc += (long long)a.nb * pl.slab[t].tiles;
+      cost += (long long)a.nb * pl.slab[t].tiles * pl.slab[t].cost;
     }
     a.slab_start[pl.n_slab] = acc;
+    a.cost_start[pl.n_slab] = cost;
     a.total = acc;
+    a.total_cost = cost;
     long long grid = sms < kScoreGridMax ? sms : kScoreGridMax;
     if (grid > a.total) grid = a.total;
     a.grid = int(grid);

@@ -19,6 +19,8 @@ __device__ __forceinline__ bool append_ok(const AppendArgs& A, int b, int* L_out
 
 // grid (hkv, B, n_layers); 128 threads copy up to T rows of K and V
 __global__ void append_copy_kernel(const __grid_constant__ AppendArgs A) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int g = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
   int L, n;
   if (!append_ok(A, b, &L, &n)) return;
@@ -42,6 +44,8 @@ __global__ void append_copy_kernel(const __grid_constant__ AppendArgs A) {
 }
 
 __global__ void append_bump_kernel(const __grid_constant__ AppendArgs A) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= A.B) return;
   int L, n;
@@ -55,11 +59,9 @@ __global__ void append_bump_kernel(const __grid_constant__ AppendArgs A) {
 }  // namespace
 
 cudaError_t append_launch(const AppendArgs& a, cudaStream_t stream) {
-  append_copy_kernel<<<dim3(a.hkv, a.B, a.n_layers), 128, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(append_copy_kernel, dim3(a.hkv, a.B, a.n_layers), dim3(128), 0, stream, a);
   if (e != cudaSuccess) return e;
-  append_bump_kernel<<<(a.B + 127) / 128, 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(append_bump_kernel, dim3((a.B + 127) / 128), dim3(128), 0, stream, a);
 }
 
 }  // namespace dustin

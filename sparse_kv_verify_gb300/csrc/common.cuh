@@ -146,6 +146,18 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Kernels of one call are launched so that the next kernel may start while
+// this one finishes.  Every kernel calls pdl_wait() before it touches global
+// memory written by an earlier kernel (it returns at once when the launch had
+// no programmatic dependency), and pdl_launch_dependents() once all of its
+// CTAs are resident.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------- tensor cores
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2,

@@ -9,6 +9,25 @@
 
 namespace dustin {
 
+// Launches kern<<<grid, block, smem, stream>>>(args) with programmatic stream
+// serialisation, so that it may begin while the previous kernel in the stream
+// drains (the kernel itself waits with pdl_wait before reading its inputs).
+template <typename Kern, typename Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       const Args& args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
 // ------------------------------------------------------------------ verify
 
 struct VerifyLayerDev {
@@ -70,6 +89,7 @@ struct ScoreSlab {
   int tiles;     // tiles per sequence: ceil(Lcap / rows)
   long long logit_off;   // float offset of this slab's logits [nb][npairs][LSP]
   int row2d;     // 0: 4-D map; else 2-D map over packed rows, value = hkv of the cache
+  int cost;      // relative cost of one tile (bytes plus logits written), for balancing
   const uint16_t* q;     // [B][nq][hq][D]
 };
 
@@ -77,7 +97,9 @@ struct ScoreArgs {
   CUtensorMap map[DUSTIN_MAX_SRH];   // one per (channel, layer) cache; box 64 x 128
   ScoreSlab slab[DUSTIN_MAX_SRH];
   long long slab_start[DUSTIN_MAX_SRH + 1];   // first flattened tile of each slab
+  long long cost_start[DUSTIN_MAX_SRH + 1];   // cost before the first tile of each slab
   long long total;                            // tiles of this group
+  long long total_cost;                       // sum of tile costs of this group
   int B, Lcap, LSP, n_slab, np_max;
   int b0, nb;            // the group of sequences handled by this launch
   int grid;              // CTAs of the stream kernel
@@ -97,6 +119,7 @@ struct ScoreLaunch {
 constexpr int kScoreGridMax = 256;
 size_t score_stream_smem();
 int score_rows_per_tile(int D);
+int score_tile_cost(int D, int npairs);
 cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream);
 
 // ------------------------------------------------------------------ select

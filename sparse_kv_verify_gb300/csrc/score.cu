@@ -37,7 +37,8 @@ constexpr int kStages = 6;
 constexpr int kConsumers = 8;                        // 8 warps x 16 rows = 128 rows
 constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int kMaxKs = 8;                            // d / 16 for d = 128
-constexpr int kNormChunk = 1024;                     // positions per normalise CTA
+constexpr int kNormThreads = 128;
+constexpr int kNormChunk = 4 * kNormThreads;         // positions per normalise CTA
 
 __device__ __forceinline__ uint32_t tile_addr(uint32_t st, int D, int r, int c) {
   // element (row r, column c) of a tile stored as two TMA boxes of
@@ -47,8 +48,29 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t st, int D, int r, int c) 
   return st + box * kBoxBytes + (r & 127) * 128 + ((chunk ^ (r & 7)) << 4) + ((c & 7) << 1);
 }
 
-__device__ __forceinline__ int cta_of(long long x, long long total, int G) {
-  return int(((x + 1) * G + total - 1) / total) - 1;
+// Work is split by cost: CTA c owns the tiles whose cost prefix lies in
+// [floor(c * W / G), floor((c + 1) * W / G)), W the total cost.
+
+// Cost before flattened tile t.
+__device__ __forceinline__ long long cost_prefix(const ScoreArgs& A, long long t) {
+  int s = 0;
+  while (s + 1 < A.n_slab && A.slab_start[s + 1] <= t) ++s;
+  return A.cost_start[s] + (t - A.slab_start[s]) * A.slab[s].cost;
+}
+
+// First tile whose cost prefix is >= P.
+__device__ __forceinline__ long long tile_at_cost(const ScoreArgs& A, long long P) {
+  if (P >= A.total_cost) return A.total;
+  int s = 0;
+  while (s + 1 < A.n_slab && A.cost_start[s + 1] <= P) ++s;
+  const long long k = (P - A.cost_start[s] + A.slab[s].cost - 1) / A.slab[s].cost;
+  return A.slab_start[s] + k;
+}
+
+// CTA that owns flattened tile t.
+__device__ __forceinline__ int owner_of(const ScoreArgs& A, long long t, int G) {
+  const long long P = cost_prefix(A, t);
+  return int(((P + 1) * G + A.total_cost - 1) / A.total_cost) - 1;
 }
 
 __device__ __forceinline__ void named_bar(int id, int n) {
@@ -154,8 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
-  const long long t0 = (long long)blockIdx.x * A.total / G;
-  const long long t1 = (long long)(blockIdx.x + 1) * A.total / G;
+  const long long t0 = tile_at_cost(A, (long long)blockIdx.x * A.total_cost / G);
+  const long long t1 = tile_at_cost(A, (long long)(blockIdx.x + 1) * A.total_cost / G);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -164,7 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
     }
     *abort_flag = 0;
     fence_barrier_init();
+    prefetch_tensormap(&A.map[0]);
   }
+  pdl_launch_dependents();
+  pdl_wait();
   __syncthreads();
   if (t0 >= t1) return;
 
@@ -308,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
         for (int w = 0; w < kConsumers; ++w)
           stat_merge(m, sm, red[(w * 32 + lane) * 2], red[(w * 32 + lane) * 2 + 1]);
         const long long first = A.slab_start[s] + (long long)bl * S.tiles;
-        const int seg = int(blockIdx.x) - cta_of(first, A.total, G);
+        const int seg = int(blockIdx.x) - owner_of(A, first, G);
         float* slot = A.stats + ((size_t(s) * A.nb + bl) * A.max_seg + seg) * size_t(A.np_max) * 2;
         slot[lane * 2] = m;
         slot[lane * 2 + 1] = sm;
@@ -324,12 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
   }
 }
 
-__global__ void __launch_bounds__(256) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
+__global__ void __launch_bounds__(kNormThreads) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
   // one row per (slab, pair): logits offset, merged max M and 1 / sum
   __shared__ long long roff[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
   __shared__ float Mg[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
   __shared__ float Ig[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
   __shared__ int nrow[2];
+  pdl_launch_dependents();
+  pdl_wait();
   const int bl = blockIdx.y;
   const int b = A.b0 + bl;
   int L = A.seq_len[b];
@@ -354,11 +381,17 @@ __global__ void __launch_bounds__(256) score_norm_kernel(const __grid_constant__
     r += p;
     float m = -INFINITY, sm = 0.f;
     const long long first = A.slab_start[s] + (long long)bl * S.tiles;
-    const int n_seg = cta_of(first + S.tiles - 1, A.total, G) - cta_of(first, A.total, G) + 1;
+    const int c0 = owner_of(A, first, G);
+    const int n_seg = owner_of(A, first + S.tiles - 1, G) - c0 + 1;
     const float* slots = A.stats + (size_t(s) * A.nb + bl) * A.max_seg * size_t(A.np_max) * 2;
-    for (int g = 0; g < n_seg; ++g)
+    for (int g = 0; g < n_seg; ++g) {
+      // CTAs whose share is smaller than one tile own no tiles and wrote nothing
+      const long long lo = tile_at_cost(A, (long long)(c0 + g) * A.total_cost / G);
+      const long long hi = tile_at_cost(A, (long long)(c0 + g + 1) * A.total_cost / G);
+      if (lo >= hi) continue;
       stat_merge(m, sm, __ldcg(slots + (size_t(g) * A.np_max + p) * 2),
                  __ldcg(slots + (size_t(g) * A.np_max + p) * 2 + 1));
+    }
     roff[r] = S.logit_off + (long long)(size_t(bl) * S.npairs + p) * A.LSP;
     Mg[r] = m;
     Ig[r] = sm > 0.f ? 1.f / sm : 0.f;
@@ -368,7 +401,7 @@ __global__ void __launch_bounds__(256) score_norm_kernel(const __grid_constant__
   // each thread: 4 consecutive positions (one float4 per logits row; rows are
   // padded to a multiple of 32 floats, so the loads are aligned and in bounds)
   const int pos = base + 4 * threadIdx.x;
-  constexpr int kBatch = 8;
+  constexpr int kBatch = 16;
   int r0 = 0;
   for (int c = 0; c < 2; ++c) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -414,8 +447,7 @@ cudaError_t launch_stream(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_
   auto kern = score_stream_kernel<NT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(pl.smem));
   if (e != cudaSuccess) return e;
-  kern<<<a.grid, kThreads, pl.smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.grid), dim3(kThreads), pl.smem, stream, a);
 }
 
 }  // namespace
@@ -425,6 +457,12 @@ size_t score_stream_smem() {
 }
 
 int score_rows_per_tile(int D) { return D == 128 ? kBoxRows : 2 * kBoxRows; }
+
+int score_tile_cost(int D, int npairs) {
+  // 32 KB of K per tile plus the logits it writes (rows x pairs), in units that
+  // match the measured per-tile times of the two tile shapes
+  return 1000 + score_rows_per_tile(D) * npairs / 2;
+}
 
 cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream) {
   cudaError_t e;
@@ -437,8 +475,7 @@ cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t
   }
   if (e != cudaSuccess) return e;
   dim3 grid((a.Lcap + kNormChunk - 1) / kNormChunk, a.nb);
-  score_norm_kernel<<<grid, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(score_norm_kernel, grid, dim3(kNormThreads), 0, stream, a);
 }
 
 }  // namespace dustin

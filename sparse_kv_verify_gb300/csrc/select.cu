@@ -259,6 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   extern __shared__ __align__(16) unsigned char dsm[];
   SelShared& sh = *reinterpret_cast<SelShared*>(dsm);
   unsigned char* rest = dsm + ((sizeof(SelShared) + 15) & ~size_t(15));
+  pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   int32_t* out = A.out + size_t(b) * A.k;
@@ -326,8 +328,7 @@ cudaError_t select_launch(const SelectArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(smem));
   if (e != cudaSuccess) return e;
-  select_kernel<<<a.B, kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, dim3(a.B), dim3(kThreads), smem, stream, a);
 }
 
 }  // namespace dustin

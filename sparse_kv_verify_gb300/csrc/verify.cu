@@ -90,6 +90,8 @@ __global__ void __launch_bounds__(64 * MT) verify_kernel(const __grid_constant__
   float* mM = mO + size_t(MT) * 16 * Ly::OS;
   float* mL = mM + MT * 16;
 
+  pdl_launch_dependents();
+  pdl_wait();
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int mt = warp >> 1, half = warp & 1;
@@ -397,8 +399,7 @@ cudaError_t launch_t(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t s
   const size_t smem = Lay<D, MT, NSTAGE>::total;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  kern<<<pl.grid, 64 * MT, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(pl.grid), dim3(64 * MT), smem, stream, a);
 }
 
 template <int D, int MT>
