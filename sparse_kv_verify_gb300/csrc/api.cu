@@ -299,8 +299,14 @@ int launch_score(const dustin_params* p, const dustin_signal* draft, const dusti
     a.cost_start[pl.n_slab] = cost;
     a.total = acc;
     a.total_cost = cost;
+    // every CTA's share of the cost must reach the largest tile cost, so that
+    // each CTA owns at least one tile (the normalise kernel relies on it)
+    long long wmax = 1;
+    for (int t = 0; t < pl.n_slab; ++t)
+      if (pl.slab[t].cost > wmax) wmax = pl.slab[t].cost;
     long long grid = sms < kScoreGridMax ? sms : kScoreGridMax;
-    if (grid > a.total) grid = a.total;
+    if (grid > a.total_cost / wmax) grid = a.total_cost / wmax;
+    if (grid < 1) grid = 1;
     a.grid = int(grid);
     if (score_launch(a, pl.launch, stream) != cudaSuccess) return DUSTIN_ECUDA;
   }
@@ -466,7 +472,6 @@ int dustin_select(const dustin_params* p, const float* importance, const int32_t
   a.sinks = p->sinks;
   a.window = p->window;
   a.m = p->m;
-  a.cache_keys = select_cache_keys(p->Lcap);
   a.imp = importance;
   a.seq_len = seq_len;
   a.out = i_verify;

@@ -126,14 +126,14 @@ cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t
 
 struct SelectArgs {
   int B, Lcap, k, sinks, window, m;
-  int cache_keys;        // 1: stage keys in shared memory
+  int cache_keys;        // set by select_launch: 1 = stage keys in shared memory
+  int slice_cap;         // set by select_launch: positions per CTA slice
   const float* imp;      // [B][2][Lcap]
   const int32_t* seq_len;
   int32_t* out;          // [B][k]
   int* err;
 };
-size_t select_smem_bytes(int Lcap, int cache_keys);
-int select_cache_keys(int Lcap);
+int select_cluster_size(const SelectArgs& a);   // CTAs per sequence select_launch uses
 cudaError_t select_launch(const SelectArgs& a, cudaStream_t stream);
 
 // ------------------------------------------------------------------ append

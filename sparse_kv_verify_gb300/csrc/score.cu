@@ -355,6 +355,7 @@ __global__ void __launch_bounds__(kNormThreads) score_norm_kernel(const __grid_c
   __shared__ float Mg[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
   __shared__ float Ig[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
   __shared__ int nrow[2];
+  __shared__ int nseg[DUSTIN_MAX_SRH];
   pdl_launch_dependents();
   pdl_wait();
   const int bl = blockIdx.y;
@@ -368,6 +369,15 @@ __global__ void __launch_bounds__(kNormThreads) score_norm_kernel(const __grid_c
       if (A.slab[s].channel == int(threadIdx.x)) n += A.slab[s].npairs;
     nrow[threadIdx.x] = n;
   }
+  // per slab: how many CTAs own tiles of this sequence (the host sizes the
+  // grid so that every CTA owns at least one tile, so each of them wrote its
+  // statistics slot)
+  if (threadIdx.x >= 32 && int(threadIdx.x) < 32 + A.n_slab) {
+    const int s = threadIdx.x - 32;
+    const long long first = A.slab_start[s] + (long long)bl * A.slab[s].tiles;
+    nseg[s] = owner_of(A, first + A.slab[s].tiles - 1, G) - owner_of(A, first, G) + 1;
+  }
+  __syncthreads();
   for (int q = threadIdx.x; q < A.n_slab * DUSTIN_MAX_PAIRS; q += blockDim.x) {
     const int s = q / DUSTIN_MAX_PAIRS, p = q - s * DUSTIN_MAX_PAIRS;
     const ScoreSlab& S = A.slab[s];
@@ -380,17 +390,17 @@ __global__ void __launch_bounds__(kNormThreads) score_norm_kernel(const __grid_c
     }
     r += p;
     float m = -INFINITY, sm = 0.f;
-    const long long first = A.slab_start[s] + (long long)bl * S.tiles;
-    const int c0 = owner_of(A, first, G);
-    const int n_seg = owner_of(A, first + S.tiles - 1, G) - c0 + 1;
+    const int n_seg = nseg[s];
     const float* slots = A.stats + (size_t(s) * A.nb + bl) * A.max_seg * size_t(A.np_max) * 2;
-    for (int g = 0; g < n_seg; ++g) {
-      // CTAs whose share is smaller than one tile own no tiles and wrote nothing
-      const long long lo = tile_at_cost(A, (long long)(c0 + g) * A.total_cost / G);
-      const long long hi = tile_at_cost(A, (long long)(c0 + g + 1) * A.total_cost / G);
-      if (lo >= hi) continue;
-      stat_merge(m, sm, __ldcg(slots + (size_t(g) * A.np_max + p) * 2),
-                 __ldcg(slots + (size_t(g) * A.np_max + p) * 2 + 1));
+    for (int g = 0; g < n_seg; g += 4) {
+      float2 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (g + u < n_seg)
+          v[u] = __ldcg(reinterpret_cast<const float2*>(slots + (size_t(g + u) * A.np_max + p) * 2));
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (g + u < n_seg) stat_merge(m, sm, v[u].x, v[u].y);
     }
     roff[r] = S.logit_off + (long long)(size_t(bl) * S.npairs + p) * A.LSP;
     Mg[r] = m;

@@ -4,43 +4,66 @@
 // by the draft signal, then the most relevant remaining tokens by the target
 // signal).
 //
-// One 1024-thread CTA per sequence.  Importance values are non-negative fp32,
-// so their bit patterns order like the values.  Each tier finds the exact
-// threshold key T of its top-cnt (descending key, ties to the lower index):
-//   1. a 4096-bin histogram of the top 12 bits (sign, exponent, 3 mantissa
-//      bits) of every candidate key -- fine enough that the shared-memory
-//      atomics rarely collide -- gives the bin that holds the cnt-th key;
-//   2. the keys of that bin are gathered into a small list and two 10-bit
-//      radix passes over the list give T and how many keys equal to T to take;
-//   3. an order-preserving compaction writes every key > T and the
-//      lowest-index keys == T, ascending.
-// If the threshold bin holds more keys than the list can take (heavy ties), the
-// refinement runs over all candidates instead.  Keys are staged in shared
-// memory when the cache capacity allows; the draft tier is recorded in a
-// bitmap that the target tier skips.
+// One thread-block cluster of CS CTAs per sequence (CS = 8, 4, 2 or 1: the
+// largest size whose B clusters are all resident at once); CTA r owns a
+// contiguous slice of the unprotected positions.  Importance values are non-negative
+// fp32, so their bit patterns order like the values.  Each tier finds the
+// exact threshold key T of its top-cnt (descending key, ties to the lower
+// index) by a three-level radix select whose histograms are merged across the
+// cluster through distributed shared memory:
+//   level 1  a 4096-bin histogram of the top 12 bits (sign, exponent and 3
+//            mantissa bits) -- fine enough that shared-memory atomics rarely
+//            collide; the merged histogram gives the bin that holds the
+//            cnt-th key,
+//   level 2  keys of that bin are gathered into a small per-CTA list and two
+//            10-bit histograms of the list give T and how many keys equal to T
+//            are needed,
+//   level 3  each CTA counts its keys > T and == T, the cluster exchanges the
+//            counts, and every CTA writes its selected positions (every key > T
+//            and the lowest-index keys == T) ascending at its offset.
+// If a threshold bin holds more keys than a CTA's list can take (heavy ties),
+// that CTA's refinement histograms scan its whole slice instead.  The draft
+// tier is recorded in a per-slice bitmap that the target tier skips.
+#include <cooperative_groups.h>
+
+#include <mutex>
+#include <vector>
+
 #include "common.cuh"
 #include "kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace dustin {
 
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins1 = 4096;      // top 12 bits
 constexpr int kBins2 = 1024;      // 10 bits
-constexpr int kCandCap = 8192;
-constexpr size_t kSmemBudget = 200 * 1024;
+constexpr int kCandCap = 4096;
+constexpr int kBatch = 8;         // independent key loads in flight per thread
+constexpr size_t kSmemBudget = 220 * 1024;
 
+// CS: CTAs per sequence (the cluster size); rank r merges level-1 bins
+// [r * 4096 / CS, (r + 1) * 4096 / CS)
+template <int CS>
 struct SelShared {
-  int hist[kBins1];
+  static constexpr int kSliceBins = kBins1 / CS;
+  int hist1[kBins1];         // level-1 histogram of this slice (later: merged scratch)
+  int gsl[kSliceBins];       // merged level-1 counts of this rank's bin slice
+  int hist2[2][kBins2];      // level-2/3 histograms of this slice (double buffered)
   uint32_t cand[kCandCap];
   int wsum[kWarps];
   int wgt[kWarps];
   int weq[kWarps];
+  int gsl_total;
   int ncand;
-  int bin;
-  int need;
+  int cnt_gt, cnt_eq;
+  int bin, need;
+  int slice, need1;
+  int gt_before, eq_before;
 };
 
 __device__ __forceinline__ uint32_t key_of(float v, int* err) {
@@ -57,33 +80,36 @@ __device__ __forceinline__ uint32_t key_of(float v, int* err) {
 }
 
 struct KeySrc {
-  const uint32_t* cached;  // shared-memory copy (or nullptr)
-  const float* global;     // importance row of this channel
+  const uint32_t* cached;  // shared-memory copy of the slice (indexed from its start)
+  const float* global;     // importance row of this channel (indexed by position)
+  int base;                // first position of the slice
   int* err;
   __device__ __forceinline__ uint32_t operator()(int i) const {
-    return cached ? cached[i] : key_of(global[i], err);
+    return cached ? cached[i - base] : key_of(global[i], err);
   }
 };
 
-__device__ __forceinline__ bool excluded(const uint32_t* excl, int i) {
-  return excl && ((excl[i >> 5] >> (i & 31)) & 1u);
-}
+struct Excl {
+  const uint32_t* bits;    // bitmap of the slice (bit i - base), or nullptr
+  int base;
+  __device__ __forceinline__ bool operator()(int i) const {
+    if (!bits) return false;
+    const int o = i - base;
+    return (bits[o >> 5] >> (o & 31)) & 1u;
+  }
+};
 
-constexpr int kBatch = 8;   // independent key loads in flight per thread
-
-// Calls f(i, key, valid) for every i in [u0, u1), block-strided, with kBatch
-// loads issued before any is used (so global-memory keys do not serialise on
-// latency).  Every lane of every warp makes the same number of calls.
+// Calls f(i, key, valid) for every i in [u0, u1), block-strided, kBatch loads
+// in flight before use; every lane of every warp makes the same calls.
 template <typename F>
-__device__ __forceinline__ void for_keys(const KeySrc& key, int u0, int u1, const uint32_t* excl,
-                                         F f) {
+__device__ __forceinline__ void for_keys(const KeySrc& key, int u0, int u1, const Excl& ex, F f) {
   for (int base = u0; base < u1; base += kThreads * kBatch) {
     uint32_t kv[kBatch];
     bool ok[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = base + u * kThreads + int(threadIdx.x);
-      ok[u] = i < u1 && !excluded(excl, i);
+      ok[u] = i < u1 && !ex(i);
       kv[u] = ok[u] ? key(i) : 0u;
     }
 #pragma unroll
@@ -91,13 +117,15 @@ __device__ __forceinline__ void for_keys(const KeySrc& key, int u0, int u1, cons
   }
 }
 
-// Over the histogram in descending bin order: the bin holding the need-th key
-// and how many keys of that bin are still needed.  Whole-block call.
-__device__ void find_bin(SelShared& sh, int nbins, int need) {
+// Over hist[0..nbins) in descending bin order: the bin holding the need-th
+// key, and how many keys of that bin are needed (written to sh.bin, sh.need).
+// Whole-block call; nbins is a multiple of kThreads.
+template <typename Sh>
+__device__ void find_bin(Sh& sh, const int* hist, int nbins, int need) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q = nbins / kThreads;   // bins per thread (4 or 1)
+  const int q = nbins / kThreads;
   int local = 0;
-  for (int k = 0; k < q; ++k) local += sh.hist[nbins - 1 - (tid * q + k)];
+  for (int k = 0; k < q; ++k) local += hist[nbins - 1 - (tid * q + k)];
   int incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -107,14 +135,14 @@ __device__ void find_bin(SelShared& sh, int nbins, int need) {
   if (lane == 31) sh.wsum[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = sh.wsum[lane];
+    const int w = lane < kWarps ? sh.wsum[lane] : 0;
     int wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, wi, o);
       if (lane >= o) wi += y;
     }
-    sh.wsum[lane] = wi - w;   // exclusive prefix of the warp sums
+    if (lane < kWarps) sh.wsum[lane] = wi - w;   // exclusive prefix
   }
   __syncthreads();
   const int before = sh.wsum[warp] + incl - local;
@@ -122,7 +150,7 @@ __device__ void find_bin(SelShared& sh, int nbins, int need) {
     int acc = before;
     for (int k = 0; k < q; ++k) {
       const int bin = nbins - 1 - (tid * q + k);
-      const int h = sh.hist[bin];
+      const int h = hist[bin];
       if (acc + h >= need) {
         sh.bin = bin;
         sh.need = need - acc;
@@ -134,27 +162,77 @@ __device__ void find_bin(SelShared& sh, int nbins, int need) {
   __syncthreads();
 }
 
-// Top `cnt` candidates of [u0, u1) minus `excl` by (key desc, index asc):
-// written ascending to out[0..cnt), bits set in `setbits` when given.
-__device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* excl, int cnt,
-                            int32_t* out, uint32_t* setbits, SelShared& sh) {
+// Top `cnt` of the cluster's candidates (this CTA: [s0, s1)) by (key desc,
+// index asc); this CTA writes its selected positions to out at its offset and
+// sets their bits in setbits (when given).  Whole-cluster call.
+template <int CS>
+__device__ void tier_select(cg::cluster_group& cluster, const KeySrc& key, int s0, int s1,
+                            const Excl& ex, int cnt, int32_t* out, uint32_t* setbits,
+                            SelShared<CS>& sh, int& hbuf) {
+  constexpr int kSliceBins = SelShared<CS>::kSliceBins;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (cnt <= 0 || u1 <= u0) return;
+  const int rank = int(cluster.block_rank());
+  if (cnt <= 0) return;   // same for every CTA of the cluster
 
-  // 1. top-12-bit histogram
-  for (int b = tid; b < kBins1; b += kThreads) sh.hist[b] = 0;
+  // ---- level 1: local 12-bit histogram, merged per bin slice
+  for (int b = tid; b < kBins1; b += kThreads) sh.hist1[b] = 0;
   if (tid == 0) sh.ncand = 0;
   __syncthreads();
-  for_keys(key, u0, u1, excl, [&](int, uint32_t kv, bool ok) {
-    if (ok) atomicAdd(&sh.hist[kv >> 20], 1);
+  for_keys(key, s0, s1, ex, [&](int, uint32_t kv, bool ok) {
+    if (ok) atomicAdd(&sh.hist1[kv >> 20], 1);
   });
+  cluster.sync();
+  {
+    int part = 0;
+    for (int j = tid; j < kSliceBins; j += kThreads) {
+      const int bin = rank * kSliceBins + j;
+      int v[CS];
+#pragma unroll
+      for (int q = 0; q < CS; ++q) v[q] = *cluster.map_shared_rank(&sh.hist1[bin], q);
+      int g = 0;
+#pragma unroll
+      for (int q = 0; q < CS; ++q) g += v[q];
+      sh.gsl[j] = g;
+      part += g;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) sh.wsum[warp] = part;
+    __syncthreads();
+    if (tid == 0) {
+      int t = 0;
+      for (int w = 0; w < kWarps; ++w) t += sh.wsum[w];
+      sh.gsl_total = t;
+    }
+  }
+  cluster.sync();
+  // which rank's bin slice holds the cnt-th key (slices in descending order)
+  if (tid == 0) {
+    int acc = 0;
+    sh.slice = 0;
+    sh.need1 = cnt;
+    for (int q = CS - 1; q >= 0; --q) {
+      const int t = *cluster.map_shared_rank(&sh.gsl_total, q);
+      if (acc + t >= cnt) {
+        sh.slice = q;
+        sh.need1 = cnt - acc;
+        break;
+      }
+      acc += t;
+    }
+  }
   __syncthreads();
-  find_bin(sh, kBins1, cnt);
-  const uint32_t b1 = uint32_t(sh.bin);
+  const int rs = sh.slice;
+  // copy that slice's merged counts into local scratch (hist1 is free now:
+  // every remote read of it finished before the last cluster barrier)
+  for (int j = tid; j < kSliceBins; j += kThreads) sh.hist1[j] = *cluster.map_shared_rank(&sh.gsl[j], rs);
+  __syncthreads();
+  find_bin(sh, sh.hist1, kSliceBins, sh.need1);
+  const uint32_t b1 = uint32_t(rs * kSliceBins + sh.bin);
   int need = sh.need;
 
-  // 2. gather the keys of the threshold bin (one atomic per warp)
-  for_keys(key, u0, u1, excl, [&](int, uint32_t kv, bool ok) {
+  // ---- gather this slice's keys of the threshold bin (one atomic per warp)
+  for_keys(key, s0, s1, ex, [&](int, uint32_t kv, bool ok) {
     const bool hit = ok && (kv >> 20) == b1;
     const uint32_t ball = __ballot_sync(0xffffffffu, hit);
     if (ball) {
@@ -168,37 +246,49 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
   __syncthreads();
   const int ncand = sh.ncand;
   const bool listed = ncand <= kCandCap;
+
+  // ---- levels 2 and 3: 10-bit histograms of the candidates, merged
   uint32_t prefix = b1 << 20;
-  // two 10-bit passes over the list (or over all candidates when it overflowed)
   for (int pass = 0; pass < 2; ++pass) {
     const int shift = 10 - 10 * pass;
     const uint32_t hi_mask = 0xFFFFFFFFu << (shift + 10);
-    __syncthreads();
-    for (int b = tid; b < kBins2; b += kThreads) sh.hist[b] = 0;
+    int* h = sh.hist2[hbuf];
+    for (int b = tid; b < kBins2; b += kThreads) h[b] = 0;
     __syncthreads();
     if (listed) {
       for (int c = tid; c < ncand; c += kThreads) {
         const uint32_t kv = sh.cand[c];
-        if ((kv & hi_mask) == prefix) atomicAdd(&sh.hist[(kv >> shift) & 1023u], 1);
+        if ((kv & hi_mask) == prefix) atomicAdd(&h[(kv >> shift) & 1023u], 1);
       }
     } else {
-      for_keys(key, u0, u1, excl, [&](int, uint32_t kv, bool ok) {
-        if (ok && (kv & hi_mask) == prefix) atomicAdd(&sh.hist[(kv >> shift) & 1023u], 1);
+      for_keys(key, s0, s1, ex, [&](int, uint32_t kv, bool ok) {
+        if (ok && (kv & hi_mask) == prefix) atomicAdd(&h[(kv >> shift) & 1023u], 1);
       });
     }
+    cluster.sync();
+    for (int j = tid; j < kBins2; j += kThreads) {
+      int v[CS];
+#pragma unroll
+      for (int q = 0; q < CS; ++q) v[q] = *cluster.map_shared_rank(&h[j], q);
+      int g = 0;
+#pragma unroll
+      for (int q = 0; q < CS; ++q) g += v[q];
+      sh.hist1[j] = g;   // merged, local scratch
+    }
     __syncthreads();
-    find_bin(sh, kBins2, need);
+    find_bin(sh, sh.hist1, kBins2, need);
     prefix |= uint32_t(sh.bin) << shift;
     need = sh.need;
+    hbuf ^= 1;   // the other buffer next: remote readers of this one may still run
   }
   const uint32_t T = prefix;
 
-  // 3. order-preserving compaction over 32-aligned warp chunks
-  const int a0 = u0 & ~31;
-  const int span = u1 - a0;
+  // ---- compaction: local counts, cluster prefix, ordered writes
+  const int a0 = s0 & ~31;
+  const int span = s1 - a0;
   const int chunk = (((span + kWarps - 1) / kWarps) + 31) & ~31;
   const int w0 = a0 + warp * chunk;
-  const int w1 = min(w0 + chunk, u1);
+  const int w1 = min(w0 + chunk, s1);
   int ngt = 0, neq = 0;
   for (int gb = w0; gb < w1; gb += 32 * kBatch) {
     uint32_t kv[kBatch];
@@ -206,7 +296,7 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = gb + 32 * u + lane;
-      cv[u] = i >= u0 && i < w1 && !excluded(excl, i);
+      cv[u] = i >= s0 && i < w1 && !ex(i);
       kv[u] = cv[u] ? key(i) : 0u;
     }
 #pragma unroll
@@ -220,7 +310,27 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
     sh.weq[warp] = neq;
   }
   __syncthreads();
-  int gt_before = 0, eq_before = 0;
+  if (tid == 0) {
+    int g = 0, e = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      g += sh.wgt[w];
+      e += sh.weq[w];
+    }
+    sh.cnt_gt = g;
+    sh.cnt_eq = e;
+  }
+  cluster.sync();
+  if (tid == 0) {
+    int g = 0, e = 0;
+    for (int q = 0; q < rank; ++q) {
+      g += *cluster.map_shared_rank(&sh.cnt_gt, q);
+      e += *cluster.map_shared_rank(&sh.cnt_eq, q);
+    }
+    sh.gt_before = g;
+    sh.eq_before = e;
+  }
+  __syncthreads();
+  int gt_before = sh.gt_before, eq_before = sh.eq_before;
   for (int w = 0; w < warp; ++w) {
     gt_before += sh.wgt[w];
     eq_before += sh.weq[w];
@@ -234,7 +344,7 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = gb + 32 * u + lane;
-      cv[u] = i >= u0 && i < w1 && !excluded(excl, i);
+      cv[u] = i >= s0 && i < w1 && !ex(i);
       kv[u] = cv[u] ? key(i) : 0u;
     }
 #pragma unroll
@@ -247,7 +357,8 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
       const bool sel = isgt || (iseq && (eq_run + __popc(eqb & lt)) < need);
       const uint32_t selb = __ballot_sync(0xffffffffu, sel);
       if (sel) out[pos + __popc(selb & lt)] = i;
-      if (setbits && lane == 0 && g0 < w1) setbits[g0 >> 5] |= selb;
+      // slice-local bitmap word of positions g0 .. g0 + 31 (g0 - a0 is 32-aligned)
+      if (setbits && lane == 0 && g0 < w1) setbits[(g0 - a0) >> 5] |= selb;
       pos += __popc(selb);
       eq_run += __popc(eqb);
     }
@@ -255,23 +366,28 @@ __device__ void tier_select(const KeySrc& key, int u0, int u1, const uint32_t* e
   __syncthreads();
 }
 
+template <int CS>
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_constant__ SelectArgs A) {
   extern __shared__ __align__(16) unsigned char dsm[];
-  SelShared& sh = *reinterpret_cast<SelShared*>(dsm);
-  unsigned char* rest = dsm + ((sizeof(SelShared) + 15) & ~size_t(15));
+  SelShared<CS>& sh = *reinterpret_cast<SelShared<CS>*>(dsm);
+  unsigned char* rest = dsm + ((sizeof(SelShared<CS>) + 15) & ~size_t(15));
   pdl_launch_dependents();
   pdl_wait();
-  const int b = blockIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = int(cluster.block_rank());
+  const int b = blockIdx.x / CS;
   const int tid = threadIdx.x;
   int32_t* out = A.out + size_t(b) * A.k;
   const int L = A.seq_len[b];
+  // the early cases below are decided per sequence, so every CTA of the
+  // cluster leaves together, before any cluster barrier
   if (L < 0 || L > A.Lcap) {
-    if (tid == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
-    for (int j = tid; j < A.k; j += kThreads) out[j] = -1;
+    if (tid == 0 && rank == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
+    for (int j = rank * kThreads + tid; j < A.k; j += CS * kThreads) out[j] = -1;
     return;
   }
   if (A.k >= L) {
-    for (int j = tid; j < A.k; j += kThreads) out[j] = j < L ? j : -1;
+    for (int j = rank * kThreads + tid; j < A.k; j += CS * kThreads) out[j] = j < L ? j : -1;
     return;
   }
   const int s_eff = min(A.sinks, L);
@@ -279,56 +395,136 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   const int nP = s_eff + (L - w0);
   const int m1 = min(A.m, A.k - nP);
   const int f = A.k - nP - m1;
-  for (int j = tid; j < nP; j += kThreads) out[j] = j < s_eff ? j : w0 + (j - s_eff);
+  if (rank == 0)
+    for (int j = tid; j < nP; j += kThreads) out[j] = j < s_eff ? j : w0 + (j - s_eff);
 
-  const int nwords = (A.Lcap + 31) >> 5;
+  // this CTA's slice of the unprotected positions [s_eff, w0)
+  const int per = (((w0 - s_eff) + CS - 1) / CS + 31) & ~31;
+  const int s0 = min(w0, s_eff + rank * per);
+  const int s1 = min(w0, s0 + per);
+  const int nwords = (per + 63) / 32;   // bits of positions from (s0 & ~31)
   uint32_t* keys = A.cache_keys ? reinterpret_cast<uint32_t*>(rest) : nullptr;
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(rest + (A.cache_keys ? size_t(A.Lcap) * 4 : 0));
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(rest + (A.cache_keys ? size_t(A.slice_cap) * 4 : 0));
   for (int w = tid; w < nwords; w += kThreads) bitmap[w] = 0u;
+  int hbuf = 0;
 
   for (int ch = 0; ch < 2; ++ch) {
     const float* row = A.imp + (size_t(b) * 2 + ch) * A.Lcap;
     if (keys) {
-      for (int base = s_eff; base < w0; base += kThreads * kBatch) {
+      for (int base = s0; base < s1; base += kThreads * kBatch) {
         float v[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           const int i = base + u * kThreads + tid;
-          v[u] = i < w0 ? row[i] : 0.f;
+          v[u] = i < s1 ? row[i] : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           const int i = base + u * kThreads + tid;
-          if (i < w0) keys[i] = key_of(v[u], A.err);
+          if (i < s1) keys[i - s0] = key_of(v[u], A.err);
         }
       }
     }
     __syncthreads();
-    KeySrc src{keys, row, A.err};
-    if (ch == 0) tier_select(src, s_eff, w0, nullptr, m1, out + nP, bitmap, sh);
-    else tier_select(src, s_eff, w0, bitmap, f, out + nP + m1, nullptr, sh);
-    __syncthreads();
+    KeySrc src{keys, row, s0, A.err};
+    if (ch == 0) {
+      tier_select(cluster, src, s0, s1, Excl{nullptr, 0}, m1, out + nP, bitmap, sh, hbuf);
+    } else {
+      tier_select(cluster, src, s0, s1, Excl{bitmap, s0 & ~31}, f, out + nP + m1, nullptr, sh,
+                  hbuf);
+    }
   }
+  cluster.sync();   // no CTA leaves while another may still read its shared memory
+}
+
+template <int CS>
+size_t smem_bytes(int slice_cap, int cache_keys) {
+  return ((sizeof(SelShared<CS>) + 15) & ~size_t(15)) + (cache_keys ? size_t(slice_cap) * 4 : 0) +
+         size_t(slice_cap + 64) / 32 * 4;
+}
+
+int slice_cap_of(int Lcap, int cs) { return int(size_t((Lcap + cs - 1) / cs + 31) & ~size_t(31)); }
+
+// Shared-memory bytes of one CTA for cluster size CS; sets cache_keys and slice_cap.
+template <int CS>
+size_t plan_smem(SelectArgs& a) {
+  a.slice_cap = slice_cap_of(a.Lcap, CS);
+  a.cache_keys = smem_bytes<CS>(a.slice_cap, 1) <= kSmemBudget ? 1 : 0;
+  return smem_bytes<CS>(a.slice_cap, a.cache_keys);
+}
+
+template <int CS>
+cudaError_t launch_cs(const SelectArgs& a0, cudaStream_t stream, bool query_only, int* max_clusters) {
+  SelectArgs a = a0;
+  const size_t smem = plan_smem<CS>(a);
+  auto kern = select_kernel<CS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.B * CS);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = CS;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  if (query_only) {
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(max_clusters, kern, &cfg);
+  }
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+cudaError_t launch_any(int cs, const SelectArgs& a, cudaStream_t stream, bool query_only, int* n) {
+  switch (cs) {
+    case 1: return launch_cs<1>(a, stream, query_only, n);
+    case 2: return launch_cs<2>(a, stream, query_only, n);
+    case 4: return launch_cs<4>(a, stream, query_only, n);
+    case 8: return launch_cs<8>(a, stream, query_only, n);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// How many clusters of cs CTAs can run at once for this Lcap on the current
+// device (cached per device, cluster size and Lcap).
+int max_active_clusters(int cs, const SelectArgs& a) {
+  struct Entry {
+    int dev, cs, Lcap, n;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : cache)
+    if (e.dev == dev && e.cs == cs && e.Lcap == a.Lcap) return e.n;
+  int n = 0;
+  if (launch_any(cs, a, nullptr, true, &n) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache.push_back({dev, cs, a.Lcap, n});
+  return n;
 }
 
 }  // namespace
 
-int select_cache_keys(int Lcap) {
-  const size_t need = sizeof(SelShared) + 16 + size_t(Lcap) * 4 + size_t((Lcap + 31) / 32) * 4;
-  return need <= kSmemBudget ? 1 : 0;
-}
-
-size_t select_smem_bytes(int Lcap, int cache_keys) {
-  return ((sizeof(SelShared) + 15) & ~size_t(15)) + (cache_keys ? size_t(Lcap) * 4 : 0) +
-         size_t((Lcap + 31) / 32) * 4;
+int select_cluster_size(const SelectArgs& a) {
+  // the largest cluster whose B clusters are all resident at once; one CTA
+  // per sequence when even pairs do not fit
+  for (int cs = 8; cs >= 2; cs /= 2)
+    if (a.B <= max_active_clusters(cs, a)) return cs;
+  return 1;
 }
 
 cudaError_t select_launch(const SelectArgs& a, cudaStream_t stream) {
-  const size_t smem = select_smem_bytes(a.Lcap, a.cache_keys);
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(smem));
-  if (e != cudaSuccess) return e;
-  return launch_pdl(select_kernel, dim3(a.B), dim3(kThreads), smem, stream, a);
+  return launch_any(select_cluster_size(a), a, stream, false, nullptr);
 }
 
 }  // namespace dustin

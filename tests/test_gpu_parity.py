@@ -105,6 +105,33 @@ def test_select_long_cache_global_keys():
     assert np.array_equal(I.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("B", [20, 48, 100, 300])
+def test_select_many_sequences(B):
+    """Batches too large for one 8-CTA cluster per sequence at once run with
+    smaller clusters (down to one CTA per sequence); results stay exact."""
+    L, k, s, w, m = 3000, 400, 8, 64, 100
+    Lcap = L + 64
+    keys = random_importance(B, B, Lcap, ties=bool(B % 2))
+    rng = np.random.default_rng(B)
+    seq = rng.integers(k - 50, L + 1, size=B).astype(np.int32)
+    p = dk.Params(B, Lcap, 4, s, w, m, k)
+    I = dk.dustin_select(p, torch.as_tensor(keys, device="cuda"), torch.as_tensor(seq, device="cuda"))
+    ref, _ = O.select(keys.astype(np.float64), seq, k, s, w, m)
+    assert np.array_equal(I.cpu().numpy(), ref)
+
+
+def test_select_uncached_keys():
+    """Slices too long for shared memory read their keys from global memory."""
+    B, L, k = 2, 500000, 4096
+    Lcap = L + 64
+    keys = random_importance(11, B, Lcap, ties=False)
+    seq = np.array([L, 480001], dtype=np.int32)
+    p = dk.Params(B, Lcap, 4, 16, 512, 1024, k)
+    I = dk.dustin_select(p, torch.as_tensor(keys, device="cuda"), torch.as_tensor(seq, device="cuda"))
+    ref, _ = O.select(keys.astype(np.float64), seq, k, 16, 512, 1024)
+    assert np.array_equal(I.cpu().numpy(), ref)
+
+
 def test_select_nan_key_flagged():
     B, L, Lcap = 1, 512, 576
     keys = random_importance(9, B, Lcap)
