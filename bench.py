@@ -19,6 +19,7 @@ step time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -66,6 +67,36 @@ def algorithmic_bytes(wl, L=None, B=None):
                            + B * T * wl.Hq * wl.d * 2 + B * T * wl.Hq * wl.d * 4)
     return dict(score_kernel=k_reads, score=score, select=select, verify=verify,
                 step=score + select + verify, dense=dense)
+
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "score_stream_kernel.dram_traffic.txt")
+TRAFFIC_SOURCES = ("sparse_kv_verify_gb300/csrc/score.cu", "sparse_kv_verify_gb300/csrc/common.cuh")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(sequences: int):
+    """DRAM bytes (read + write) of one stream-kernel launch over `sequences`
+    sequences, scaled from the ncu capture recorded in TRAFFIC_FILE; None when
+    there is no capture or the kernel source has changed since it was taken."""
+    try:
+        fields = {}
+        with open(TRAFFIC_FILE) as fh:
+            for ln in fh:
+                if "=" in ln and not ln.startswith("#"):
+                    k, v = ln.strip().split("=", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("source_sha256_16") != kernel_source_hash():
+            return None
+        return float(fields["dram_bytes_per_sequence"]) * sequences
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def max_over_ranks(x: float, dist, device) -> float:
@@ -313,7 +344,7 @@ def gpu_arm(args, rank, world, dist):
     flags = dk.check(call.ws)
     if flags:
         raise RuntimeError(f"device flags {flags:#x} after warm-up")
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    n_launch, group = call.launches()
     barrier()
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(local)
@@ -323,19 +354,26 @@ def gpu_arm(args, rank, world, dist):
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for i in range(args.steps):
-            call(events=ev[i])
+            call()
         t_end.record(stream)
         torch.cuda.synchronize(dev)
     clocks = sampler.result()
     barrier()
     total_ms = t_start.elapsed_time(t_end)
-    stage = {k: [] for k in ("score_kernel", "score_reduce", "select", "verify")}
+    step_ms = max_over_ranks(total_ms / args.steps, dist, dev)
+
+    # ---- per-stage breakdown (separate steps: the stage events themselves
+    # cost a little and are kept out of the timed region above)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        call(events=ev[i])
+    torch.cuda.synchronize(dev)
+    stage = {k: [] for k in ("score_stream_group0", "score", "select", "verify")}
     for e in ev:
-        stage["score_kernel"].append(e[0].elapsed_time(e[1]))
-        stage["score_reduce"].append(e[1].elapsed_time(e[2]))
+        stage["score_stream_group0"].append(e[0].elapsed_time(e[1]))
+        stage["score"].append(e[0].elapsed_time(e[2]))
         stage["select"].append(e[2].elapsed_time(e[3]))
         stage["verify"].append(e[3].elapsed_time(e[4]))
-    step_ms = max_over_ranks(total_ms / args.steps, dist, dev)
 
     if args.profile:
         # profiling run (ncu): warm-up and timed steps only
@@ -393,8 +431,10 @@ def gpu_arm(args, rank, world, dist):
         return 0
 
     peak, peak_kind = peak_hbm()
-    sk_ms = statistics.mean(stage["score_kernel"])
-    achieved = ab["score_kernel"] / (sk_ms * 1e-3) / 1e9
+    # dominant kernel: the score stream kernel of the first sequence group
+    sk_ms = statistics.mean(stage["score_stream_group0"])
+    sk_bytes = algorithmic_bytes(wl, B=group)["score_kernel"]
+    achieved = sk_bytes / (sk_ms * 1e-3) / 1e9
     stage_us = {k: statistics.mean(v) * 1e3 for k, v in stage.items()}
     value = world * ab["step"] / (step_ms * 1e-3) / 1e9
     line = {
@@ -404,7 +444,7 @@ def gpu_arm(args, rank, world, dist):
         "data": "synthetic", "config": config_block(args),
         "step_us": step_ms * 1e3,
         "stage_us": stage_us,
-        "stage_gbs": {"score": ab["score"] / (stage_us["score_kernel"] + stage_us["score_reduce"]) / 1e3,
+        "stage_gbs": {"score": ab["score"] / stage_us["score"] / 1e3,
                       "select": ab["select"] / stage_us["select"] / 1e3,
                       "verify": ab["verify"] / stage_us["verify"] / 1e3},
         "algorithmic_bytes_per_step": ab["step"],
@@ -414,13 +454,15 @@ def gpu_arm(args, rank, world, dist):
                   "frac_of_hbm": ab["dense"] / (dense_ms * 1e-3) / 1e9 / peak},
         "speedup_vs_dense": {"attention_only": dense_ms / (stage_us["verify"] * 1e-3),
                              "step": dense_ms / step_ms},
-        "roofline": {"kernel": "score_kernel", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": "score_stream_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "algorithmic_bytes_per_launch": ab["score_kernel"]},
+                     "frac": achieved / peak, "traffic": traffic_per_launch(group),
+                     "algorithmic_bytes_per_launch": sk_bytes,
+                     "sequences_per_launch": group},
         "e2e": {"value": world * ab["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": n_launch * args.steps,
+        "launches_per_step": n_launch,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

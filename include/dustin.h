@@ -136,9 +136,10 @@ typedef struct {
   float* importance;                   /* device fp32 [B][2][Lcap] (output) */
   int32_t* i_verify;                   /* device int32 [B][k] (output) */
   cudaEvent_t* stage_events;           /* NULL, or host array of 5 events recorded on
-                                          the stream: before score, after the score
-                                          kernel, after the score reduce, after select,
-                                          after verify */
+                                          the stream: before score, after the stream
+                                          kernel of the first scoring group (before its
+                                          normalise kernel), after all score kernels,
+                                          after select, after verify */
 } dustin_step;
 
 /* Library version string (static storage). */
@@ -215,6 +216,15 @@ int dustin_kv_append(const dustin_params* p, int32_t n_layers, const dustin_kv* 
 
 /* score -> select -> sparse verify of every layer, on one stream. */
 int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Host-only query (no device work): how many kernels one dustin_verify_step
+ * call with these arguments launches, and how many sequences each scoring
+ * group holds.  Scoring runs over groups of *group_size sequences so that a
+ * group's logits stay resident in L2; each group takes two kernels (stream,
+ * normalise), then select and verify take one each.  Returns DUSTIN_EINVAL /
+ * DUSTIN_ERANGE for arguments dustin_verify_step would reject while planning
+ * the scoring. */
+int dustin_step_launches(const dustin_step* s, int32_t* n_launches, int32_t* group_size);
 
 /* Bytes of the library-owned scratch array used by dustin_score_noalloc. */
 #define DUSTIN_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -26,7 +26,7 @@ MAX_SRH, MAX_PAIRS, MAX_LAYERS, MAX_QROWS, MAX_LCAP = 32, 32, 16, 128, 1 << 20
 
 EXPORTS = ["dustin_version", "dustin_workspace_bytes", "dustin_workspace_init", "dustin_check",
            "dustin_score", "dustin_select", "dustin_verify_attn", "dense_verify_attn",
-           "dustin_kv_append", "dustin_verify_step"]
+           "dustin_kv_append", "dustin_verify_step", "dustin_step_launches"]
 
 
 class DustinError(RuntimeError):
@@ -107,6 +107,7 @@ def lib():
                                        POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_void_p,
                                        c_void_p, c_size_t, c_void_p]
         L.dustin_verify_step.argtypes = [POINTER(CStep), c_void_p, c_size_t, c_void_p]
+        L.dustin_step_launches.argtypes = [POINTER(CStep), POINTER(c_int32), POINTER(c_int32)]
         L.dustin_score_noalloc.argtypes = [POINTER(CParams), POINTER(CSignal), POINTER(CSignal),
                                            POINTER(CSRH), c_int32, c_void_p, c_void_p, c_void_p]
         L.dustin_score_noalloc.restype = ctypes.c_int
@@ -379,10 +380,17 @@ class StepCall:
                           _ptr(self.i_verify, torch.int32), None)
         self.events = events
 
+    def launches(self):
+        """(kernels one call launches, sequences per scoring group)."""
+        n, g = c_int32(0), c_int32(0)
+        _check("dustin_step_launches",
+               lib().dustin_step_launches(ctypes.byref(self.step), ctypes.byref(n), ctypes.byref(g)))
+        return n.value, g.value
+
     def __call__(self, stream=None, events=None):
         """Runs the step.  ``events``: optional 5 torch.cuda.Event(enable_timing=True)
-        recorded before score, after the score kernel, after the score reduce,
-        after select and after verify."""
+        recorded before score, after the first scoring group's stream kernel,
+        after all score kernels, after select and after verify."""
         ev = events if events is not None else self.events
         if ev is not None:
             for e in ev:

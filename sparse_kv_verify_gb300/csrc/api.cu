@@ -259,7 +259,7 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
 
 int launch_score(const dustin_params* p, const dustin_signal* draft, const dustin_signal* target,
                  const ScorePlan& pl, const int32_t* seq_len, float* importance, void* ws,
-                 cudaStream_t stream, cudaEvent_t mid = nullptr) {
+                 cudaStream_t stream, cudaEvent_t after_first_stream = nullptr) {
   static thread_local ScoreArgs a;   // large (tensor maps): keep it off the stack
   std::memset(&a, 0, sizeof(a));
   int rank[DUSTIN_MAX_SRH];
@@ -308,9 +308,9 @@ int launch_score(const dustin_params* p, const dustin_signal* draft, const dusti
     if (grid > a.total_cost / wmax) grid = a.total_cost / wmax;
     if (grid < 1) grid = 1;
     a.grid = int(grid);
-    if (score_launch(a, pl.launch, stream) != cudaSuccess) return DUSTIN_ECUDA;
+    if (score_launch(a, pl.launch, stream, b0 == 0 ? after_first_stream : nullptr) != cudaSuccess)
+      return DUSTIN_ECUDA;
   }
-  if (mid && cudaEventRecord(mid, stream) != cudaSuccess) return DUSTIN_ECUDA;
   return DUSTIN_OK;
 }
 
@@ -539,6 +539,17 @@ int dustin_kv_append(const dustin_params* p, int32_t n_layers, const dustin_kv* 
     L.vsb = v[l].sb; L.vsh = v[l].sh; L.vsl = v[l].sl;
   }
   return append_launch(a, stream) == cudaSuccess ? DUSTIN_OK : DUSTIN_ECUDA;
+}
+
+int dustin_step_launches(const dustin_step* s, int32_t* n_launches, int32_t* group_size) {
+  if (!s || !n_launches || !group_size) return DUSTIN_EINVAL;
+  static thread_local ScorePlan pl;
+  const int st = build_score_plan(&s->p, s->draft, s->target, s->srh, s->n_srh, &pl);
+  if (st != DUSTIN_OK) return st;
+  const int groups = (s->p.B + pl.nb - 1) / pl.nb;
+  *n_launches = 2 * groups + 2;   // stream + normalise per group, select, verify
+  *group_size = pl.nb;
+  return DUSTIN_OK;
 }
 
 int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStream_t stream) {

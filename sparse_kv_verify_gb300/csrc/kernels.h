@@ -120,7 +120,10 @@ constexpr int kScoreGridMax = 256;
 size_t score_stream_smem();
 int score_rows_per_tile(int D);
 int score_tile_cost(int D, int npairs);
-cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream);
+// Launches the stream and normalise kernels of one sequence group; records
+// after_stream (if given) between the two.
+cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream,
+                         cudaEvent_t after_stream = nullptr);
 
 // ------------------------------------------------------------------ select
 

@@ -474,7 +474,8 @@ int score_tile_cost(int D, int npairs) {
   return 1000 + score_rows_per_tile(D) * npairs / 2;
 }
 
-cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream) {
+cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream,
+                         cudaEvent_t after_stream) {
   cudaError_t e;
   switch (pl.NT) {
     case 1: e = launch_stream<1>(a, pl, stream); break;
@@ -484,6 +485,7 @@ cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
+  if (after_stream && (e = cudaEventRecord(after_stream, stream)) != cudaSuccess) return e;
   dim3 grid((a.Lcap + kNormChunk - 1) / kNormChunk, a.nb);
   return launch_pdl(score_norm_kernel, grid, dim3(kNormThreads), 0, stream, a);
 }

@@ -142,3 +142,32 @@ def test_step_rejects_null_and_too_many_layers(L):
     assert lib.dustin_verify_step(None, 0x100000, 1 << 20, None) == -1
     assert lib.dustin_check(None, None, None) == -5
     assert lib.dustin_workspace_init(None, 256, None) == -5
+
+
+def test_step_launch_count(L):
+    """The launch-count query plans like dustin_verify_step: two kernels per
+    scoring group, then select and verify."""
+    from sparse_kv_verify_gb300 import binding as bd
+    lib = L.lib()
+
+    def step(B, Lcap):
+        kv_t = (bd.CKV * 1)(bd.CKV(0x10000, 8, 128, 8 * Lcap * 128, Lcap * 128, 128))
+        kv_d = (bd.CKV * 1)(bd.CKV(0x20000, 2, 64, 2 * Lcap * 64, Lcap * 64, 64))
+        q = (ctypes.c_void_p * 1)(0x30000)
+        tgt = bd.CSignal(1, 64, 6, q, kv_t)
+        dft = bd.CSignal(1, 14, 5, q, kv_d)
+        srh = (bd.CSRH * 8)(*[bd.CSRH(1, 0, h) for h in (0, 16, 32, 48)],
+                            *[bd.CSRH(0, 0, h) for h in (0, 3, 7, 10)])
+        lay = (bd.CVerifyLayer * 1)()
+        s = bd.CStep(bd.CParams(B, Lcap, 5, 16, 256, 512, 2048), ctypes.pointer(dft),
+                     ctypes.pointer(tgt), srh, 8, 64, 1, lay, 0x40000, 0x50000, 0x60000, None)
+        n, g = ctypes.c_int32(0), ctypes.c_int32(0)
+        st = lib.dustin_step_launches(ctypes.byref(s), ctypes.byref(n), ctypes.byref(g))
+        return st, n.value, g.value, (dft, tgt, srh, lay, kv_t, kv_d, q)
+
+    st, n, g, _ = step(2, 4096)
+    assert (st, n, g) == (0, 4, 2)              # one group
+    st, n, g, _ = step(16, 32832)               # 44 logits rows of 32 K positions per sequence
+    assert st == 0 and 1 <= g < 16 and n == 2 * (-(-16 // g)) + 2
+    assert lib.dustin_step_launches(None, ctypes.byref(ctypes.c_int32()),
+                                    ctypes.byref(ctypes.c_int32())) == -1
