@@ -37,8 +37,9 @@ constexpr int kStages = 6;
 constexpr int kConsumers = 8;                        // 8 warps x 16 rows = 128 rows
 constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int kMaxKs = 8;                            // d / 16 for d = 128
-constexpr int kNormThreads = 128;
-constexpr int kNormChunk = 4 * kNormThreads;         // positions per normalise CTA
+constexpr int kNormThreads = 256;
+constexpr int kNormChunk = 1024;                     // positions per normalise CTA
+constexpr int kNormRows = 16;                        // logits rows in flight per thread
 
 __device__ __forceinline__ uint32_t tile_addr(uint32_t st, int D, int r, int c) {
   // element (row r, column c) of a tile stored as two TMA boxes of
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
   }
 }
 
-__global__ void __launch_bounds__(kNormThreads) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
+__global__ void __launch_bounds__(kNormThreads, 2) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
   // one row per (slab, pair): logits offset, merged max M and 1 / sum
   __shared__ long long roff[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
   __shared__ float Mg[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
@@ -408,37 +409,55 @@ __global__ void __launch_bounds__(kNormThreads) score_norm_kernel(const __grid_c
   }
   __syncthreads();
   const int base = blockIdx.x * kNormChunk;
-  // each thread: 4 consecutive positions (one float4 per logits row; rows are
-  // padded to a multiple of 32 floats, so the loads are aligned and in bounds)
-  const int pos = base + 4 * threadIdx.x;
-  constexpr int kBatch = 16;
-  int r0 = 0;
-  for (int c = 0; c < 2; ++c) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const int rn = nrow[c];
+  // A warp covers 32 positions per pass: lane = (row group rg, position quad);
+  // a thread sums rows rg, rg + 4, ... of its 4 positions with every load of
+  // a batch in flight, then the 4 row groups are reduced with shuffles.
+  // (Rows are padded to a multiple of 32 floats, so the float4 loads are
+  // aligned and in bounds.)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = lane & 7, rg = lane >> 3;
+  const int n0 = nrow[0], nr = nrow[0] + nrow[1];
+  for (int sub = 0; sub < kNormChunk; sub += kNormThreads) {
+    const int pos = base + sub + warp * 32 + quad * 4;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     if (pos < L) {
-      for (int r = 0; r < rn; r += kBatch) {
-        float4 l[kBatch];
+      for (int rb = rg; rb < nr; rb += 4 * kNormRows) {
+        float4 l[kNormRows];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-          if (r + u < rn) l[u] = __ldcs(reinterpret_cast<const float4*>(A.logits + roff[r0 + r + u] + pos));
+        for (int u = 0; u < kNormRows; ++u) {
+          const int r = rb + 4 * u;
+          if (r < nr) l[u] = __ldcs(reinterpret_cast<const float4*>(A.logits + roff[r] + pos));
+        }
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          if (r + u < rn) {
-            const float M = Mg[r0 + r + u], I = Ig[r0 + r + u];
-            acc[0] += fast_exp2(l[u].x - M) * I;
-            acc[1] += fast_exp2(l[u].y - M) * I;
-            acc[2] += fast_exp2(l[u].z - M) * I;
-            acc[3] += fast_exp2(l[u].w - M) * I;
+        for (int u = 0; u < kNormRows; ++u) {
+          const int r = rb + 4 * u;
+          if (r < nr) {
+            const float M = Mg[r], I = Ig[r];
+            const int c = r < n0 ? 0 : 1;
+            acc[c][0] += fast_exp2(l[u].x - M) * I;
+            acc[c][1] += fast_exp2(l[u].y - M) * I;
+            acc[c][2] += fast_exp2(l[u].z - M) * I;
+            acc[c][3] += fast_exp2(l[u].w - M) * I;
           }
         }
       }
     }
-    r0 += rn;
-    float* out = A.importance + (size_t(b) * 2 + c) * A.Lcap;
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (pos + e < A.Lcap) out[pos + e] = (pos + e < L) ? acc[e] : 0.f;
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[c][e] += __shfl_xor_sync(0xffffffffu, acc[c][e], 8);
+        acc[c][e] += __shfl_xor_sync(0xffffffffu, acc[c][e], 16);
+      }
+    if (rg == 0) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float* out = A.importance + (size_t(b) * 2 + c) * A.Lcap;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (pos + e < A.Lcap) out[pos + e] = (pos + e < L) ? acc[c][e] : 0.f;
+      }
+    }
   }
   // the logits of this chunk are dead: drop them from L2 without write-back
   __syncthreads();

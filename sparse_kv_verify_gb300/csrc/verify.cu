@@ -72,8 +72,10 @@ __device__ __forceinline__ int cta_of(long long x, long long total, int G) {
   return int(((x + 1) * G + total - 1) / total) - 1;
 }
 
+// Up to 3 resident CTAs per SM (96 threads per m-tile pair of warps at <= 112
+// registers): the gathers of one CTA overlap the MMAs of the others.
 template <int D, int MT, int NST>
-__global__ void __launch_bounds__(64 * MT) verify_kernel(const __grid_constant__ VerifyArgs A) {
+__global__ void __launch_bounds__(64 * MT, MT <= 3 ? 3 : 1) verify_kernel(const __grid_constant__ VerifyArgs A) {
   using Ly = Lay<D, MT, NST>;
   constexpr int NTH = 64 * MT;
   constexpr int RS = Ly::RS;
@@ -187,7 +189,8 @@ __global__ void __launch_bounds__(64 * MT) verify_kernel(const __grid_constant__
     for (int x = 0; x < NOT; ++x) o[x][0] = o[x][1] = o[x][2] = o[x][3] = 0.f;
     float mrow[2] = {-INFINITY, -INFINITY};
     float lrow[2] = {0.f, 0.f};
-    uint32_t qa[NKS][4];
+    // A fragments are re-read from shared memory two k-steps at a time
+    const uint32_t qb = smem_u32(Qs) + (16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1)) * RS + 16 * (lane >> 4);
     const int r0 = 16 * mt + (lane >> 2);
     const int tr0 = r0 / GQ, tr1 = (r0 + 8) / GQ;
 
@@ -202,15 +205,6 @@ __global__ void __launch_bounds__(64 * MT) verify_kernel(const __grid_constant__
       if (i + NST - 1 < n) issue_tile(i + NST - 1);
       cp_async_commit();
 
-      if (i == 0) {
-        const uint32_t qb = smem_u32(Qs);
-#pragma unroll
-        for (int ks = 0; ks < NKS; ++ks) {
-          const int row = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
-          const int col = 16 * ks + 8 * (lane >> 4);
-          ldmatrix_x4(qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], qb + row * RS + col * 2);
-        }
-      }
       const uint32_t Kt = smem_u32(ring + size_t(i % NST) * Ly::stage_bytes);
       const uint32_t Vt = Kt + TK * RS;
       const int* slot = idxs + (i % (NST + 1)) * TK;
@@ -222,15 +216,18 @@ __global__ void __launch_bounds__(64 * MT) verify_kernel(const __grid_constant__
 #pragma unroll
       for (int j = 0; j < NJ; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) {
+      for (int ks = 0; ks < NKS; ks += 2) {
+        uint32_t qa[2][4];
+        ldmatrix_x4(qa[0][0], qa[0][1], qa[0][2], qa[0][3], qb + ks * 32);
+        ldmatrix_x4(qa[1][0], qa[1][1], qa[1][2], qa[1][3], qb + ks * 32 + 32);
 #pragma unroll
-        for (int ks = 0; ks < NKS; ks += 2) {
+        for (int j = 0; j < NJ; ++j) {
           uint32_t b0, b1, b2, b3;
           const int row = kb0 + 8 * j + (lane & 7);
           const int col = 16 * ks + 8 * (lane >> 3);
           ldmatrix_x4(b0, b1, b2, b3, Kt + row * RS + col * 2);
-          mma_bf16_16816(sacc[j], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-          mma_bf16_16816(sacc[j], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
+          mma_bf16_16816(sacc[j], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1);
+          mma_bf16_16816(sacc[j], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
         }
       }
 #pragma unroll
@@ -243,6 +240,10 @@ __global__ void __launch_bounds__(64 * MT) verify_kernel(const __grid_constant__
           sacc[j][e] = valid ? sacc[j][e] * A.scale_log2 : -INFINITY;
         }
       }
+      // Online softmax with a lazily moved reference: mrow is the reference
+      // the exponentials are taken against; it only moves (and O and the row
+      // sum are rescaled) when a tile's max passes it by more than 2^8, so
+      // every p = 2^(s - mrow) stays <= 256 and most tiles skip the rescale.
 #pragma unroll
       for (int hi = 0; hi < 2; ++hi) {
         float mx = -INFINITY;
@@ -250,10 +251,17 @@ __global__ void __launch_bounds__(64 * MT) verify_kernel(const __grid_constant__
         for (int j = 0; j < NJ; ++j) mx = fmaxf(mx, fmaxf(sacc[j][2 * hi], sacc[j][2 * hi + 1]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mnew = fmaxf(mrow[hi], mx);
-        const float basev = (mnew == -INFINITY) ? 0.f : mnew;
-        const float alpha = fast_exp2(mrow[hi] - basev);
-        mrow[hi] = mnew;
+        if (mx > mrow[hi] + 8.f) {          // also the first tile with a valid key
+          const float alpha = fast_exp2(mrow[hi] - mx);   // 0 while mrow is -inf
+          mrow[hi] = mx;
+          lrow[hi] *= alpha;
+#pragma unroll
+          for (int x = 0; x < NOT; ++x) {
+            o[x][2 * hi] *= alpha;
+            o[x][2 * hi + 1] *= alpha;
+          }
+        }
+        const float basev = (mrow[hi] == -INFINITY) ? 0.f : mrow[hi];
         float ls = 0.f;
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
@@ -264,12 +272,7 @@ __global__ void __launch_bounds__(64 * MT) verify_kernel(const __grid_constant__
             ls += p;
           }
         }
-        lrow[hi] = lrow[hi] * alpha + ls;
-#pragma unroll
-        for (int x = 0; x < NOT; ++x) {
-          o[x][2 * hi] *= alpha;
-          o[x][2 * hi + 1] *= alpha;
-        }
+        lrow[hi] += ls;
       }
 #pragma unroll
       for (int kk = 0; kk < NJ / 2; ++kk) {
