@@ -6,24 +6,29 @@
 //
 // One thread-block cluster of CS CTAs per sequence (CS = 8, 4, 2 or 1: the
 // largest size whose B clusters are all resident at once); CTA r owns a
-// contiguous slice of the unprotected positions.  Importance values are non-negative
-// fp32, so their bit patterns order like the values.  Each tier finds the
-// exact threshold key T of its top-cnt (descending key, ties to the lower
-// index) by a three-level radix select whose histograms are merged across the
-// cluster through distributed shared memory:
-//   level 1  a 4096-bin histogram of the top 12 bits (sign, exponent and 3
-//            mantissa bits) -- fine enough that shared-memory atomics rarely
-//            collide; the merged histogram gives the bin that holds the
-//            cnt-th key,
-//   level 2  keys of that bin are gathered into a small per-CTA list and two
-//            10-bit histograms of the list give T and how many keys equal to T
-//            are needed,
-//   level 3  each CTA counts its keys > T and == T, the cluster exchanges the
-//            counts, and every CTA writes its selected positions (every key > T
-//            and the lowest-index keys == T) ascending at its offset.
-// If a threshold bin holds more keys than a CTA's list can take (heavy ties),
-// that CTA's refinement histograms scan its whole slice instead.  The draft
-// tier is recorded in a per-slice bitmap that the target tier skips.
+// contiguous slice of the unprotected positions.  Importance values are
+// non-negative fp32, so their bit patterns order like the values.  Each tier
+// finds the exact threshold key T of its top-cnt (descending key, ties to the
+// lower index):
+//   level 1  4096-bin histograms of the top 12 bits (sign, exponent and 3
+//            mantissa bits) of both channels are built while the keys are
+//            staged in shared memory; per tier they are merged across the
+//            cluster through distributed shared memory (each rank merges one
+//            slice of the bins), which gives the bin b1 that holds the cnt-th
+//            key.  The draft tier's winners are taken out of the target
+//            histogram as they are written.
+//   pass A   one pass over the CTA's keys gathers the keys of bin b1 with their
+//            positions and counts, per warp chunk, the keys above bin b1.
+//   exact T  every CTA pulls all ranks' bin-b1 keys and finds T and the number
+//            of keys equal to T that are taken with two local 10-bit radix
+//            passes -- no cluster barrier -- and, from the same lists, how many
+//            keys above T and equal to T lower ranks and lower warp chunks hold.
+//   write    one ordered pass writes every key above T and the lowest-index
+//            keys equal to T at their offsets (the draft tier also marks them
+//            in a per-slice bitmap that the target tier skips).
+// If the threshold bin holds more keys than the candidate lists take (heavy
+// ties), T is found with histograms merged across the cluster instead, over
+// the candidate lists where they fit and over whole slices where they do not.
 #include <cooperative_groups.h>
 
 #include <mutex>
@@ -42,7 +47,8 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins1 = 4096;      // top 12 bits
 constexpr int kBins2 = 1024;      // 10 bits
-constexpr int kCandCap = 4096;
+constexpr int kCandCap = 2048;    // (key, position) candidates per CTA
+constexpr int kPullCap = 4096;    // candidate keys of all ranks pulled into one CTA
 constexpr int kBatch = 8;         // independent key loads in flight per thread
 constexpr size_t kSmemBudget = 220 * 1024;
 
@@ -51,19 +57,24 @@ constexpr size_t kSmemBudget = 220 * 1024;
 template <int CS>
 struct SelShared {
   static constexpr int kSliceBins = kBins1 / CS;
-  int hist1[kBins1];         // level-1 histogram of this slice (later: merged scratch)
+  static constexpr int kScratch = kSliceBins > kBins2 ? kSliceBins : kBins2;
+  int h1[2][kBins1];         // level-1 histograms of this CTA's keys, per channel
   int gsl[kSliceBins];       // merged level-1 counts of this rank's bin slice
-  int hist2[2][kBins2];      // level-2/3 histograms of this slice (double buffered)
-  uint32_t cand[kCandCap];
-  int wsum[kWarps];
-  int wgt[kWarps];
-  int weq[kWarps];
-  int gsl_total;
-  int ncand;
-  int cnt_gt, cnt_eq;
-  int bin, need;
-  int slice, need1;
-  int gt_before, eq_before;
+  int scratch[kScratch];     // a merged slice copy / local radix histograms
+  union {
+    uint32_t pulled[kPullCap];   // every rank's threshold-bin keys, in rank order
+    int hist2[2][kBins2];        // or: cluster-merged refinement histograms (heavy ties)
+  };
+  uint32_t ckey[kCandCap];   // this CTA's keys of the threshold bin ...
+  int cpos[kCandCap];        // ... and their positions
+  int wabove[kWarps];        // per warp chunk: keys above the threshold bin
+  int wgt[kWarps], weq[kWarps], wsum[kWarps];
+  int rgt[CS], req[CS];      // per rank: pulled keys above / equal to T
+  int poff[CS + 1];          // offsets of the ranks' lists in pulled
+  int gsl_total, ncand, n_above;
+  int bin, need, slice, need1;
+  int gt_before, eq_before, cnt_gt, cnt_eq;
+  int overflow;
 };
 
 __device__ __forceinline__ uint32_t key_of(float v, int* err) {
@@ -99,6 +110,18 @@ struct Excl {
   }
 };
 
+// The slice [s0, s1) cut into one contiguous, 32-aligned chunk per warp (the
+// order in which positions are written).
+struct Chunks {
+  int a0, chunk;
+  __device__ Chunks(int s0, int s1) {
+    a0 = s0 & ~31;
+    chunk = (((s1 - a0 + kWarps - 1) / kWarps) + 31) & ~31;
+    if (chunk == 0) chunk = 32;
+  }
+  __device__ __forceinline__ int of(int i) const { return (i - a0) / chunk; }
+};
+
 // Calls f(i, key, valid) for every i in [u0, u1), block-strided, kBatch loads
 // in flight before use; every lane of every warp makes the same calls.
 template <typename F>
@@ -109,7 +132,7 @@ __device__ __forceinline__ void for_keys(const KeySrc& key, int u0, int u1, cons
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = base + u * kThreads + int(threadIdx.x);
-      ok[u] = i < u1 && !ex(i);
+      ok[u] = i >= key.base && i < u1 && !ex(i);
       kv[u] = ok[u] ? key(i) : 0u;
     }
 #pragma unroll
@@ -162,92 +185,18 @@ __device__ void find_bin(Sh& sh, const int* hist, int nbins, int need) {
   __syncthreads();
 }
 
-// Top `cnt` of the cluster's candidates (this CTA: [s0, s1)) by (key desc,
-// index asc); this CTA writes its selected positions to out at its offset and
-// sets their bits in setbits (when given).  Whole-cluster call.
+// Heavy ties: the threshold key T below bin b1 from 10-bit histograms merged
+// across the cluster (over the candidate lists where every CTA's fits, over
+// the whole slice where it does not), then the per-warp and per-rank counts
+// of keys above / equal to T.  Whole-cluster call; returns T, sets need.
 template <int CS>
-__device__ void tier_select(cg::cluster_group& cluster, const KeySrc& key, int s0, int s1,
-                            const Excl& ex, int cnt, int32_t* out, uint32_t* setbits,
-                            SelShared<CS>& sh, int& hbuf) {
-  constexpr int kSliceBins = SelShared<CS>::kSliceBins;
+__device__ uint32_t slow_threshold(cg::cluster_group& cluster, const KeySrc& key, int s0, int s1,
+                                   const Excl& ex, const Chunks& ck, uint32_t b1, int& need,
+                                   SelShared<CS>& sh, int& hbuf) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = int(cluster.block_rank());
-  if (cnt <= 0) return;   // same for every CTA of the cluster
-
-  // ---- level 1: local 12-bit histogram, merged per bin slice
-  for (int b = tid; b < kBins1; b += kThreads) sh.hist1[b] = 0;
-  if (tid == 0) sh.ncand = 0;
-  __syncthreads();
-  for_keys(key, s0, s1, ex, [&](int, uint32_t kv, bool ok) {
-    if (ok) atomicAdd(&sh.hist1[kv >> 20], 1);
-  });
-  cluster.sync();
-  {
-    int part = 0;
-    for (int j = tid; j < kSliceBins; j += kThreads) {
-      const int bin = rank * kSliceBins + j;
-      int v[CS];
-#pragma unroll
-      for (int q = 0; q < CS; ++q) v[q] = *cluster.map_shared_rank(&sh.hist1[bin], q);
-      int g = 0;
-#pragma unroll
-      for (int q = 0; q < CS; ++q) g += v[q];
-      sh.gsl[j] = g;
-      part += g;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    if (lane == 0) sh.wsum[warp] = part;
-    __syncthreads();
-    if (tid == 0) {
-      int t = 0;
-      for (int w = 0; w < kWarps; ++w) t += sh.wsum[w];
-      sh.gsl_total = t;
-    }
-  }
-  cluster.sync();
-  // which rank's bin slice holds the cnt-th key (slices in descending order)
-  if (tid == 0) {
-    int acc = 0;
-    sh.slice = 0;
-    sh.need1 = cnt;
-    for (int q = CS - 1; q >= 0; --q) {
-      const int t = *cluster.map_shared_rank(&sh.gsl_total, q);
-      if (acc + t >= cnt) {
-        sh.slice = q;
-        sh.need1 = cnt - acc;
-        break;
-      }
-      acc += t;
-    }
-  }
-  __syncthreads();
-  const int rs = sh.slice;
-  // copy that slice's merged counts into local scratch (hist1 is free now:
-  // every remote read of it finished before the last cluster barrier)
-  for (int j = tid; j < kSliceBins; j += kThreads) sh.hist1[j] = *cluster.map_shared_rank(&sh.gsl[j], rs);
-  __syncthreads();
-  find_bin(sh, sh.hist1, kSliceBins, sh.need1);
-  const uint32_t b1 = uint32_t(rs * kSliceBins + sh.bin);
-  int need = sh.need;
-
-  // ---- gather this slice's keys of the threshold bin (one atomic per warp)
-  for_keys(key, s0, s1, ex, [&](int, uint32_t kv, bool ok) {
-    const bool hit = ok && (kv >> 20) == b1;
-    const uint32_t ball = __ballot_sync(0xffffffffu, hit);
-    if (ball) {
-      int slot0 = 0;
-      if (lane == 0) slot0 = atomicAdd(&sh.ncand, __popc(ball));
-      slot0 = __shfl_sync(0xffffffffu, slot0, 0);
-      const int slot = slot0 + __popc(ball & ((1u << lane) - 1u));
-      if (hit && slot < kCandCap) sh.cand[slot] = kv;
-    }
-  });
-  __syncthreads();
   const int ncand = sh.ncand;
   const bool listed = ncand <= kCandCap;
-
-  // ---- levels 2 and 3: 10-bit histograms of the candidates, merged
   uint32_t prefix = b1 << 20;
   for (int pass = 0; pass < 2; ++pass) {
     const int shift = 10 - 10 * pass;
@@ -257,7 +206,7 @@ __device__ void tier_select(cg::cluster_group& cluster, const KeySrc& key, int s
     __syncthreads();
     if (listed) {
       for (int c = tid; c < ncand; c += kThreads) {
-        const uint32_t kv = sh.cand[c];
+        const uint32_t kv = sh.ckey[c];
         if ((kv & hi_mask) == prefix) atomicAdd(&h[(kv >> shift) & 1023u], 1);
       }
     } else {
@@ -273,23 +222,18 @@ __device__ void tier_select(cg::cluster_group& cluster, const KeySrc& key, int s
       int g = 0;
 #pragma unroll
       for (int q = 0; q < CS; ++q) g += v[q];
-      sh.hist1[j] = g;   // merged, local scratch
+      sh.scratch[j] = g;
     }
     __syncthreads();
-    find_bin(sh, sh.hist1, kBins2, need);
+    find_bin(sh, sh.scratch, kBins2, need);
     prefix |= uint32_t(sh.bin) << shift;
     need = sh.need;
     hbuf ^= 1;   // the other buffer next: remote readers of this one may still run
   }
   const uint32_t T = prefix;
-
-  // ---- compaction: local counts, cluster prefix, ordered writes
-  const int a0 = s0 & ~31;
-  const int span = s1 - a0;
-  const int chunk = (((span + kWarps - 1) / kWarps) + 31) & ~31;
-  const int w0 = a0 + warp * chunk;
-  const int w1 = min(w0 + chunk, s1);
+  // per-warp counts of keys above / equal to T in this CTA's chunks
   int ngt = 0, neq = 0;
+  const int w0 = ck.a0 + warp * ck.chunk, w1 = min(w0 + ck.chunk, s1);
   for (int gb = w0; gb < w1; gb += 32 * kBatch) {
     uint32_t kv[kBatch];
     bool cv[kBatch];
@@ -330,6 +274,183 @@ __device__ void tier_select(cg::cluster_group& cluster, const KeySrc& key, int s
     sh.eq_before = e;
   }
   __syncthreads();
+  return T;
+}
+
+// Top `cnt` of the cluster's candidates (this CTA: [s0, s1) of key, minus ex)
+// by (key desc, index asc), given this CTA's level-1 histogram h of them;
+// writes this CTA's selected positions to out at its offset, and for the draft
+// tier sets their bits in setbits and takes their target keys (sub) out of the
+// target histogram.  Whole-cluster call.
+template <int CS>
+__device__ void tier_select(cg::cluster_group& cluster, const KeySrc& key, int s0, int s1,
+                            const Excl& ex, int cnt, int* h, int32_t* out, uint32_t* setbits,
+                            const KeySrc* sub, SelShared<CS>& sh, int& hbuf) {
+  constexpr int kSliceBins = SelShared<CS>::kSliceBins;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = int(cluster.block_rank());
+  if (cnt <= 0) return;   // same for every CTA of the cluster
+  const Chunks ck(s0, s1);
+
+  // ---- level 1: merge this rank's bin slice of every rank's histogram
+  cluster.sync();                                   // A: every histogram complete
+  // (ncand is reset only now: until every rank has passed barrier A, another
+  // rank may still be reading this rank's previous candidate list)
+  if (tid < kWarps) sh.wabove[tid] = 0;
+  if (tid == 0) sh.ncand = 0;
+  {
+    int part = 0;
+    for (int j = tid; j < kSliceBins; j += kThreads) {
+      const int bin = rank * kSliceBins + j;
+      int v[CS];
+#pragma unroll
+      for (int q = 0; q < CS; ++q) v[q] = *cluster.map_shared_rank(&h[bin], q);
+      int g = 0;
+#pragma unroll
+      for (int q = 0; q < CS; ++q) g += v[q];
+      sh.gsl[j] = g;
+      part += g;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) sh.wsum[warp] = part;
+    __syncthreads();
+    if (tid == 0) {
+      int t = 0;
+      for (int w = 0; w < kWarps; ++w) t += sh.wsum[w];
+      sh.gsl_total = t;
+    }
+  }
+  cluster.sync();                                   // B: every slice merged
+  if (tid == 0) {   // which rank's bin slice holds the cnt-th key (slices in descending order)
+    int acc = 0;
+    sh.slice = 0;
+    sh.need1 = cnt;
+    for (int q = CS - 1; q >= 0; --q) {
+      const int t = *cluster.map_shared_rank(&sh.gsl_total, q);
+      if (acc + t >= cnt) {
+        sh.slice = q;
+        sh.need1 = cnt - acc;
+        break;
+      }
+      acc += t;
+    }
+  }
+  __syncthreads();
+  const int rs = sh.slice;
+  for (int j = tid; j < kSliceBins; j += kThreads) sh.scratch[j] = *cluster.map_shared_rank(&sh.gsl[j], rs);
+  __syncthreads();
+  find_bin(sh, sh.scratch, kSliceBins, sh.need1);
+  const uint32_t b1 = uint32_t(rs * kSliceBins + sh.bin);
+  int need = sh.need;
+
+  // ---- pass A: keys of bin b1 (with positions); per chunk, keys above bin b1
+  // (walked from the 32-aligned slice start: a warp row of 32 positions lies in
+  // one chunk, so the above-bin count takes one ballot and one atomic per row)
+  const Excl exA{ex.bits, ex.base};
+  for_keys(key, ck.a0, s1, exA, [&](int i, uint32_t kv, bool ok0) {
+    const bool ok = ok0 && i >= s0;
+    const uint32_t bin = kv >> 20;
+    const uint32_t above = __ballot_sync(0xffffffffu, ok && bin > b1);
+    if (above && lane == 0) atomicAdd(&sh.wabove[ck.of(i)], __popc(above));
+    const bool hit = ok && bin == b1;
+    const uint32_t ball = __ballot_sync(0xffffffffu, hit);
+    if (ball) {
+      int slot0 = 0;
+      if (lane == 0) slot0 = atomicAdd(&sh.ncand, __popc(ball));
+      slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+      const int slot = slot0 + __popc(ball & ((1u << lane) - 1u));
+      if (hit && slot < kCandCap) {
+        sh.ckey[slot] = kv;
+        sh.cpos[slot] = i;
+      }
+    }
+  });
+  __syncthreads();
+  if (tid == 0) {
+    int a = 0;
+    for (int w = 0; w < kWarps; ++w) a += sh.wabove[w];
+    sh.n_above = a;
+  }
+  cluster.sync();                                   // C: candidate lists published
+  if (tid == 0) {
+    int off = 0, over = 0;
+    for (int q = 0; q < CS; ++q) {
+      const int n = *cluster.map_shared_rank(&sh.ncand, q);
+      sh.poff[q] = off;
+      if (n > kCandCap) over = 1;
+      off += n;
+    }
+    sh.poff[CS] = off;
+    sh.overflow = over || off > kPullCap;
+  }
+  __syncthreads();
+
+  uint32_t T;
+  if (!sh.overflow) {
+    // ---- exact threshold from every rank's bin-b1 keys, locally
+    const int total = sh.poff[CS];
+#pragma unroll
+    for (int q = 0; q < CS; ++q) {
+      const int o = sh.poff[q], n = sh.poff[q + 1] - o;
+      const uint32_t* src = cluster.map_shared_rank(sh.ckey, q);
+      for (int j = tid; j < n; j += kThreads) sh.pulled[o + j] = src[j];
+    }
+    uint32_t prefix = b1 << 20;
+    for (int pass = 0; pass < 2; ++pass) {
+      const int shift = 10 - 10 * pass;
+      const uint32_t hi_mask = 0xFFFFFFFFu << (shift + 10);
+      for (int b = tid; b < kBins2; b += kThreads) sh.scratch[b] = 0;
+      __syncthreads();
+      for (int j = tid; j < total; j += kThreads) {
+        const uint32_t kv = sh.pulled[j];
+        if ((kv & hi_mask) == prefix) atomicAdd(&sh.scratch[(kv >> shift) & 1023u], 1);
+      }
+      __syncthreads();
+      find_bin(sh, sh.scratch, kBins2, need);
+      prefix |= uint32_t(sh.bin) << shift;
+      need = sh.need;
+    }
+    T = prefix;
+    // per rank and per warp chunk: keys above / equal to T
+    if (tid < CS) {
+      sh.rgt[tid] = 0;
+      sh.req[tid] = 0;
+    }
+    if (tid < kWarps) {
+      sh.wgt[tid] = sh.wabove[tid];
+      sh.weq[tid] = 0;
+    }
+    __syncthreads();
+    for (int j = tid; j < total; j += kThreads) {
+      const uint32_t kv = sh.pulled[j];
+      if (kv >= T) {
+        int q = 0;
+        while (j >= sh.poff[q + 1]) ++q;
+        atomicAdd(kv > T ? &sh.rgt[q] : &sh.req[q], 1);
+      }
+    }
+    const int ncand = sh.ncand;
+    for (int c = tid; c < ncand; c += kThreads) {
+      const uint32_t kv = sh.ckey[c];
+      if (kv >= T) atomicAdd(kv > T ? &sh.wgt[ck.of(sh.cpos[c])] : &sh.weq[ck.of(sh.cpos[c])], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int g = 0, e = 0;
+      for (int q = 0; q < rank; ++q) {
+        g += *cluster.map_shared_rank(&sh.n_above, q) + sh.rgt[q];
+        e += sh.req[q];
+      }
+      sh.gt_before = g;
+      sh.eq_before = e;
+    }
+    __syncthreads();
+  } else {
+    T = slow_threshold(cluster, key, s0, s1, ex, ck, b1, need, sh, hbuf);
+  }
+
+  // ---- ordered write: every key above T and the lowest-index keys equal to T
   int gt_before = sh.gt_before, eq_before = sh.eq_before;
   for (int w = 0; w < warp; ++w) {
     gt_before += sh.wgt[w];
@@ -338,6 +459,7 @@ __device__ void tier_select(cg::cluster_group& cluster, const KeySrc& key, int s
   int pos = gt_before + min(eq_before, need);
   int eq_run = eq_before;
   const uint32_t lt = (1u << lane) - 1u;
+  const int w0 = ck.a0 + warp * ck.chunk, w1 = min(w0 + ck.chunk, s1);
   for (int gb = w0; gb < w1; gb += 32 * kBatch) {
     uint32_t kv[kBatch];
     bool cv[kBatch];
@@ -356,9 +478,12 @@ __device__ void tier_select(cg::cluster_group& cluster, const KeySrc& key, int s
       const uint32_t eqb = __ballot_sync(0xffffffffu, iseq);
       const bool sel = isgt || (iseq && (eq_run + __popc(eqb & lt)) < need);
       const uint32_t selb = __ballot_sync(0xffffffffu, sel);
-      if (sel) out[pos + __popc(selb & lt)] = i;
+      if (sel) {
+        out[pos + __popc(selb & lt)] = i;
+        if (sub) atomicAdd(&sh.h1[1][(*sub)(i) >> 20], -1);
+      }
       // slice-local bitmap word of positions g0 .. g0 + 31 (g0 - a0 is 32-aligned)
-      if (setbits && lane == 0 && g0 < w1) setbits[(g0 - a0) >> 5] |= selb;
+      if (setbits && lane == 0 && g0 < w1) setbits[(g0 - ck.a0) >> 5] |= selb;
       pos += __popc(selb);
       eq_run += __popc(eqb);
     }
@@ -367,7 +492,7 @@ __device__ void tier_select(cg::cluster_group& cluster, const KeySrc& key, int s
 }
 
 template <int CS>
-__global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_constant__ SelectArgs A) {
+__global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_constant__ SelectArgs A) {
   extern __shared__ __align__(16) unsigned char dsm[];
   SelShared<CS>& sh = *reinterpret_cast<SelShared<CS>*>(dsm);
   unsigned char* rest = dsm + ((sizeof(SelShared<CS>) + 15) & ~size_t(15));
@@ -403,43 +528,52 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   const int s0 = min(w0, s_eff + rank * per);
   const int s1 = min(w0, s0 + per);
   const int nwords = (per + 63) / 32;   // bits of positions from (s0 & ~31)
-  uint32_t* keys = A.cache_keys ? reinterpret_cast<uint32_t*>(rest) : nullptr;
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(rest + (A.cache_keys ? size_t(A.slice_cap) * 4 : 0));
+  uint32_t* keys0 = A.cache_keys ? reinterpret_cast<uint32_t*>(rest) : nullptr;
+  uint32_t* keys1 = A.cache_keys ? keys0 + A.slice_cap : nullptr;
+  uint32_t* bitmap =
+      reinterpret_cast<uint32_t*>(rest + (A.cache_keys ? size_t(2) * A.slice_cap * 4 : 0));
   for (int w = tid; w < nwords; w += kThreads) bitmap[w] = 0u;
+  for (int j = tid; j < 2 * kBins1; j += kThreads) (&sh.h1[0][0])[j] = 0;
   int hbuf = 0;
+  __syncthreads();
 
-  for (int ch = 0; ch < 2; ++ch) {
-    const float* row = A.imp + (size_t(b) * 2 + ch) * A.Lcap;
-    if (keys) {
-      for (int base = s0; base < s1; base += kThreads * kBatch) {
-        float v[kBatch];
+  // stage both channels' keys (when they fit) and build their level-1 histograms
+  const float* row0 = A.imp + (size_t(b) * 2 + 0) * A.Lcap;
+  const float* row1 = A.imp + (size_t(b) * 2 + 1) * A.Lcap;
+  for (int base = s0; base < s1; base += kThreads * kBatch) {
+    float v0[kBatch], v1[kBatch];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int i = base + u * kThreads + tid;
-          v[u] = i < s1 ? row[i] : 0.f;
-        }
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kThreads + tid;
+      v0[u] = i < s1 ? row0[i] : 0.f;
+      v1[u] = i < s1 ? row1[i] : 0.f;
+    }
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int i = base + u * kThreads + tid;
-          if (i < s1) keys[i - s0] = key_of(v[u], A.err);
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kThreads + tid;
+      if (i < s1) {
+        const uint32_t k0 = key_of(v0[u], A.err), k1 = key_of(v1[u], A.err);
+        if (keys0) {
+          keys0[i - s0] = k0;
+          keys1[i - s0] = k1;
         }
+        atomicAdd(&sh.h1[0][k0 >> 20], 1);
+        atomicAdd(&sh.h1[1][k1 >> 20], 1);
       }
     }
-    __syncthreads();
-    KeySrc src{keys, row, s0, A.err};
-    if (ch == 0) {
-      tier_select(cluster, src, s0, s1, Excl{nullptr, 0}, m1, out + nP, bitmap, sh, hbuf);
-    } else {
-      tier_select(cluster, src, s0, s1, Excl{bitmap, s0 & ~31}, f, out + nP + m1, nullptr, sh,
-                  hbuf);
-    }
   }
+  __syncthreads();
+  const KeySrc src0{keys0, row0, s0, A.err}, src1{keys1, row1, s0, A.err};
+  tier_select(cluster, src0, s0, s1, Excl{nullptr, 0}, m1, &sh.h1[0][0], out + nP, bitmap, &src1,
+              sh, hbuf);
+  tier_select(cluster, src1, s0, s1, Excl{bitmap, s0 & ~31}, f, &sh.h1[1][0], out + nP + m1,
+              nullptr, static_cast<const KeySrc*>(nullptr), sh, hbuf);
   cluster.sync();   // no CTA leaves while another may still read its shared memory
 }
 
 template <int CS>
 size_t smem_bytes(int slice_cap, int cache_keys) {
-  return ((sizeof(SelShared<CS>) + 15) & ~size_t(15)) + (cache_keys ? size_t(slice_cap) * 4 : 0) +
+  return ((sizeof(SelShared<CS>) + 15) & ~size_t(15)) + (cache_keys ? size_t(2) * slice_cap * 4 : 0) +
          size_t(slice_cap + 64) / 32 * 4;
 }
 
