@@ -488,9 +488,10 @@ size_t score_stream_smem() {
 int score_rows_per_tile(int D) { return D == 128 ? kBoxRows : 2 * kBoxRows; }
 
 int score_tile_cost(int D, int npairs) {
-  // 32 KB of K per tile plus the logits it writes (rows x pairs), in units that
-  // match the measured per-tile times of the two tile shapes
-  return 1000 + score_rows_per_tile(D) * npairs / 2;
+  // 32 KB of K per tile plus the logits it writes (rows x pairs); the weight of
+  // the logits term is the one that gave the shortest full score stage on the
+  // 16-sequence, 32 K-position workload (heavier weights gave the same time)
+  return 1000 + score_rows_per_tile(D) * npairs;
 }
 
 cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream,
