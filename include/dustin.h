@@ -214,6 +214,22 @@ int dustin_kv_append(const dustin_params* p, int32_t n_layers, const dustin_kv* 
                      const int32_t* n_accept, int32_t* seq_len, void* ws, size_t ws_bytes,
                      cudaStream_t stream);
 
+/* The literal "compressed target KV cache" of section 3, step 3 of the pages,
+ * for callers that verify several passes against one selection.  For every
+ * layer l, sequence b, KV head g and j < k: row j of kc[l]/vc[l] (bf16
+ * [B][hkv][>= k][d], same hkv and d as k[l]/v[l]) becomes row i_verify[b][j]
+ * of k[l]/v[l]; entries -1 give zero rows, other indices outside
+ * [0, seq_len[b]) give zero rows and set DUSTIN_DEV_INDEX.  seq_len_c[b]
+ * (device, out) = the number of entries of i_verify[b] before its first -1
+ * (the -1 entries must form a suffix, as dustin_select writes them).
+ * dense_verify_attn over (kc, vc, seq_len_c) with Lcap = k then gives the same
+ * result as dustin_verify_attn over (k, v, i_verify).  dustin_verify_attn
+ * itself gathers the rows in-kernel and never writes such a copy. */
+int dustin_compact_kv(const dustin_params* p, int32_t n_layers, const dustin_kv* k,
+                      const dustin_kv* v, const int32_t* i_verify, const int32_t* seq_len,
+                      const dustin_kv* kc, const dustin_kv* vc, int32_t* seq_len_c, void* ws,
+                      size_t ws_bytes, cudaStream_t stream);
+
 /* score -> select -> sparse verify of every layer, on one stream. */
 int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStream_t stream);
 

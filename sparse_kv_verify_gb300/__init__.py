@@ -7,5 +7,6 @@ from . import binding  # noqa: F401
 from .binding import (  # noqa: F401
     DustinError, Params, Signal, VerifyLayer, Workspace, StepCall, workspace, workspace_bytes,
     check, version, lib, kv_view, dustin_score, dustin_select, dustin_verify_attn,
-    dense_verify_attn, dustin_kv_append, dustin_verify_step, dustin_score_noalloc, EXPORTS, LIB_PATH,
+    dense_verify_attn, dustin_kv_append, dustin_compact_kv, dustin_verify_step, dustin_score_noalloc,
+    EXPORTS, LIB_PATH,
     DEV_INDEX, DEV_NAN, DEV_APPEND, DEV_TIMEOUT, DEV_SEQLEN)

@@ -26,7 +26,7 @@ MAX_SRH, MAX_PAIRS, MAX_LAYERS, MAX_QROWS, MAX_LCAP = 32, 32, 16, 128, 1 << 20
 
 EXPORTS = ["dustin_version", "dustin_workspace_bytes", "dustin_workspace_init", "dustin_check",
            "dustin_score", "dustin_select", "dustin_verify_attn", "dense_verify_attn",
-           "dustin_kv_append", "dustin_verify_step", "dustin_step_launches"]
+           "dustin_kv_append", "dustin_verify_step", "dustin_step_launches", "dustin_compact_kv"]
 
 
 class DustinError(RuntimeError):
@@ -108,6 +108,9 @@ def lib():
                                        c_void_p, c_size_t, c_void_p]
         L.dustin_verify_step.argtypes = [POINTER(CStep), c_void_p, c_size_t, c_void_p]
         L.dustin_step_launches.argtypes = [POINTER(CStep), POINTER(c_int32), POINTER(c_int32)]
+        L.dustin_compact_kv.argtypes = [POINTER(CParams), c_int32, POINTER(CKV), POINTER(CKV),
+                                        c_void_p, c_void_p, POINTER(CKV), POINTER(CKV), c_void_p,
+                                        c_void_p, c_size_t, c_void_p]
         L.dustin_score_noalloc.argtypes = [POINTER(CParams), POINTER(CSignal), POINTER(CSignal),
                                            POINTER(CSRH), c_int32, c_void_p, c_void_p, c_void_p]
         L.dustin_score_noalloc.restype = ctypes.c_int
@@ -325,6 +328,27 @@ def dense_verify_attn(p: Params, q, k, v, kb, vb, seq_len, o=None, ws=None,
                                  _ptr(o, torch.float32), ws.ptr, ws.nbytes, _stream(stream))
     _check("dense_verify_attn", st)
     return o
+
+
+def dustin_compact_kv(p: Params, ks, vs, i_verify, seq_len, kcs=None, vcs=None, seq_len_c=None,
+                      ws=None, stream=None):
+    """Copies the selected rows of every layer's caches into compact caches
+    [B][hkv][k][d]; returns (kcs, vcs, seq_len_c)."""
+    n = len(ks)
+    if kcs is None:
+        kcs = [torch.empty((p.B, t.shape[1], p.k, t.shape[3]), dtype=t.dtype, device=t.device) for t in ks]
+    if vcs is None:
+        vcs = [torch.empty((p.B, t.shape[1], p.k, t.shape[3]), dtype=t.dtype, device=t.device) for t in vs]
+    if seq_len_c is None:
+        seq_len_c = torch.empty_like(seq_len)
+    arr = lambda ts: (CKV * n)(*[kv_view(t) for t in ts])
+    if ws is None:
+        ws = workspace(p, device=seq_len.device, stream=stream)
+    st = lib().dustin_compact_kv(ctypes.byref(p.c()), n, arr(ks), arr(vs), _ptr(i_verify, torch.int32),
+                                 _ptr(seq_len, torch.int32), arr(kcs), arr(vcs),
+                                 _ptr(seq_len_c, torch.int32), ws.ptr, ws.nbytes, _stream(stream))
+    _check("dustin_compact_kv", st)
+    return kcs, vcs, seq_len_c
 
 
 def dustin_kv_append(p: Params, ks, vs, kbs, vbs, n_accept, seq_len, ws=None, stream=None):

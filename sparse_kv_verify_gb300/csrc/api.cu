@@ -144,12 +144,6 @@ bool signal_ok(const dustin_signal* s) {
   return s && s->n_layers >= 1 && s->n_layers <= 4096 && s->hq >= 1 && s->nq >= 1 && s->q && s->k;
 }
 
-long long group_tiles(const ScorePlan& pl, int nb) {
-  long long t = 0;
-  for (int i = 0; i < pl.n_slab; ++i) t += (long long)nb * pl.slab[i].tiles;
-  return t;
-}
-
 // Validates the SRH list and plans the score launches.  scratch_off is where
 // the scratch begins in the workspace and scratch_max bounds it (0: no bound
 // beyond the L2 budget).
@@ -539,6 +533,44 @@ int dustin_kv_append(const dustin_params* p, int32_t n_layers, const dustin_kv* 
     L.vsb = v[l].sb; L.vsh = v[l].sh; L.vsl = v[l].sl;
   }
   return append_launch(a, stream) == cudaSuccess ? DUSTIN_OK : DUSTIN_ECUDA;
+}
+
+int dustin_compact_kv(const dustin_params* p, int32_t n_layers, const dustin_kv* k,
+                      const dustin_kv* v, const int32_t* i_verify, const int32_t* seq_len,
+                      const dustin_kv* kc, const dustin_kv* vc, int32_t* seq_len_c, void* ws,
+                      size_t ws_bytes, cudaStream_t stream) {
+  if (!params_ok(p)) return DUSTIN_EINVAL;
+  if (n_layers < 1) return DUSTIN_EINVAL;
+  if (n_layers > DUSTIN_MAX_LAYERS) return DUSTIN_ERANGE;
+  if (!k || !v || !kc || !vc || !i_verify || !seq_len || !seq_len_c) return DUSTIN_EINVAL;
+  if (!ws_ok(ws, ws_bytes, kScratch)) return DUSTIN_EWORKSPACE;
+  CompactArgs a{};
+  a.B = p->B;
+  a.Lcap = p->Lcap;
+  a.k = p->k;
+  a.hkv = k[0].hkv;
+  a.D = k[0].d;
+  a.n_layers = n_layers;
+  a.ivf = i_verify;
+  a.seq_len = seq_len;
+  a.seq_len_c = seq_len_c;
+  a.err = err_word(ws);
+  for (int l = 0; l < n_layers; ++l) {
+    if (!kv_ok(k[l], p->Lcap) || !kv_ok(v[l], p->Lcap)) return DUSTIN_EINVAL;
+    if (!kv_ok(kc[l], p->k) || !kv_ok(vc[l], p->k)) return DUSTIN_EINVAL;
+    for (const dustin_kv* t : {&k[l], &v[l], &kc[l], &vc[l]})
+      if (t->hkv != a.hkv || t->d != a.D) return DUSTIN_EINVAL;
+    CompactLayerDev& L = a.layer[l];
+    L.k = static_cast<const uint16_t*>(k[l].ptr);
+    L.v = static_cast<const uint16_t*>(v[l].ptr);
+    L.kc = static_cast<uint16_t*>(const_cast<void*>(kc[l].ptr));
+    L.vc = static_cast<uint16_t*>(const_cast<void*>(vc[l].ptr));
+    L.ksb = k[l].sb; L.ksh = k[l].sh; L.ksl = k[l].sl;
+    L.vsb = v[l].sb; L.vsh = v[l].sh; L.vsl = v[l].sl;
+    L.kcsb = kc[l].sb; L.kcsh = kc[l].sh; L.kcsl = kc[l].sl;
+    L.vcsb = vc[l].sb; L.vcsh = vc[l].sh; L.vcsl = vc[l].sl;
+  }
+  return compact_launch(a, stream) == cudaSuccess ? DUSTIN_OK : DUSTIN_ECUDA;
 }
 
 int dustin_step_launches(const dustin_step* s, int32_t* n_launches, int32_t* group_size) {

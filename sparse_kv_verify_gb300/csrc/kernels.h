@@ -158,4 +158,25 @@ struct AppendArgs {
 };
 cudaError_t append_launch(const AppendArgs& a, cudaStream_t stream);
 
+// ----------------------------------------------------------------- compact
+
+struct CompactLayerDev {
+  const uint16_t* k;
+  const uint16_t* v;
+  uint16_t* kc;
+  uint16_t* vc;
+  int64_t ksb, ksh, ksl, vsb, vsh, vsl;
+  int64_t kcsb, kcsh, kcsl, vcsb, vcsh, vcsl;
+};
+
+struct CompactArgs {
+  int B, Lcap, k, hkv, D, n_layers;
+  const int32_t* ivf;        // [B][k]
+  const int32_t* seq_len;
+  int32_t* seq_len_c;        // [B] out: compact lengths
+  int* err;
+  CompactLayerDev layer[DUSTIN_MAX_LAYERS];
+};
+cudaError_t compact_launch(const CompactArgs& a, cudaStream_t stream);
+
 }  // namespace dustin

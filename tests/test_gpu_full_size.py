@@ -137,8 +137,8 @@ def test_selection_policies_bit_exact(policy):
 def test_attention_recovery_of_policies():
     """Share of the dense verification attention mass captured by each
     policy's I_verify, on the 8 K-position layer with planted salient keys:
-    the tiered selection recovers at least as much as the sink + window cache
-    and as each single signal alone."""
+    the tiered selection recovers more than the sink + window cache and at
+    least as much as the weaker of the two single signals."""
     wl = WORKLOADS["layer8k"]
     x = generate(wl, device="cuda")
     seq = torch.as_tensor(x.seq_len, device="cuda")
@@ -154,3 +154,20 @@ def test_attention_recovery_of_policies():
     assert arr["dustin"] > arr["streaming"]
     assert arr["dustin"] >= min(arr["draft_only"], arr["target_only"])
     assert all(0.0 < v <= 1.0 + 1e-12 for v in arr.values())
+
+
+def test_collect_two_query_scoring():
+    """Scoring on two query rows only (the first draft look-ahead row and the
+    bonus row of the historical target queries): the caller passes signals
+    holding just those rows, and the scores match the oracle on the same rows."""
+    wl = WORKLOADS["layer8k"]
+    x = generate(wl, device="cuda")
+    seq = torch.as_tensor(x.seq_len, device="cuda")
+    dq = [t[:, :1].contiguous() for t in x.draft_q]          # first draft row
+    hq = [t[:, -1:].contiguous() for t in x.hist_q]          # bonus row
+    imp = dk.dustin_score(params_of(wl), dk.Signal(dq, x.Kd), dk.Signal(hq, x.K), wl.srh, seq)
+    ref = O.score([to_bits(t) for t in dq], [to_bits(t) for t in x.Kd], [to_bits(t) for t in hq],
+                  [to_bits(t) for t in x.K], wl.srh, x.seq_len, wl.Lcap)
+    assert_importance(imp, ref, x.seq_len)
+    # each channel's mass is one per (head, row): 4 heads x 1 row
+    assert np.allclose(ref[0, :, : x.seq_len[0]].sum(axis=1), [4.0, 4.0])

@@ -344,3 +344,28 @@ def test_full_size_dense_sampled(big):
                       to_bits(x.V[0][b:b + 1, g:g + 1]), to_bits(x.Kb[0][b:b + 1, g:g + 1]),
                       to_bits(x.Vb[0][b:b + 1, g:g + 1]), x.seq_len[b:b + 1])
         assert_attention(o[b:b + 1, :, hs], ref)
+
+
+@pytest.mark.parametrize("name,over", [("layer8k", {}), ("tiny", dict(k=1100, n_layers=2))])
+def test_compact_kv_then_dense_equals_sparse_verify(name, over):
+    """The compacted-cache variant: the selected rows copied into compact
+    caches and verified densely give bit-for-bit the sparse verification of
+    the full caches (same keys in the same order), in every layer."""
+    c = Case(WORKLOADS[name].with_(**over))
+    wl, x = c.wl, c.x
+    I_ref, _ = O.select(c.oracle_score(), x.seq_len, wl.k, wl.sinks, wl.window, wl.m)
+    I = torch.as_tensor(I_ref.astype(np.int32), device="cuda")
+    ws = dk.workspace(c.p)
+    kcs, vcs, slc = dk.dustin_compact_kv(c.p, x.K, x.V, I, c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    valid = (I_ref >= 0).sum(axis=1)
+    assert np.array_equal(slc.cpu().numpy(), valid)
+    pc = params_of(wl, Lcap=wl.k)
+    for l in range(wl.n_layers):
+        o_sparse = dk.dustin_verify_attn(c.p, x.Q[l], x.K[l], x.V[l], x.Kb[l], x.Vb[l], I, c.seq)
+        o_dense = dk.dense_verify_attn(pc, x.Q[l], kcs[l], vcs[l], x.Kb[l], x.Vb[l], slc)
+        assert torch.equal(o_sparse, o_dense)
+        b, g = 0, x.K[l].shape[1] - 1
+        rows = I_ref[b][: valid[b]]
+        assert torch.equal(kcs[l][b, g, : valid[b]], x.K[l][b, g, torch.as_tensor(rows, device="cuda")])
+        assert torch.all(kcs[l][b, g, valid[b]:] == 0)
