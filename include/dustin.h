@@ -68,6 +68,7 @@ typedef enum {
 #define DUSTIN_MAX_PAIRS 32         /* (SRH head x query row) pairs sharing one KV head */
 #define DUSTIN_MAX_LAYERS 16        /* layers per verify / append call */
 #define DUSTIN_MAX_QROWS 128        /* (gamma+1) * (Hq/Hkv) verify query rows per KV head */
+#define DUSTIN_MAX_BLOCK 64         /* gamma+1 draft-block rows per verify call */
 #define DUSTIN_MAX_LCAP (1 << 20)   /* positions per cache */
 
 /* A bf16 KV-cache view, element (b, g, pos, j) at

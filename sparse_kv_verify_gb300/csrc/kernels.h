@@ -38,6 +38,15 @@ struct VerifyLayerDev {
   const uint16_t* vb;
   float* o;            // [B][T][hq][D]
   int64_t ksb, ksh, ksl, vsb, vsh, vsl;
+  // cache strides in rows of the gather maps (row = gcd of the strides)
+  int krb, krh, krl, vrb, vrh, vrl;
+};
+
+// TMA maps of one layer: q 3-D (d, hq, B*T), box (64, G, T); k and v 2-D
+// rows of the cache; kb and vb 2-D rows [B*hkv*T][d]; row maps have box
+// (64, 1) for four-row gathers; all with the 128-byte swizzle.
+struct VerifyMapsDev {
+  CUtensorMap q, k, v, kb, vb;
 };
 
 struct VerifyArgs {
@@ -45,7 +54,7 @@ struct VerifyArgs {
   int k;                // budget (sparse); unused for dense
   int dense;            // 1: keys are positions 0..seq_len-1
   int n_layers;
-  int ctx_tiles;        // 32-key tiles of context per unit
+  int ctx_tiles;        // 64-key tiles of context per unit
   int tiles_u;          // ctx_tiles + 1 (the draft-block tile)
   long long total;      // units * tiles_u
   int max_seg;          // partial slots per unit
@@ -57,6 +66,7 @@ struct VerifyArgs {
   float* partial;       // [units][max_seg][slot_floats]: O [NQ][D], m [NQ], l [NQ]
   int* counters;        // [units], zero between launches
   VerifyLayerDev layer[DUSTIN_MAX_LAYERS];
+  VerifyMapsDev maps[DUSTIN_MAX_LAYERS];
 };
 
 struct VerifyLaunch {

@@ -7,21 +7,32 @@
 // entries of I_verify; dense: positions 0..seq_len-1) plus the gamma+1
 // draft-block rows under the causal mask u <= t.
 //
-// Schedule (stream-K): each unit is cut into 32-key tiles followed by one
-// block tile; all units' tiles form one sequence that is split evenly over a
-// grid sized to the GPU's resident capacity, so every CTA moves the same
-// number of bytes whatever B, Hkv and k are.  A CTA walks its range one unit
-// segment at a time.
+// Schedule (stream-K): each unit is cut into 64-key tiles followed by one
+// block tile; all units' tiles form one sequence that is split evenly over one
+// persistent CTA per SM, so every CTA moves the same number of bytes whatever
+// B, Hkv and k are.
 //
-// Data path: every warp issues 16-byte cp.async gathers (zero-filled for
-// padding / out-of-context rows) into a 3-stage ring of 32-key tiles in padded
-// shared-memory rows (2*d + 16 bytes, so ldmatrix is bank-conflict free); the
-// index list runs one stage ahead through shared memory.  The ring is small so
-// that several CTAs share an SM: cp.async reaches HBM bandwidth only with many
-// resident warps.  Two warps share each 16-row m-tile of queries and take one
-// half of every key tile: S = Q K^T and
-// O += P V are bf16 m16n8k16 tensor-core MMAs with fp32 accumulation, with an
-// online softmax in the log2 domain.
+// Roles inside a CTA (warp specialised, handing over through mbarriers):
+//   warps 4-7        loaders, each for every fourth tile: gather the tile's
+//   (loaders)        K and V rows with TMA row gathers (four rows per
+//                    instruction, 128-byte swizzle) into a five-stage ring,
+//                    and a segment's query rows with one tiled TMA load into
+//                    one of two query buffers (a TMA instruction costs its
+//                    warp tens of cycles, so the issue is spread over warps);
+//   warp 8 (MMA)     one thread issues the tensor-core MMAs: S = Q K^T of the
+//                    next tile into one of two S buffers in tensor memory as
+//                    soon as its rows have landed, then O += P V of the
+//                    current tile with P read from tensor memory;
+//   warps 0-3        one thread per query row (tensor-memory lane; warps with
+//                    no query row sit the loop out): online
+//                    softmax of its S row in the log2 domain, with the
+//                    reference max moved only when a tile passes it by more
+//                    than 2^8 (so O is rarely rescaled), P rounded to bf16 and
+//                    stored back to tensor memory; then the epilogue.
+//
+// Rows a tile does not use (I_verify padding, positions past seq_len, block
+// rows past gamma) are loaded from a valid row of the same sequence and given
+// probability zero, so the MMAs only ever see finite data.
 //
 // Combine: a segment that covers a whole unit writes O directly; otherwise it
 // writes (row max, row sum, unnormalised O) to the workspace and the last CTA
@@ -34,37 +45,152 @@ namespace dustin {
 
 namespace {
 
-constexpr int TK = 32;  // keys per tile: small stages so that ~3 CTAs share an SM
-constexpr int NSTAGE = 3;
-constexpr int TKH = TK / 2;   // keys per warp (each m-tile has two warps)
+constexpr int TK = 64;           // keys per tile (and the largest draft block)
+constexpr int NSTAGE = 5;        // K/V ring stages
+constexpr int kSoftmaxWarps = 4;    // one thread per tensor-memory lane
+constexpr int kLoaders = 4;         // loader warps, each issuing every fourth tile
+constexpr int kLoaderWarp0 = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + kLoaders;
+constexpr int NTH = 32 * (kMmaWarp + 1);
+constexpr int kSCol = 0;         // S buffers: columns [0, 64) and [64, 128)
+constexpr int kPCol = 128;       // P buffers (bf16 pairs): [128, 160) and [160, 192)
+static_assert(TK == DUSTIN_MAX_BLOCK, "the draft block must fit one tile");
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(src_bytes)
+template <int D>
+struct TmemCfg {
+  static constexpr int cols = D == 128 ? 512 : 256;
+  static constexpr int o_col = D == 128 ? 256 : 192;
+};
+
+// ---- tcgen05 ---------------------------------------------------------------
+
+// Shared-memory operand descriptor: start, leading and stride byte offsets
+// (each >> 4), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t tc_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((addr >> 4) & 0x3FFFu) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// Instruction descriptor of a bf16 x bf16 -> fp32 MMA of M x N; A K-major, B
+// K-major (b_mn = 0) or MN-major (b_mn = 1).
+__host__ __device__ constexpr uint32_t tc_idesc(int M, int N, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(b_mn) << 16) | (uint32_t(N >> 3) << 17) |
+         (uint32_t(M >> 4) << 24);
+}
+
+// D (tensor memory) (+)= A (shared memory) * B (shared memory)
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          int acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// D (tensor memory) (+)= A (tensor memory: one row per lane, two bf16 per
+// column) * B (shared memory)
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, int acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-template <int D, int MT, int NST>
+// 32 consecutive 32-bit columns of this thread's lane (the load and its wait
+// in one statement, so that no register is read before it has landed).
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// ---- TMA -------------------------------------------------------------------
+
+// Rows r0..r3 x 64 columns from column c of a row map, landing as four
+// consecutive 128-byte rows at dst (swizzled by their shared-memory address).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int c, int r0,
+                                            int r1, int r2, int r3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Bounded wait that ignores the abort flag (drains copies in flight before
+// the CTA exits).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+}
+
+// Named barrier over the first nthr threads (the softmax warps in use).
+__device__ __forceinline__ void softmax_bar(int nthr) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+}
+
+template <int D>
 struct Lay {
-  static constexpr int RS = D * 2 + 16;          // padded row stride (bytes)
-  static constexpr int CH = D / 8;               // 16-byte chunks per row
-  static constexpr int OS = D + 4;               // merge-area row stride (floats)
-  static constexpr size_t q_off = 0;
-  static constexpr size_t q_bytes = size_t(MT) * 16 * RS;
-  static constexpr size_t stage_bytes = size_t(2) * TK * RS;
-  static constexpr size_t ring_off = q_off + q_bytes;
-  static constexpr size_t ring_bytes = NST * stage_bytes;
-  static constexpr size_t merge_bytes = size_t(MT) * 16 * OS * 4 + size_t(MT) * 16 * 8;
-  static constexpr size_t ring_alloc = ring_bytes > merge_bytes ? ring_bytes : merge_bytes;
-  static constexpr size_t idx_off = ring_off + ring_alloc;
-  static constexpr size_t idx_bytes = size_t(NST + 1) * TK * 4;
-  static constexpr size_t misc_off = idx_off + idx_bytes;
-  static constexpr size_t total = misc_off + 16;
+  static constexpr int NP = D / 64;                    // 64-column panels per row
+  static constexpr size_t q_panel = 128 * 128;         // [128 rows][64 columns]
+  static constexpr size_t q_buf = NP * q_panel;
+  static constexpr size_t q_off = 0;                   // two query buffers
+  static constexpr size_t ring_off = q_off + 2 * q_buf;
+  static constexpr size_t kv_panel = size_t(TK) * 128;    // [64 keys][64 columns]
+  static constexpr size_t half_bytes = NP * kv_panel;     // K (or V) of one tile
+  static constexpr size_t stage_bytes = 2 * half_bytes;
+  static constexpr size_t mask_off = ring_off + NSTAGE * stage_bytes;   // [NSTAGE][4] words
+  static constexpr size_t bar_off = mask_off + NSTAGE * 16;
+  // full[NSTAGE], empty[NSTAGE], s_full[2], p_full[2], q_full[2], q_empty[2], pv_done[2]
+  static constexpr int n_bars = 2 * NSTAGE + 10;
+  static constexpr size_t misc_off = bar_off + n_bars * 8;   // tmem base, s_last, abort
+  static constexpr size_t total = misc_off + 16 + 1024;      // + slack for the 1024-byte base
 };
 
 // CTA that owns flattened tile x, for start(c) = c * total / G.
@@ -72,382 +198,434 @@ __device__ __forceinline__ int cta_of(long long x, long long total, int G) {
   return int(((x + 1) * G + total - 1) / total) - 1;
 }
 
-// Up to 3 resident CTAs per SM (96 threads per m-tile pair of warps at <= 112
-// registers): the gathers of one CTA overlap the MMAs of the others.
-template <int D, int MT, int NST>
-__global__ void __launch_bounds__(64 * MT, MT <= 3 ? 3 : 1) verify_kernel(const __grid_constant__ VerifyArgs A) {
-  using Ly = Lay<D, MT, NST>;
-  constexpr int NTH = 64 * MT;
-  constexpr int RS = Ly::RS;
-  constexpr int CH = Ly::CH;
-  constexpr int NKS = D / 16;
-  constexpr int NOT = D / 8;
+// One stream-K segment of this CTA: tiles [ta, ta + n) of unit u.
+struct Seg {
+  int u, ta, n;
+};
+__device__ __forceinline__ Seg next_seg(long long& t, long long t1, int tiles_u) {
+  Seg s;
+  s.u = int(t / tiles_u);
+  s.ta = int(t % tiles_u);
+  const long long rem_t = t1 - t;
+  const int tb = int(rem_t < (long long)(tiles_u - s.ta) ? s.ta + rem_t : tiles_u);
+  s.n = tb - s.ta;
+  t += s.n;
+  return s;
+}
 
-  extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* Qs = smem + Ly::q_off;
-  unsigned char* ring = smem + Ly::ring_off;
-  int* idxs = reinterpret_cast<int*>(smem + Ly::idx_off);
-  volatile int* s_last = reinterpret_cast<volatile int*>(smem + Ly::misc_off);
-  float* mO = reinterpret_cast<float*>(ring);               // merge area (after drain)
-  float* mM = mO + size_t(MT) * 16 * Ly::OS;
-  float* mL = mM + MT * 16;
+template <int D>
+__global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ VerifyArgs A) {
+  using Ly = Lay<D>;
+  using Tm = TmemCfg<D>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* masks = reinterpret_cast<uint32_t*>(smem + Ly::mask_off);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Ly::bar_off);
+  uint64_t* empty = full + NSTAGE;
+  uint64_t* s_full = empty + NSTAGE;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* q_full = p_full + 2;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* pv_done = q_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::misc_off);
+  volatile int* s_last = reinterpret_cast<volatile int*>(smem + Ly::misc_off + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::misc_off + 8);
 
-  pdl_launch_dependents();
-  pdl_wait();
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int mt = warp >> 1, half = warp & 1;
+  const int T = A.T, NQ = A.NQ, GQ = A.G;
+  const int n_act = (NQ + 31) >> 5;   // softmax warps that hold query rows
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 32 * n_act);
+      mbar_init(&q_full[x], 1);
+      mbar_init(&q_empty[x], 1);
+      mbar_init(&pv_done[x], 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp < kSoftmaxWarps) {
+    // query rows past NQ stay zero in both query buffers (the loads write rows
+    // < NQ only), so their scores are exactly zero
+    for (int q = NQ * 8 + tid; q < 128 * 8; q += kSoftmaxWarps * 32)
+#pragma unroll
+      for (int x = 0; x < 2 * Ly::NP; ++x)
+        *reinterpret_cast<uint4*>(smem + Ly::q_off + x * Ly::q_panel + size_t(q) * 16) =
+            make_uint4(0, 0, 0, 0);
+    fence_proxy_async();
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "n"(Tm::cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
   const int G = gridDim.x;
   const long long total = A.total;
   const long long t0 = (long long)blockIdx.x * total / G;
   const long long t1 = (long long)(blockIdx.x + 1) * total / G;
-  const int T = A.T, NQ = A.NQ, GQ = A.G;
   const int tiles_u = A.tiles_u, ctx_tiles = A.ctx_tiles;
   const int units_per_layer = A.B * A.hkv;
 
-  for (long long t = t0; t < t1;) {
-    const int u = int(t / tiles_u);
-    const int ta = int(t % tiles_u);
-    const long long rem_t = t1 - t;
-    const int tb = int(rem_t < (long long)(tiles_u - ta) ? ta + rem_t : tiles_u);
-    t += tb - ta;
-    const int n = tb - ta;
-    const int layer = u / units_per_layer;
-    const int b = (u % units_per_layer) / A.hkv;
-    const int g = u % A.hkv;
-    const VerifyLayerDev& Lr = A.layer[layer];
-    int L = A.seq_len[b];
-    if (L < 0 || L > A.Lcap) {
-      if (tid == 0 && g == 0 && layer == 0 && ta == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
-      L = 0;
-    }
-    const uint16_t* kbase = Lr.k + size_t(b) * Lr.ksb + size_t(g) * Lr.ksh;
-    const uint16_t* vbase = Lr.v + size_t(b) * Lr.vsb + size_t(g) * Lr.vsh;
-    const size_t blk_off = (size_t(b) * A.hkv + g) * T * D;
-
-    // Key index of row r of local tile i, in two halves so that the global
-    // load of I_verify is consumed one iteration after it is issued.
-    auto raw_key = [&](int i, int r) -> int {
-      const int tt = ta + i;
-      if (tt >= ctx_tiles) return r;                     // draft-block tile
-      const int j = tt * TK + r;
-      if (A.dense) return j;
-      return j < A.k ? __ldg(A.ivf + size_t(b) * A.k + j) : -1;
-    };
-    auto checked_key = [&](int i, int raw) -> int {       // -1: masked row
-      const int tt = ta + i;
-      if (tt >= ctx_tiles) return raw < T ? raw : -1;
-      if (A.dense) return raw < L ? raw : -1;
-      if (raw < -1 || raw >= L) {
-        flag_error(A.err, DUSTIN_DEV_INDEX);
-        return -1;
+  if (warp >= kLoaderWarp0 && warp < kLoaderWarp0 + kLoaders) {
+    // =============================================================== loaders
+    // loader warp lw handles the tiles gi = lw (mod kLoaders) of this CTA
+    const int lw = warp - kLoaderWarp0;
+    const int gq = lane & 15;        // this lane's group of four rows
+    const int which = lane >> 4;     // 0: K, 1: V
+    constexpr uint32_t kTileBytes = 2u * TK * D * 2;
+    long long gi = 0;
+    int s = 0;
+    for (long long t = t0; t < t1; ++s) {
+      const Seg sg = next_seg(t, t1, tiles_u);
+      const int layer = sg.u / units_per_layer;
+      const int b = (sg.u % units_per_layer) / A.hkv;
+      const int g = sg.u % A.hkv;
+      const VerifyMapsDev& M = A.maps[layer];
+      const VerifyLayerDev& Lr = A.layer[layer];
+      int L = A.seq_len[b];
+      if (L < 0 || L > A.Lcap) {
+        if (lw == 0 && lane == 0 && g == 0 && layer == 0 && sg.ta == 0)
+          flag_error(A.err, DUSTIN_DEV_SEQLEN);
+        L = 0;
       }
-      return raw;
-    };
-    auto issue_tile = [&](int i) {
-      const int s = i % NST;
-      const int* slot = idxs + (i % (NST + 1)) * TK;
-      const bool blk = (ta + i) >= ctx_tiles;
-      unsigned char* st = ring + size_t(s) * Ly::stage_bytes;
-      for (int q = tid; q < 2 * TK * CH; q += NTH) {
-        const int which = q / (TK * CH);
-        const int rem = q - which * (TK * CH);
-        const int row = rem / CH, ch = rem - (rem / CH) * CH;
-        const int id = slot[row];
-        const bool ok = id >= 0;
-        const uint16_t* src;
-        if (blk) src = (which ? Lr.vb : Lr.kb) + blk_off + size_t(ok ? id : 0) * D + ch * 8;
-        else if (which) src = vbase + size_t(ok ? id : 0) * Lr.vsl + ch * 8;
-        else src = kbase + size_t(ok ? id : 0) * Lr.ksl + ch * 8;
-        cp_async16(st + size_t(which) * TK * RS + size_t(row) * RS + ch * 16, src, ok ? 16u : 0u);
+      // this segment's query rows -> query buffer s % 2
+      const int qb = s & 1;
+      if (s % kLoaders == lw && lane == 0) {
+        if (s >= 2) mbar_wait(&q_empty[qb], uint32_t((s >> 1) - 1) & 1u, A.err, abort_flag);
+        mbar_arrive_expect_tx(&q_full[qb], uint32_t(NQ) * D * 2);
+#pragma unroll
+        for (int h = 0; h < Ly::NP; ++h)
+          tma_load_3d(sbase + uint32_t(Ly::q_off + qb * Ly::q_buf + h * Ly::q_panel), &M.q, h * 64,
+                      g * GQ, b * T, &q_full[qb]);
       }
-    };
-
-    // ------------------------------------------------------------- prologue
-    for (int q = tid; q < MT * 16 * CH; q += NTH) {
-      const int r = q / CH, ch = q - (q / CH) * CH;
-      unsigned char* dst = Qs + size_t(r) * RS + ch * 16;
-      if (r < NQ) {
-        const int tq = r / GQ, hl = r - (r / GQ) * GQ;
-        cp_async16(dst, Lr.q + ((size_t(b) * T + tq) * A.hq + size_t(g) * GQ + hl) * D + ch * 8, 16u);
-      } else {
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    for (int i = 0; i < NST && i < n; ++i)
-      if (tid < TK) idxs[(i % (NST + 1)) * TK + tid] = checked_key(i, raw_key(i, tid));
-    int pf = (tid < TK && NST < n) ? raw_key(NST, tid) : -1;
-    __syncthreads();
+      __syncwarp();
+      const int rb_row = (which ? Lr.vrb : Lr.krb) * b + (which ? Lr.vrh : Lr.krh) * g;
+      const int rl = which ? Lr.vrl : Lr.krl;
+      const int blk_row = (b * A.hkv + g) * T;
+      const CUtensorMap* cmap = which ? &M.v : &M.k;
+      const CUtensorMap* bmap = which ? &M.vb : &M.kb;
+      for (int i = 0; i < sg.n; ++i, ++gi) {
+        if (int(gi % kLoaders) != lw) continue;
+        // raw key indices of this lane's four rows (loaded before the wait)
+        const int tt = sg.ta + i;
+        const bool blk = tt >= ctx_tiles;
+        int raw[4];
 #pragma unroll
-    for (int i = 0; i < NST - 1; ++i) {
-      if (i < n) issue_tile(i);
-      cp_async_commit();
-    }
-
-    float o[NOT][4];
-#pragma unroll
-    for (int x = 0; x < NOT; ++x) o[x][0] = o[x][1] = o[x][2] = o[x][3] = 0.f;
-    float mrow[2] = {-INFINITY, -INFINITY};
-    float lrow[2] = {0.f, 0.f};
-    // A fragments are re-read from shared memory two k-steps at a time
-    const uint32_t qb = smem_u32(Qs) + (16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1)) * RS + 16 * (lane >> 4);
-    const int r0 = 16 * mt + (lane >> 2);
-    const int tr0 = r0 / GQ, tr1 = (r0 + 8) / GQ;
-
-    // ------------------------------------------------------------ main loop
-    for (int i = 0; i < n; ++i) {
-      cp_async_wait<NST - 2>();
-      __syncthreads();
-      if (tid < TK && i + NST < n) {
-        idxs[((i + NST) % (NST + 1)) * TK + tid] = checked_key(i + NST, pf);
-        pf = (i + NST + 1 < n) ? raw_key(i + NST + 1, tid) : -1;
-      }
-      if (i + NST - 1 < n) issue_tile(i + NST - 1);
-      cp_async_commit();
-
-      const uint32_t Kt = smem_u32(ring + size_t(i % NST) * Ly::stage_bytes);
-      const uint32_t Vt = Kt + TK * RS;
-      const int* slot = idxs + (i % (NST + 1)) * TK;
-      const bool blk = (ta + i) >= ctx_tiles;
-      const int kb0 = TKH * half;   // first key of this warp's half
-      constexpr int NJ = TKH / 8;   // 8-key n-tiles per warp
-
-      float sacc[NJ][4];
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < NKS; ks += 2) {
-        uint32_t qa[2][4];
-        ldmatrix_x4(qa[0][0], qa[0][1], qa[0][2], qa[0][3], qb + ks * 32);
-        ldmatrix_x4(qa[1][0], qa[1][1], qa[1][2], qa[1][3], qb + ks * 32 + 32);
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-          uint32_t b0, b1, b2, b3;
-          const int row = kb0 + 8 * j + (lane & 7);
-          const int col = 16 * ks + 8 * (lane >> 3);
-          ldmatrix_x4(b0, b1, b2, b3, Kt + row * RS + col * 2);
-          mma_bf16_16816(sacc[j], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0, b1);
-          mma_bf16_16816(sacc[j], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b2, b3);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int key = kb0 + 8 * j + 2 * (lane & 3) + (e & 1);
-          bool valid = slot[key] >= 0;
-          if (blk) valid = valid && key <= ((e >> 1) ? tr1 : tr0);
-          sacc[j][e] = valid ? sacc[j][e] * A.scale_log2 : -INFINITY;
-        }
-      }
-      // Online softmax with a lazily moved reference: mrow is the reference
-      // the exponentials are taken against; it only moves (and O and the row
-      // sum are rescaled) when a tile's max passes it by more than 2^8, so
-      // every p = 2^(s - mrow) stays <= 256 and most tiles skip the rescale.
-#pragma unroll
-      for (int hi = 0; hi < 2; ++hi) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) mx = fmaxf(mx, fmaxf(sacc[j][2 * hi], sacc[j][2 * hi + 1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        if (mx > mrow[hi] + 8.f) {          // also the first tile with a valid key
-          const float alpha = fast_exp2(mrow[hi] - mx);   // 0 while mrow is -inf
-          mrow[hi] = mx;
-          lrow[hi] *= alpha;
-#pragma unroll
-          for (int x = 0; x < NOT; ++x) {
-            o[x][2 * hi] *= alpha;
-            o[x][2 * hi + 1] *= alpha;
+        for (int j = 0; j < 4; ++j) {
+          const int r = gq * 4 + j;
+          if (blk) raw[j] = r;
+          else if (A.dense) raw[j] = tt * TK + r;
+          else {
+            const int jj = tt * TK + r;
+            raw[j] = jj < A.k ? __ldg(A.ivf + size_t(b) * A.k + jj) : -1;
           }
         }
-        const float basev = (mrow[hi] == -INFINITY) ? 0.f : mrow[hi];
-        float ls = 0.f;
+        const int st = int(gi % NSTAGE);
+        if (gi >= NSTAGE)
+          mbar_wait(&empty[st], uint32_t(gi / NSTAGE - 1) & 1u, A.err, abort_flag);
+        bool valid[4];
+        bool any = false;
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
+        for (int j = 0; j < 4; ++j) {
+          if (blk) valid[j] = raw[j] < T;
+          else if (A.dense) valid[j] = raw[j] < L;
+          else {
+            valid[j] = raw[j] >= 0 && raw[j] < L;
+            if ((raw[j] < -1 || raw[j] >= L) && which == 0) flag_error(A.err, DUSTIN_DEV_INDEX);
+          }
+          any = any || valid[j];
+        }
+        int row[4];
+        const CUtensorMap* map;
+        if (blk) {
+          map = bmap;
 #pragma unroll
-          for (int e = 2 * hi; e < 2 * hi + 2; ++e) {
-            const float p = bf16_round(fast_exp2(sacc[j][e] - basev));
-            sacc[j][e] = p;
-            ls += p;
+          for (int j = 0; j < 4; ++j) row[j] = blk_row + (valid[j] ? raw[j] : 0);
+        } else if (any) {   // some row is in context, so position 0 is valid
+          map = cmap;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) row[j] = rb_row + (valid[j] ? raw[j] : 0) * rl;
+        } else {            // no row in context: read block row 0 instead
+          map = bmap;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) row[j] = blk_row;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t bits = __ballot_sync(0xffffffffu, valid[j]) & 0xFFFFu;
+          if (lane == 0) masks[st * 4 + j] = bits;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
+        __syncwarp();
+        const uint32_t dst = sbase + uint32_t(Ly::ring_off + size_t(st) * Ly::stage_bytes +
+                                              which * Ly::half_bytes) + uint32_t(gq * 512);
+#pragma unroll
+        for (int h = 0; h < Ly::NP; ++h)
+          tma_gather4(dst + uint32_t(h * Ly::kv_panel), map, h * 64, row[0], row[1], row[2], row[3],
+                      &full[st]);
+      }
+    }
+    // every copy issued has landed before the CTA may exit
+    if (lane == 0) {
+      for (long long x = gi - NSTAGE < 0 ? 0 : gi - NSTAGE; x < gi; ++x)
+        if (int(x % kLoaders) == lw) mbar_drain(&full[x % NSTAGE], uint32_t(x / NSTAGE) & 1u);
+      for (int x = s - 2 < 0 ? 0 : s - 2; x < s; ++x)
+        if (x % kLoaders == lw) mbar_drain(&q_full[x & 1], uint32_t(x >> 1) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // =================================================================== MMA
+    if (lane == 0) {
+      constexpr uint32_t kIdS = tc_idesc(128, TK, 0);
+      constexpr uint32_t kIdPV = tc_idesc(128, D, 1);
+      const uint32_t o_tmem = tmem + Tm::o_col;
+      long long gi = 0;
+      int s = 0;
+      // S = Q K^T of tile g2 into S buffer g2 % 2, once its rows have landed
+      auto issue_s = [&](long long g2, uint32_t qbuf) {
+        const int st = int(g2 % NSTAGE);
+        mbar_wait(&full[st], uint32_t(g2 / NSTAGE) & 1u, A.err, abort_flag);
+        tc_fence_after();
+        const uint32_t kst = sbase + uint32_t(Ly::ring_off + size_t(st) * Ly::stage_bytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = uint32_t((kk & 3) * 32);
+          const uint64_t a = tc_desc(qbuf + uint32_t((kk >> 2) * Ly::q_panel) + koff, 16, 1024);
+          const uint64_t bd = tc_desc(kst + uint32_t((kk >> 2) * Ly::kv_panel) + koff, 16, 1024);
+          tc_mma_ss(tmem + uint32_t(kSCol + (g2 & 1) * TK), a, bd, kIdS, kk > 0);
+        }
+        tc_commit(&s_full[g2 & 1]);
+      };
+      for (long long t = t0; t < t1; ++s) {
+        const Seg sg = next_seg(t, t1, tiles_u);
+        const int qb = s & 1;
+        const uint32_t qbuf = sbase + uint32_t(Ly::q_off + qb * Ly::q_buf);
+        mbar_wait(&q_full[qb], uint32_t(s >> 1) & 1u, A.err, abort_flag);
+        issue_s(gi, qbuf);
+        for (int i = 0; i < sg.n; ++i, ++gi) {
+          if (i + 1 < sg.n) issue_s(gi + 1, qbuf);
+          mbar_wait(&p_full[gi & 1], uint32_t(gi >> 1) & 1u, A.err, abort_flag);
+          tc_fence_after();
+          const int st = int(gi % NSTAGE);
+          const uint32_t vst =
+              sbase + uint32_t(Ly::ring_off + size_t(st) * Ly::stage_bytes + Ly::half_bytes);
+          const uint32_t p_tmem = tmem + uint32_t(kPCol + (gi & 1) * (TK / 2));
+#pragma unroll
+          for (int kk = 0; kk < TK / 16; ++kk) {
+            const uint64_t bd = tc_desc(vst + uint32_t(kk * 2048), uint32_t(Ly::kv_panel), 1024);
+            tc_mma_ts(o_tmem, p_tmem + uint32_t(kk * 8), bd, kIdPV, (i > 0 || kk > 0) ? 1 : 0);
+          }
+          tc_commit(&empty[st]);
+          tc_commit(&pv_done[gi & 1]);
+        }
+        tc_commit(&q_empty[qb]);
+      }
+      // every MMA of this CTA has completed
+      if (s > 0) mbar_drain(&q_empty[(s - 1) & 1], uint32_t((s - 1) >> 1) & 1u);
+    }
+    __syncwarp();
+  } else if (warp < kSoftmaxWarps) {
+    // =============================================================== softmax
+    // warps holding query rows run the tiles; every softmax warp takes part
+    // in the combine
+    const bool act_warp = warp < n_act;
+    constexpr int nthr = 32 * kSoftmaxWarps;
+    const int row = tid;             // query row == tensor-memory lane
+    const bool active = row < NQ;
+    const int tq_row = active ? row / GQ : 0;
+    const float scale = A.scale_log2;
+    const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+    const uint32_t o_lane = lane_base + uint32_t(Tm::o_col);
+    long long gi = 0;
+    for (long long t = t0; t < t1;) {
+      const Seg sg = next_seg(t, t1, tiles_u);
+      const int u = sg.u, n = sg.n;
+      const int layer = u / units_per_layer;
+      const int b = (u % units_per_layer) / A.hkv;
+      const int g = u % A.hkv;
+      const VerifyLayerDev& Lr = A.layer[layer];
+      float mref = -INFINITY, lsum = 0.f;   // reference max (log2 domain) and row sum
+      for (int i = 0; act_warp && i < n; ++i, ++gi) {
+        const int st = int(gi % NSTAGE);
+        mbar_wait(&full[st], uint32_t(gi / NSTAGE) & 1u, A.err, abort_flag);
+        const uint32_t mw0 = masks[st * 4], mw1 = masks[st * 4 + 1], mw2 = masks[st * 4 + 2],
+                       mw3 = masks[st * 4 + 3];
+        const bool blk = sg.ta + i >= ctx_tiles;
+        mbar_wait(&s_full[gi & 1], uint32_t(gi >> 1) & 1u, A.err, abort_flag);
+        tc_fence_after();
+        float s[TK];
+        tc_ld32(lane_base + uint32_t(kSCol + (gi & 1) * TK), reinterpret_cast<uint32_t*>(s));
+        tc_ld32(lane_base + uint32_t(kSCol + (gi & 1) * TK + 32), reinterpret_cast<uint32_t*>(s + 32));
+        if (blk || (mw0 & mw1 & mw2 & mw3) != 0xFFFFu) {
+          // rows the tile does not use (and, in the block tile, u > t) get -inf
+#pragma unroll
+          for (int j = 0; j < TK; ++j) {
+            const uint32_t w = (j & 3) == 0 ? mw0 : (j & 3) == 1 ? mw1 : (j & 3) == 2 ? mw2 : mw3;
+            const bool valid = ((w >> (j >> 2)) & 1u) != 0 && (!blk || j <= tq_row);
+            s[j] = valid ? s[j] : -INFINITY;
           }
         }
-        lrow[hi] += ls;
-      }
+        // raw row max (the scale is positive)
+        float m8[8];
 #pragma unroll
-      for (int kk = 0; kk < NJ / 2; ++kk) {
-        const uint32_t a0 = pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]);
-        const uint32_t a1 = pack_bf16(sacc[2 * kk][2], sacc[2 * kk][3]);
-        const uint32_t a2 = pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-        const uint32_t a3 = pack_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
-#pragma unroll
-        for (int jj = 0; jj < D / 16; ++jj) {
-          uint32_t b0, b1, b2, b3;
-          const int row = kb0 + 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
-          const int col = 16 * jj + 8 * (lane >> 4);
-          ldmatrix_x4_trans(b0, b1, b2, b3, Vt + row * RS + col * 2);
-          mma_bf16_16816(o[2 * jj], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(o[2 * jj + 1], a0, a1, a2, a3, b2, b3);
+        for (int x = 0; x < 8; ++x)
+          m8[x] = fmaxf(fmaxf(fmaxf(s[x], s[x + 8]), fmaxf(s[x + 16], s[x + 24])),
+                        fmaxf(fmaxf(s[x + 32], s[x + 40]), fmaxf(s[x + 48], s[x + 56])));
+        const float mx =
+            fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) *
+            scale;
+        float alpha = 1.f;
+        if (mx > mref + 8.f) {   // also the first tile with a valid key
+          alpha = fast_exp2(mref - mx);   // 0 while mref is -inf
+          mref = mx;
+          lsum *= alpha;
         }
-      }
-    }
+        const float nb = (mref == -INFINITY) ? 0.f : -mref;
+        uint32_t pk[TK / 2];
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int hi = 0; hi < 2; ++hi) {
-      lrow[hi] += __shfl_xor_sync(0xffffffffu, lrow[hi], 1);
-      lrow[hi] += __shfl_xor_sync(0xffffffffu, lrow[hi], 2);
-    }
-    cp_async_wait<0>();
-    __syncthreads();   // ring is free: it becomes the merge area
-
-    // ------------------------------------------- merge the two key halves
-    if (half == 1) {
-#pragma unroll
-      for (int hi = 0; hi < 2; ++hi) {
-        const int row = r0 + 8 * hi;
-        if ((lane & 3) == 0) {
-          mM[row] = mrow[hi];
-          mL[row] = lrow[hi];
+        for (int j = 0; j < TK; j += 2) {
+          const uint32_t v = pack_bf16(fast_exp2(fmaf(s[j], scale, nb)), fast_exp2(fmaf(s[j + 1], scale, nb)));
+          pk[j / 2] = v;
+          ls[(j >> 1) & 3] += __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
         }
-        float* dst = mO + size_t(row) * Ly::OS + 2 * (lane & 3);
+        lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // rescale this row of O once P V of the previous tile is in (the
+        // first tile of a segment overwrites O); tensor-memory loads and
+        // stores are collective, so the whole warp takes part
+        if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          mbar_wait(&pv_done[(gi - 1) & 1], uint32_t((gi - 1) >> 1) & 1u, A.err, abort_flag);
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tc_ld32(o_lane + uint32_t(c), o);
 #pragma unroll
-        for (int x = 0; x < NOT; ++x)
-          *reinterpret_cast<float2*>(dst + 8 * x) = make_float2(o[x][2 * hi], o[x][2 * hi + 1]);
-      }
-    }
-    __syncthreads();
-
-    const int seg_first = cta_of((long long)u * tiles_u, total, G);
-    const int seg_last = cta_of((long long)u * tiles_u + tiles_u - 1, total, G);
-    const int n_seg = seg_last - seg_first + 1;
-    const int seg = blockIdx.x - seg_first;
-    const size_t slot_floats = size_t(A.slot_floats);   // NQ*D + 2*NQ, rounded to 4
-    float* part = A.partial + (size_t(u) * A.max_seg + seg) * slot_floats;
-
-    if (half == 0) {
-#pragma unroll
-      for (int hi = 0; hi < 2; ++hi) {
-        const int row = r0 + 8 * hi;
-        const float m1 = mM[row], l1 = mL[row];
-        const float M = fmaxf(mrow[hi], m1);
-        const float bv = (M == -INFINITY) ? 0.f : M;
-        const float a0 = exp2f(mrow[hi] - bv), a1 = exp2f(m1 - bv);
-        const float l = lrow[hi] * a0 + l1 * a1;
-        const float* src = mO + size_t(row) * Ly::OS + 2 * (lane & 3);
-        if (row < NQ) {
-          if (n_seg == 1) {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int tq = row / GQ, hl = row - (row / GQ) * GQ;
-            float* dst = Lr.o + ((size_t(b) * T + tq) * A.hq + size_t(g) * GQ + hl) * D + 2 * (lane & 3);
-#pragma unroll
-            for (int x = 0; x < NOT; ++x) {
-              const float2 h1 = *reinterpret_cast<const float2*>(src + 8 * x);
-              *reinterpret_cast<float2*>(dst + 8 * x) =
-                  make_float2((o[x][2 * hi] * a0 + h1.x * a1) * inv, (o[x][2 * hi + 1] * a0 + h1.y * a1) * inv);
-            }
-          } else {
-            float* dst = part + size_t(row) * D + 2 * (lane & 3);
-#pragma unroll
-            for (int x = 0; x < NOT; ++x) {
-              const float2 h1 = *reinterpret_cast<const float2*>(src + 8 * x);
-              *reinterpret_cast<float2*>(dst + 8 * x) =
-                  make_float2(o[x][2 * hi] * a0 + h1.x * a1, o[x][2 * hi + 1] * a0 + h1.y * a1);
-            }
-            if ((lane & 3) == 0) {
-              part[size_t(NQ) * D + row] = M;
-              part[size_t(NQ) * D + NQ + row] = l;
-            }
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+            tc_st32(o_lane + uint32_t(c), o);
           }
         }
+        tc_st32(lane_base + uint32_t(kPCol + (gi & 1) * (TK / 2)), pk);
+        tc_fence_before();
+        mbar_arrive(&p_full[gi & 1]);
       }
-    }
-    if (n_seg > 1) {
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) *s_last = (atomicAdd(&A.counters[u], 1) == n_seg - 1) ? 1 : 0;
-      __syncthreads();
-      if (*s_last) {
+
+      // ----------------------------------------------------------- epilogue
+      const int seg_first = cta_of((long long)u * tiles_u, total, G);
+      const int seg_last = cta_of((long long)u * tiles_u + tiles_u - 1, total, G);
+      const int n_seg = seg_last - seg_first + 1;
+      const int seg = blockIdx.x - seg_first;
+      const size_t slot_floats = size_t(A.slot_floats);   // NQ*D + 2*NQ, rounded to 4
+      float* part = A.partial + (size_t(u) * A.max_seg + seg) * slot_floats;
+      if (act_warp) {
+        mbar_wait(&pv_done[(gi - 1) & 1], uint32_t((gi - 1) >> 1) & 1u, A.err, abort_flag);
+        tc_fence_after();
+        const int tq = active ? row / GQ : 0, hl = active ? row - (row / GQ) * GQ : 0;
+        float* dst = n_seg == 1 ? Lr.o + ((size_t(b) * T + tq) * A.hq + size_t(g) * GQ + hl) * D
+                                : part + size_t(active ? row : 0) * D;
+        const float osc = n_seg == 1 ? (lsum > 0.f ? 1.f / lsum : 0.f) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tc_ld32(o_lane + uint32_t(c), o);   // collective: every lane loads
+          if (active) {
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+              *reinterpret_cast<float4*>(dst + c + x) =
+                  make_float4(__uint_as_float(o[x]) * osc, __uint_as_float(o[x + 1]) * osc,
+                              __uint_as_float(o[x + 2]) * osc, __uint_as_float(o[x + 3]) * osc);
+          }
+        }
+        if (active && n_seg > 1) {
+          part[size_t(NQ) * D + row] = mref;
+          part[size_t(NQ) * D + NQ + row] = lsum;
+        }
+      }
+      tc_fence_before();
+      if (n_seg > 1) {
         __threadfence();
-        const float* base0 = A.partial + size_t(u) * A.max_seg * slot_floats;
-        for (int q = tid; q < NQ * (D / 4); q += NTH) {
-          const int row = q / (D / 4), c4 = q - row * (D / 4);
-          float M = -INFINITY;
-          for (int s = 0; s < n_seg; ++s)
-            M = fmaxf(M, __ldcg(base0 + s * slot_floats + size_t(NQ) * D + row));
-          const float bv = (M == -INFINITY) ? 0.f : M;
-          float lsum = 0.f;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int s = 0; s < n_seg; ++s) {
-            const float* ps = base0 + s * slot_floats;
-            const float w = exp2f(__ldcg(ps + size_t(NQ) * D + row) - bv);
-            lsum += w * __ldcg(ps + size_t(NQ) * D + NQ + row);
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(ps + size_t(row) * D) + c4);
-            acc.x += w * x.x; acc.y += w * x.y; acc.z += w * x.z; acc.w += w * x.w;
+        softmax_bar(nthr);
+        if (tid == 0) *s_last = (atomicAdd(&A.counters[u], 1) == n_seg - 1) ? 1 : 0;
+        softmax_bar(nthr);
+        if (*s_last) {
+          // log-sum-exp merge of the unit's segments: one item is a row and
+          // 32 columns; the loads of a segment are independent of each other
+          // so that many are in flight at once
+          __threadfence();
+          const float* base0 = A.partial + size_t(u) * A.max_seg * slot_floats;
+          const size_t mo = size_t(NQ) * D;   // m at mo + r, l at mo + NQ + r
+          constexpr int kC4 = 8;              // float4 per item
+          constexpr int kIpr = D / (4 * kC4);  // items per row
+          for (int it = tid; it < NQ * kIpr; it += nthr) {
+            const int r = it / kIpr, c0 = (it - r * kIpr) * kC4;
+            float M = -INFINITY;
+#pragma unroll 4
+            for (int s2 = 0; s2 < n_seg; ++s2) M = fmaxf(M, __ldcg(base0 + s2 * slot_floats + mo + r));
+            const float bv = (M == -INFINITY) ? 0.f : M;
+            float lsc = 0.f;
+            float4 acc[kC4];
+#pragma unroll
+            for (int k = 0; k < kC4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+            for (int s2 = 0; s2 < n_seg; ++s2) {
+              const float* ps = base0 + s2 * slot_floats;
+              const float w = exp2f(__ldcg(ps + mo + r) - bv);
+              lsc += w * __ldcg(ps + mo + NQ + r);
+              const float4* px = reinterpret_cast<const float4*>(ps + size_t(r) * D) + c0;
+#pragma unroll
+              for (int k = 0; k < kC4; ++k) {
+                const float4 x = __ldcg(px + k);
+                acc[k].x += w * x.x;
+                acc[k].y += w * x.y;
+                acc[k].z += w * x.z;
+                acc[k].w += w * x.w;
+              }
+            }
+            const float inv = lsc > 0.f ? 1.f / lsc : 0.f;
+            const int tq = r / GQ, hl = r - (r / GQ) * GQ;
+            float4* dst = reinterpret_cast<float4*>(
+                              Lr.o + ((size_t(b) * T + tq) * A.hq + size_t(g) * GQ + hl) * D) + c0;
+#pragma unroll
+            for (int k = 0; k < kC4; ++k)
+              dst[k] = make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
           }
-          const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-          const int tq = row / GQ, hl = row - (row / GQ) * GQ;
-          float4* dst = reinterpret_cast<float4*>(
-              Lr.o + ((size_t(b) * T + tq) * A.hq + size_t(g) * GQ + hl) * D) + c4;
-          *dst = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+          if (tid == 0) A.counters[u] = 0;
         }
-        if (tid == 0) A.counters[u] = 0;
+        softmax_bar(nthr);   // every softmax thread has read s_last before it is reused
       }
     }
-    __syncthreads();   // merge area / idx slots are reused by the next segment
   }
-}
 
-template <int D, int MT>
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(Tm::cols)
+                 : "memory");
+}
+template <int D>
 cudaError_t launch_t(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t stream) {
-  auto kern = verify_kernel<D, MT, NSTAGE>;
-  const size_t smem = Lay<D, MT, NSTAGE>::total;
+  auto kern = verify_kernel<D>;
+  const size_t smem = Lay<D>::total;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(pl.grid), dim3(64 * MT), smem, stream, a);
-}
-
-template <int D, int MT>
-int occupancy_t() {
-  int n = 0;
-  auto kern = verify_kernel<D, MT, NSTAGE>;
-  const size_t smem = Lay<D, MT, NSTAGE>::total;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-    return 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 64 * MT, smem) != cudaSuccess) return 1;
-  return n > 0 ? n : 1;
-}
-
-template <int D>
-int occupancy_mt(int MT) {
-  static int cache[9] = {};
-  if (MT < 1 || MT > 8) return 1;
-  if (!cache[MT]) {
-    switch (MT) {
-      case 1: cache[MT] = occupancy_t<D, 1>(); break;
-      case 2: cache[MT] = occupancy_t<D, 2>(); break;
-      case 3: cache[MT] = occupancy_t<D, 3>(); break;
-      case 4: cache[MT] = occupancy_t<D, 4>(); break;
-      case 5: cache[MT] = occupancy_t<D, 5>(); break;
-      case 6: cache[MT] = occupancy_t<D, 6>(); break;
-      case 7: cache[MT] = occupancy_t<D, 7>(); break;
-      default: cache[MT] = occupancy_t<D, 8>(); break;
-    }
-  }
-  return cache[MT];
-}
-
-template <int D>
-cudaError_t launch_mt(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t stream) {
-  switch (pl.MT) {
-    case 1: return launch_t<D, 1>(a, pl, stream);
-    case 2: return launch_t<D, 2>(a, pl, stream);
-    case 3: return launch_t<D, 3>(a, pl, stream);
-    case 4: return launch_t<D, 4>(a, pl, stream);
-    case 5: return launch_t<D, 5>(a, pl, stream);
-    case 6: return launch_t<D, 6>(a, pl, stream);
-    case 7: return launch_t<D, 7>(a, pl, stream);
-    case 8: return launch_t<D, 8>(a, pl, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return launch_pdl(kern, dim3(pl.grid), dim3(NTH), smem, stream, a);
 }
 
 }  // namespace
@@ -463,10 +641,8 @@ VerifyLaunch verify_plan(int D, int NQ, int nkeys_cap, int B, int hkv, int n_lay
   pl.tiles_u = pl.ctx_tiles + 1;
   pl.units = (long long)B * hkv * n_layers;
   pl.total = pl.units * pl.tiles_u;
-  // as many CTAs as can be resident (several per SM)
-  int occ = 1;
-  if (num_sms > 0) occ = (D == 128) ? occupancy_mt<128>(pl.MT) : occupancy_mt<64>(pl.MT);
-  long long grid = num_sms > 0 ? (long long)num_sms * occ : kVerifyGridMax;
+  // persistent: one CTA per SM (the shared memory holds one)
+  long long grid = num_sms > 0 ? num_sms : 148;
   if (grid > kVerifyGridMax) grid = kVerifyGridMax;
   if (grid > pl.total) grid = pl.total;
   pl.grid = int(grid);
@@ -475,7 +651,7 @@ VerifyLaunch verify_plan(int D, int NQ, int nkeys_cap, int B, int hkv, int n_lay
   const long long per = pl.total / kVerifyGridMax;
   pl.max_seg = int(pl.tiles_u / (per > 0 ? per : 1)) + 2;
   pl.slot_floats = ((long long)NQ * D + 2LL * NQ + 3) / 4 * 4;   // 16-byte aligned slots
-  pl.smem = 0;
+  pl.smem = D == 128 ? Lay<128>::total : Lay<64>::total;
   return pl;
 }
 
@@ -484,8 +660,8 @@ size_t verify_scratch_bytes(const VerifyLaunch& pl) {
 }
 
 cudaError_t verify_launch(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t stream) {
-  if (pl.D == 128) return launch_mt<128>(a, pl, stream);
-  if (pl.D == 64) return launch_mt<64>(a, pl, stream);
+  if (pl.D == 128) return launch_t<128>(a, pl, stream);
+  if (pl.D == 64) return launch_t<64>(a, pl, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -65,6 +65,11 @@ def test_workspace_sizing(L):
     assert lib.dustin_workspace_bytes(ctypes.byref(p), None, None, None, 0, 8, 3, 128, 1) == 0
     assert lib.dustin_workspace_bytes(ctypes.byref(p), None, None, None, 0, 8, 2, 96, 1) == 0
     assert lib.dustin_workspace_bytes(ctypes.byref(p), None, None, None, 0, 8, 2, 128, 17) == 0
+    # the draft block is at most 64 rows (gamma + 1 <= 64), whatever the group size
+    p64 = bd.CParams(2, 1024, 63, 4, 32, 32, 128)
+    p65 = bd.CParams(2, 1024, 64, 4, 32, 32, 128)
+    assert lib.dustin_workspace_bytes(ctypes.byref(p64), None, None, None, 0, 8, 8, 128, 1) > base
+    assert lib.dustin_workspace_bytes(ctypes.byref(p65), None, None, None, 0, 8, 8, 128, 1) == 0
     # duplicate SRH, bad channel, head out of range -> 0 (invalid)
     for bad in [(1, 0, 0), ]:
         srh2 = (bd.CSRH * 2)(bd.CSRH(1, 0, 0), bd.CSRH(*bad))
