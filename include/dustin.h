@@ -151,13 +151,13 @@ const char* dustin_version(void);
  * per-unit partials from (hq, hkv, d, n_layers).  Pass n_srh = 0 (and NULL
  * pointers) when nothing is scored and n_layers = 0 when nothing is verified.
  * Returns 0 if the arguments are invalid.  Every workspace holds at least
- * 256 + 65536 bytes (error word and the verify combine counters). */
+ * 256 + 65536 bytes (the error word and a reserved area). */
 size_t dustin_workspace_bytes(const dustin_params* p, const dustin_signal* draft,
                               const dustin_signal* target, const dustin_srh* srh,
                               int32_t n_srh, int32_t hq, int32_t hkv, int32_t d,
                               int32_t n_layers);
 
-/* Clears the error word and the verify counters of a workspace
+/* Clears the error word and the reserved area of a workspace
  * (asynchronously, on stream).  Call it once before first use, and again
  * after dustin_check has reported DUSTIN_DEV_TIMEOUT. */
 int dustin_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
@@ -238,7 +238,8 @@ int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStre
  * call with these arguments launches, and how many sequences each scoring
  * group holds.  Scoring runs over groups of *group_size sequences so that a
  * group's logits stay resident in L2; each group takes two kernels (stream,
- * normalise), then select and verify take one each.  Returns DUSTIN_EINVAL /
+ * normalise), select takes one, and verification two (the stream-K kernel
+ * and the merge of the units it split).  Returns DUSTIN_EINVAL /
  * DUSTIN_ERANGE for arguments dustin_verify_step would reject while planning
  * the scoring. */
 int dustin_step_launches(const dustin_step* s, int32_t* n_launches, int32_t* group_size);

@@ -2,8 +2,7 @@
 // and kernel launches for the calls declared in include/dustin.h.  Nothing
 // here allocates device memory; scratch lives in the caller's workspace:
 //   [0, 256)                 header: the sticky device error word (int32 at 0)
-//   [256, 256 + 64 KiB)      per-unit segment counters of the verify combine
-//                            (zero between calls; kept zero by the kernels)
+//   [256, 256 + 64 KiB)      reserved (cleared by dustin_workspace_init)
 //   [kScratch, ...)          scratch shared by the stages of one call:
 //                            score: logits of one group of sequences
 //                                   [n_slab][nb][pairs][LSP] (kept in L2) and
@@ -23,7 +22,7 @@ using namespace dustin;
 namespace {
 
 constexpr size_t kHeader = 256;
-constexpr size_t kCounterBytes = 65536;             // verify units <= 16384
+constexpr size_t kCounterBytes = 65536;             // reserved; verify units <= 16384
 constexpr size_t kScratch = kHeader + kCounterBytes;
 
 int num_sms() {
@@ -116,49 +115,39 @@ bool encode_cache_map(CUtensorMap* m, const dustin_kv& v, int Lcap, int B, int* 
   return r == CUDA_SUCCESS;
 }
 
-// Verification reads cache rows through a 2-D map whose row pitch is the
-// greatest common divisor of the view's strides; a row (b, g, pos) starts at
-// map row (b*sb + g*sh + pos*sl) / pitch.
-int64_t gcd64(int64_t a, int64_t b) {
-  while (b) {
-    const int64_t t = a % b;
-    a = b;
-    b = t;
-  }
-  return a;
-}
-int64_t kv_row_pitch(const dustin_kv& v) { return gcd64(v.sb, gcd64(v.sh, v.sl)); }
-int64_t kv_map_rows(const dustin_kv& v, int B, int Lcap) {
-  return (int64_t(B - 1) * v.sb + int64_t(v.hkv - 1) * v.sh + int64_t(Lcap - 1) * v.sl) /
-             kv_row_pitch(v) + 1;
-}
-
-// Row map (d columns x rows, pitch in elements) with box 64 x 1 for four-row
-// gathers into 128-byte swizzled tiles.
-bool encode_row_map(CUtensorMap* m, const void* ptr, int d, int64_t rows, int64_t pitch) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cuuint64_t(d), cuuint64_t(rows)};
-  cuuint64_t strides[1] = {cuuint64_t(pitch) * 2};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Verify queries [B][T][hq][d] as 3-D (d, hq, B*T) with box (64, G, T): one
 // load brings the G x T query rows of one (sequence, KV head) as rows t*G + h.
 bool encode_query_map(CUtensorMap* m, const void* q, int d, int hq, int BT, int G, int T) {
+  // the encoding depends on these arguments only: repeated calls on the same
+  // buffers (one per layer and step) reuse the previous result
+  struct Key {
+    const void* q;
+    int d, hq, BT, G, T;
+  };
+  constexpr int kSlots = 2 * DUSTIN_MAX_LAYERS;
+  static thread_local Key keys[kSlots];
+  static thread_local CUtensorMap maps[kSlots];
+  static thread_local int next = 0;
+  for (int i = 0; i < kSlots; ++i)
+    if (keys[i].q == q && keys[i].d == d && keys[i].hq == hq && keys[i].BT == BT && keys[i].G == G &&
+        keys[i].T == T) {
+      *m = maps[i];
+      return true;
+    }
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(hq), cuuint64_t(BT)};
   cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(hq) * d * 2};
   cuuint32_t box[3] = {64, cuuint32_t(G), cuuint32_t(T)};
   cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  keys[next] = Key{q, d, hq, BT, G, T};
+  maps[next] = *m;
+  next = (next + 1) % kSlots;
+  return true;
 }
 
 // ------------------------------------------------------------- score plan
@@ -364,11 +353,6 @@ int check_verify_layer(const dustin_params* p, int32_t hq, const void* q, const 
   if (hq < 1 || hq % k.hkv) return DUSTIN_EINVAL;
   const int64_t nq = int64_t(p->gamma + 1) * (hq / k.hkv);
   if (nq > DUSTIN_MAX_QROWS || p->gamma + 1 > DUSTIN_MAX_BLOCK) return DUSTIN_ERANGE;
-  if (kv_row_pitch(k) < k.d || kv_row_pitch(v) < v.d) return DUSTIN_EINVAL;
-  const int64_t lim = (int64_t(1) << 31) - 1;
-  if (kv_map_rows(k, p->B, p->Lcap) > lim || kv_map_rows(v, p->B, p->Lcap) > lim ||
-      int64_t(p->B) * k.hkv * (p->gamma + 1) > lim)
-    return DUSTIN_ERANGE;
   return DUSTIN_OK;
 }
 
@@ -382,9 +366,6 @@ void fill_layer(VerifyLayerDev& L, const void* q, const dustin_kv& k, const dust
   L.o = o;
   L.ksb = k.sb; L.ksh = k.sh; L.ksl = k.sl;
   L.vsb = v.sb; L.vsh = v.sh; L.vsl = v.sl;
-  const int64_t ku = kv_row_pitch(k), vu = kv_row_pitch(v);
-  L.krb = int(k.sb / ku); L.krh = int(k.sh / ku); L.krl = int(k.sl / ku);
-  L.vrb = int(v.sb / vu); L.vrh = int(v.sh / vu); L.vrl = int(v.sl / vu);
 }
 
 struct VerifyShape {
@@ -436,20 +417,11 @@ int run_verify(const dustin_params* p, int32_t hq, int hkv, int D, int n_layers,
   a.ivf = ivf;
   a.seq_len = seq_len;
   a.err = err_word(ws);
-  a.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + kHeader);
   a.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kScratch);
   for (int l = 0; l < n_layers; ++l) {
     const VerifyLayerDev& L = layers[l];
     a.layer[l] = L;
-    dustin_kv kv{const_cast<uint16_t*>(L.k), hkv, D, L.ksb, L.ksh, L.ksl};
-    dustin_kv vv{const_cast<uint16_t*>(L.v), hkv, D, L.vsb, L.vsh, L.vsl};
-    VerifyMapsDev& M = a.maps[l];
-    const int64_t blk_rows = int64_t(p->B) * hkv * a.T;
-    if (!encode_query_map(&M.q, L.q, D, hq, p->B * a.T, a.G, a.T) ||
-        !encode_row_map(&M.k, L.k, D, kv_map_rows(kv, p->B, p->Lcap), kv_row_pitch(kv)) ||
-        !encode_row_map(&M.v, L.v, D, kv_map_rows(vv, p->B, p->Lcap), kv_row_pitch(vv)) ||
-        !encode_row_map(&M.kb, L.kb, D, blk_rows, D) || !encode_row_map(&M.vb, L.vb, D, blk_rows, D))
-      return DUSTIN_ECUDA;
+    if (!encode_query_map(&a.qmap[l], L.q, D, hq, p->B * a.T, a.G, a.T)) return DUSTIN_ECUDA;
   }
   if (verify_launch(a, pl, stream) != cudaSuccess) return DUSTIN_ECUDA;
   return DUSTIN_OK;
@@ -645,7 +617,7 @@ int dustin_step_launches(const dustin_step* s, int32_t* n_launches, int32_t* gro
   const int st = build_score_plan(&s->p, s->draft, s->target, s->srh, s->n_srh, &pl);
   if (st != DUSTIN_OK) return st;
   const int groups = (s->p.B + pl.nb - 1) / pl.nb;
-  *n_launches = 2 * groups + 2;   // stream + normalise per group, select, verify
+  *n_launches = 2 * groups + 3;   // stream + normalise per group, select, verify + merge
   *group_size = pl.nb;
   return DUSTIN_OK;
 }

@@ -38,15 +38,6 @@ struct VerifyLayerDev {
   const uint16_t* vb;
   float* o;            // [B][T][hq][D]
   int64_t ksb, ksh, ksl, vsb, vsh, vsl;
-  // cache strides in rows of the gather maps (row = gcd of the strides)
-  int krb, krh, krl, vrb, vrh, vrl;
-};
-
-// TMA maps of one layer: q 3-D (d, hq, B*T), box (64, G, T); k and v 2-D
-// rows of the cache; kb and vb 2-D rows [B*hkv*T][d]; row maps have box
-// (64, 1) for four-row gathers; all with the 128-byte swizzle.
-struct VerifyMapsDev {
-  CUtensorMap q, k, v, kb, vb;
 };
 
 struct VerifyArgs {
@@ -64,9 +55,18 @@ struct VerifyArgs {
   const int32_t* seq_len;
   int* err;
   float* partial;       // [units][max_seg][slot_floats]: O [NQ][D], m [NQ], l [NQ]
-  int* counters;        // [units], zero between launches
   VerifyLayerDev layer[DUSTIN_MAX_LAYERS];
-  VerifyMapsDev maps[DUSTIN_MAX_LAYERS];
+  // per layer: the queries as 3-D (d, hq, B*T) with box (64, G, T) and the
+  // 128-byte swizzle, so one load brings a unit's G x T query rows
+  CUtensorMap qmap[DUSTIN_MAX_LAYERS];
+};
+
+// The segment merge that follows the stream-K kernel.
+struct VerifyCombineArgs {
+  int NQ, T, hq, hkv, G, units_per_layer, tiles_u, main_grid, max_seg;
+  long long total, slot_floats;
+  const float* partial;
+  float* o[DUSTIN_MAX_LAYERS];
 };
 
 struct VerifyLaunch {

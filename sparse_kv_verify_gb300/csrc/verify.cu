@@ -141,18 +141,6 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t* v) {
 
 // ---- TMA -------------------------------------------------------------------
 
-// Rows r0..r3 x 64 columns from column c of a row map, landing as four
-// consecutive 128-byte rows at dst (swizzled by their shared-memory address).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int c, int r0,
-                                            int r1, int r2, int r3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(smem_u32(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, uint64_t* bar) {
   asm volatile(
@@ -162,6 +150,21 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// Arrive on bar once every cp.async this thread issued so far has completed
+// (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Byte offset of 16-byte chunk c of row r in a [rows][64 bf16] panel with the
+// 128-byte swizzle (chunk ^= row % 8; 8-row groups 1024 bytes apart).
+__device__ __forceinline__ uint32_t swz(int r, int c) { return uint32_t(r) * 128u + (uint32_t(c ^ (r & 7)) << 4); }
+
 // Bounded wait that ignores the abort flag (drains copies in flight before
 // the CTA exits).
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
@@ -170,10 +173,6 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
     if (globaltimer() - t0 > kWaitLimitNs) return;
 }
 
-// Named barrier over the first nthr threads (the softmax warps in use).
-__device__ __forceinline__ void softmax_bar(int nthr) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
-}
 
 template <int D>
 struct Lay {
@@ -187,9 +186,9 @@ struct Lay {
   static constexpr size_t stage_bytes = 2 * half_bytes;
   static constexpr size_t mask_off = ring_off + NSTAGE * stage_bytes;   // [NSTAGE][4] words
   static constexpr size_t bar_off = mask_off + NSTAGE * 16;
-  // full[NSTAGE], empty[NSTAGE], s_full[2], p_full[2], q_full[2], q_empty[2], pv_done[2]
-  static constexpr int n_bars = 2 * NSTAGE + 10;
-  static constexpr size_t misc_off = bar_off + n_bars * 8;   // tmem base, s_last, abort
+  // full[NSTAGE], empty[NSTAGE], s_full[2], p_full[2], q_full[2], q_empty[2]
+  static constexpr int n_bars = 2 * NSTAGE + 8;
+  static constexpr size_t misc_off = bar_off + n_bars * 8;   // tmem base, abort
   static constexpr size_t total = misc_off + 16 + 1024;      // + slack for the 1024-byte base
 };
 
@@ -227,9 +226,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
   uint64_t* p_full = s_full + 2;
   uint64_t* q_full = p_full + 2;
   uint64_t* q_empty = q_full + 2;
-  uint64_t* pv_done = q_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::misc_off);
-  volatile int* s_last = reinterpret_cast<volatile int*>(smem + Ly::misc_off + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::misc_off + 8);
 
   const int tid = threadIdx.x;
@@ -238,7 +235,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
   const int n_act = (NQ + 31) >> 5;   // softmax warps that hold query rows
   if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 32 * kLoaders + kLoaders);
       mbar_init(&empty[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -246,7 +243,6 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       mbar_init(&p_full[x], 32 * n_act);
       mbar_init(&q_full[x], 1);
       mbar_init(&q_empty[x], 1);
-      mbar_init(&pv_done[x], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -284,11 +280,19 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
 
   if (warp >= kLoaderWarp0 && warp < kLoaderWarp0 + kLoaders) {
     // =============================================================== loaders
-    // loader warp lw handles the tiles gi = lw (mod kLoaders) of this CTA
+    // Loader warp lw fetches keys [16 lw, 16 lw + 16) of every tile: lanes
+    // 0-15 read one key index each, then the warp copies the K and V rows of
+    // its keys with 16-byte cp.async (one row of 256 bytes per half-warp)
+    // straight into the 128-byte-swizzled layout the MMA reads; unused rows
+    // are zero-filled.  Each thread's copies arrive on the stage's barrier as
+    // they complete (cp.async.mbarrier.arrive), and lane 0 arrives once more
+    // after publishing the warp's valid-key bits.
     const int lw = warp - kLoaderWarp0;
-    const int gq = lane & 15;        // this lane's group of four rows
-    const int which = lane >> 4;     // 0: K, 1: V
-    constexpr uint32_t kTileBytes = 2u * TK * D * 2;
+    constexpr int CH = D / 8;             // 16-byte chunks per row
+    constexpr int KPI = 32 / CH;          // rows per warp instruction
+    constexpr int NI = 16 / KPI;          // instructions per tensor
+    const int c = lane % CH;
+    const int ksub = lane / CH;
     long long gi = 0;
     int s = 0;
     for (long long t = t0; t < t1; ++s) {
@@ -296,7 +300,6 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       const int layer = sg.u / units_per_layer;
       const int b = (sg.u % units_per_layer) / A.hkv;
       const int g = sg.u % A.hkv;
-      const VerifyMapsDev& M = A.maps[layer];
       const VerifyLayerDev& Lr = A.layer[layer];
       int L = A.seq_len[b];
       if (L < 0 || L > A.Lcap) {
@@ -311,83 +314,61 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
         mbar_arrive_expect_tx(&q_full[qb], uint32_t(NQ) * D * 2);
 #pragma unroll
         for (int h = 0; h < Ly::NP; ++h)
-          tma_load_3d(sbase + uint32_t(Ly::q_off + qb * Ly::q_buf + h * Ly::q_panel), &M.q, h * 64,
+          tma_load_3d(sbase + uint32_t(Ly::q_off + qb * Ly::q_buf + h * Ly::q_panel), &A.qmap[layer], h * 64,
                       g * GQ, b * T, &q_full[qb]);
       }
       __syncwarp();
-      const int rb_row = (which ? Lr.vrb : Lr.krb) * b + (which ? Lr.vrh : Lr.krh) * g;
-      const int rl = which ? Lr.vrl : Lr.krl;
-      const int blk_row = (b * A.hkv + g) * T;
-      const CUtensorMap* cmap = which ? &M.v : &M.k;
-      const CUtensorMap* bmap = which ? &M.vb : &M.kb;
+      const uint16_t* kbase = Lr.k + size_t(b) * Lr.ksb + size_t(g) * Lr.ksh;
+      const uint16_t* vbase = Lr.v + size_t(b) * Lr.vsb + size_t(g) * Lr.vsh;
+      const size_t blk_off = (size_t(b) * A.hkv + g) * T * D;
+      const int kk = 16 * lw + (lane & 15);   // key whose index this lane reads
       for (int i = 0; i < sg.n; ++i, ++gi) {
-        if (int(gi % kLoaders) != lw) continue;
-        // raw key indices of this lane's four rows (loaded before the wait)
         const int tt = sg.ta + i;
         const bool blk = tt >= ctx_tiles;
-        int raw[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = gq * 4 + j;
-          if (blk) raw[j] = r;
-          else if (A.dense) raw[j] = tt * TK + r;
-          else {
-            const int jj = tt * TK + r;
-            raw[j] = jj < A.k ? __ldg(A.ivf + size_t(b) * A.k + jj) : -1;
-          }
+        int raw;                                 // loaded before the wait
+        if (blk) raw = kk;
+        else if (A.dense) raw = tt * TK + kk;
+        else {
+          const int jj = tt * TK + kk;
+          raw = jj < A.k ? __ldg(A.ivf + size_t(b) * A.k + jj) : -1;
         }
         const int st = int(gi % NSTAGE);
         if (gi >= NSTAGE)
           mbar_wait(&empty[st], uint32_t(gi / NSTAGE - 1) & 1u, A.err, abort_flag);
-        bool valid[4];
-        bool any = false;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (blk) valid[j] = raw[j] < T;
-          else if (A.dense) valid[j] = raw[j] < L;
-          else {
-            valid[j] = raw[j] >= 0 && raw[j] < L;
-            if ((raw[j] < -1 || raw[j] >= L) && which == 0) flag_error(A.err, DUSTIN_DEV_INDEX);
-          }
-          any = any || valid[j];
+        bool valid;
+        if (blk) valid = raw < T;
+        else if (A.dense) valid = raw < L;
+        else {
+          valid = raw >= 0 && raw < L;
+          if (lane < 16 && (raw < -1 || raw >= L)) flag_error(A.err, DUSTIN_DEV_INDEX);
         }
-        int row[4];
-        const CUtensorMap* map;
-        if (blk) {
-          map = bmap;
+        const uint32_t vbits = __ballot_sync(0xffffffffu, valid) & 0xFFFFu;
+        const uint32_t stage = sbase + uint32_t(Ly::ring_off + size_t(st) * Ly::stage_bytes);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) row[j] = blk_row + (valid[j] ? raw[j] : 0);
-        } else if (any) {   // some row is in context, so position 0 is valid
-          map = cmap;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) row[j] = rb_row + (valid[j] ? raw[j] : 0) * rl;
-        } else {            // no row in context: read block row 0 instead
-          map = bmap;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) row[j] = blk_row;
+        for (int m = 0; m < 2 * NI; ++m) {
+          const int which = m / NI;
+          const int kl = (m % NI) * KPI + ksub;            // key within the warp's 16
+          const int r = __shfl_sync(0xffffffffu, raw, kl);
+          const bool ok = (vbits >> kl) & 1u;
+          const int rr = ok ? r : 0;
+          const uint16_t* src;
+          if (blk) src = (which ? Lr.vb : Lr.kb) + blk_off + size_t(rr) * D + c * 8;
+          else if (which) src = vbase + size_t(rr) * Lr.vsl + c * 8;
+          else src = kbase + size_t(rr) * Lr.ksl + c * 8;
+          const int key = 16 * lw + kl;
+          cp_async16(stage + uint32_t(which * Ly::half_bytes + (c >> 3) * Ly::kv_panel) + swz(key, c & 7),
+                     src, ok ? 16u : 0u);
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t bits = __ballot_sync(0xffffffffu, valid[j]) & 0xFFFFu;
-          if (lane == 0) masks[st * 4 + j] = bits;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
-        __syncwarp();
-        const uint32_t dst = sbase + uint32_t(Ly::ring_off + size_t(st) * Ly::stage_bytes +
-                                              which * Ly::half_bytes) + uint32_t(gq * 512);
-#pragma unroll
-        for (int h = 0; h < Ly::NP; ++h)
-          tma_gather4(dst + uint32_t(h * Ly::kv_panel), map, h * 64, row[0], row[1], row[2], row[3],
-                      &full[st]);
+        if (lane == 0) masks[st * 4 + lw] = vbits;
+        cp_async_arrive_noinc(&full[st]);
+        if (lane == 0) mbar_arrive(&full[st]);
       }
     }
-    // every copy issued has landed before the CTA may exit
-    if (lane == 0) {
-      for (long long x = gi - NSTAGE < 0 ? 0 : gi - NSTAGE; x < gi; ++x)
-        if (int(x % kLoaders) == lw) mbar_drain(&full[x % NSTAGE], uint32_t(x / NSTAGE) & 1u);
+    cp_async_wait_all();
+    // the query loads this warp issued have landed before the CTA may exit
+    if (lane == 0)
       for (int x = s - 2 < 0 ? 0 : s - 2; x < s; ++x)
         if (x % kLoaders == lw) mbar_drain(&q_full[x & 1], uint32_t(x >> 1) & 1u);
-    }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // =================================================================== MMA
@@ -401,6 +382,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       auto issue_s = [&](long long g2, uint32_t qbuf) {
         const int st = int(g2 % NSTAGE);
         mbar_wait(&full[st], uint32_t(g2 / NSTAGE) & 1u, A.err, abort_flag);
+        fence_proxy_async();   // the rows were written by cp.async (generic proxy)
         tc_fence_after();
         const uint32_t kst = sbase + uint32_t(Ly::ring_off + size_t(st) * Ly::stage_bytes);
 #pragma unroll
@@ -431,8 +413,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
             const uint64_t bd = tc_desc(vst + uint32_t(kk * 2048), uint32_t(Ly::kv_panel), 1024);
             tc_mma_ts(o_tmem, p_tmem + uint32_t(kk * 8), bd, kIdPV, (i > 0 || kk > 0) ? 1 : 0);
           }
-          tc_commit(&empty[st]);
-          tc_commit(&pv_done[gi & 1]);
+          tc_commit(&empty[st]);   // P V of tile gi done: its stage is free
         }
         tc_commit(&q_empty[qb]);
       }
@@ -440,12 +421,8 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       if (s > 0) mbar_drain(&q_empty[(s - 1) & 1], uint32_t((s - 1) >> 1) & 1u);
     }
     __syncwarp();
-  } else if (warp < kSoftmaxWarps) {
+  } else if (warp < n_act) {
     // =============================================================== softmax
-    // warps holding query rows run the tiles; every softmax warp takes part
-    // in the combine
-    const bool act_warp = warp < n_act;
-    constexpr int nthr = 32 * kSoftmaxWarps;
     const int row = tid;             // query row == tensor-memory lane
     const bool active = row < NQ;
     const int tq_row = active ? row / GQ : 0;
@@ -461,7 +438,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       const int g = u % A.hkv;
       const VerifyLayerDev& Lr = A.layer[layer];
       float mref = -INFINITY, lsum = 0.f;   // reference max (log2 domain) and row sum
-      for (int i = 0; act_warp && i < n; ++i, ++gi) {
+      for (int i = 0; i < n; ++i, ++gi) {
         const int st = int(gi % NSTAGE);
         mbar_wait(&full[st], uint32_t(gi / NSTAGE) & 1u, A.err, abort_flag);
         const uint32_t mw0 = masks[st * 4], mw1 = masks[st * 4 + 1], mw2 = masks[st * 4 + 2],
@@ -476,8 +453,8 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
           // rows the tile does not use (and, in the block tile, u > t) get -inf
 #pragma unroll
           for (int j = 0; j < TK; ++j) {
-            const uint32_t w = (j & 3) == 0 ? mw0 : (j & 3) == 1 ? mw1 : (j & 3) == 2 ? mw2 : mw3;
-            const bool valid = ((w >> (j >> 2)) & 1u) != 0 && (!blk || j <= tq_row);
+            const uint32_t w = j < 16 ? mw0 : j < 32 ? mw1 : j < 48 ? mw2 : mw3;
+            const bool valid = ((w >> (j & 15)) & 1u) != 0 && (!blk || j <= tq_row);
             s[j] = valid ? s[j] : -INFINITY;
           }
         }
@@ -510,7 +487,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
         // first tile of a segment overwrites O); tensor-memory loads and
         // stores are collective, so the whole warp takes part
         if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          mbar_wait(&pv_done[(gi - 1) & 1], uint32_t((gi - 1) >> 1) & 1u, A.err, abort_flag);
+          mbar_wait(&empty[(gi - 1) % NSTAGE], uint32_t((gi - 1) / NSTAGE) & 1u, A.err, abort_flag);
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
@@ -533,8 +510,8 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       const int seg = blockIdx.x - seg_first;
       const size_t slot_floats = size_t(A.slot_floats);   // NQ*D + 2*NQ, rounded to 4
       float* part = A.partial + (size_t(u) * A.max_seg + seg) * slot_floats;
-      if (act_warp) {
-        mbar_wait(&pv_done[(gi - 1) & 1], uint32_t((gi - 1) >> 1) & 1u, A.err, abort_flag);
+      {
+        mbar_wait(&empty[(gi - 1) % NSTAGE], uint32_t((gi - 1) / NSTAGE) & 1u, A.err, abort_flag);
         tc_fence_after();
         const int tq = active ? row / GQ : 0, hl = active ? row - (row / GQ) * GQ : 0;
         float* dst = n_seg == 1 ? Lr.o + ((size_t(b) * T + tq) * A.hq + size_t(g) * GQ + hl) * D
@@ -558,57 +535,6 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
         }
       }
       tc_fence_before();
-      if (n_seg > 1) {
-        __threadfence();
-        softmax_bar(nthr);
-        if (tid == 0) *s_last = (atomicAdd(&A.counters[u], 1) == n_seg - 1) ? 1 : 0;
-        softmax_bar(nthr);
-        if (*s_last) {
-          // log-sum-exp merge of the unit's segments: one item is a row and
-          // 32 columns; the loads of a segment are independent of each other
-          // so that many are in flight at once
-          __threadfence();
-          const float* base0 = A.partial + size_t(u) * A.max_seg * slot_floats;
-          const size_t mo = size_t(NQ) * D;   // m at mo + r, l at mo + NQ + r
-          constexpr int kC4 = 8;              // float4 per item
-          constexpr int kIpr = D / (4 * kC4);  // items per row
-          for (int it = tid; it < NQ * kIpr; it += nthr) {
-            const int r = it / kIpr, c0 = (it - r * kIpr) * kC4;
-            float M = -INFINITY;
-#pragma unroll 4
-            for (int s2 = 0; s2 < n_seg; ++s2) M = fmaxf(M, __ldcg(base0 + s2 * slot_floats + mo + r));
-            const float bv = (M == -INFINITY) ? 0.f : M;
-            float lsc = 0.f;
-            float4 acc[kC4];
-#pragma unroll
-            for (int k = 0; k < kC4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-            for (int s2 = 0; s2 < n_seg; ++s2) {
-              const float* ps = base0 + s2 * slot_floats;
-              const float w = exp2f(__ldcg(ps + mo + r) - bv);
-              lsc += w * __ldcg(ps + mo + NQ + r);
-              const float4* px = reinterpret_cast<const float4*>(ps + size_t(r) * D) + c0;
-#pragma unroll
-              for (int k = 0; k < kC4; ++k) {
-                const float4 x = __ldcg(px + k);
-                acc[k].x += w * x.x;
-                acc[k].y += w * x.y;
-                acc[k].z += w * x.z;
-                acc[k].w += w * x.w;
-              }
-            }
-            const float inv = lsc > 0.f ? 1.f / lsc : 0.f;
-            const int tq = r / GQ, hl = r - (r / GQ) * GQ;
-            float4* dst = reinterpret_cast<float4*>(
-                              Lr.o + ((size_t(b) * T + tq) * A.hq + size_t(g) * GQ + hl) * D) + c0;
-#pragma unroll
-            for (int k = 0; k < kC4; ++k)
-              dst[k] = make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
-          }
-          if (tid == 0) A.counters[u] = 0;
-        }
-        softmax_bar(nthr);   // every softmax thread has read s_last before it is reused
-      }
     }
   }
 
@@ -619,13 +545,78 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(Tm::cols)
                  : "memory");
 }
+// Log-sum-exp merge of the segments of every unit that the stream-K split
+// cut into more than one (a one-segment unit was written by its CTA).  One
+// thread per output float4; the partials of a segment are (unnormalised O,
+// log2-domain reference max m, row sum l) relative to that m.
+constexpr int kCombineThreads = 128;
+
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads) verify_combine_kernel(const __grid_constant__ VerifyCombineArgs C) {
+  pdl_launch_dependents();
+  const int u = blockIdx.y;
+  const int seg_first = cta_of((long long)u * C.tiles_u, C.total, C.main_grid);
+  const int seg_last = cta_of((long long)u * C.tiles_u + C.tiles_u - 1, C.total, C.main_grid);
+  const int n_seg = seg_last - seg_first + 1;
+  if (n_seg == 1) return;
+  const int q = blockIdx.x * kCombineThreads + threadIdx.x;
+  if (q >= C.NQ * (D / 4)) return;
+  pdl_wait();
+  const int r = q / (D / 4), c4 = q - r * (D / 4);
+  const size_t slot = size_t(C.slot_floats);
+  const float* base0 = C.partial + size_t(u) * C.max_seg * slot;
+  const size_t mo = size_t(C.NQ) * D;   // m at mo + r, l at mo + NQ + r
+  float M = -INFINITY;
+#pragma unroll 4
+  for (int s2 = 0; s2 < n_seg; ++s2) M = fmaxf(M, __ldg(base0 + s2 * slot + mo + r));
+  const float bv = (M == -INFINITY) ? 0.f : M;
+  float lsc = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int s2 = 0; s2 < n_seg; ++s2) {
+    const float* ps = base0 + s2 * slot;
+    const float w = exp2f(__ldg(ps + mo + r) - bv);
+    lsc += w * __ldg(ps + mo + C.NQ + r);
+    const float4 x = __ldg(reinterpret_cast<const float4*>(ps + size_t(r) * D) + c4);
+    acc.x += w * x.x;
+    acc.y += w * x.y;
+    acc.z += w * x.z;
+    acc.w += w * x.w;
+  }
+  const float inv = lsc > 0.f ? 1.f / lsc : 0.f;
+  const int layer = u / C.units_per_layer;
+  const int b = (u % C.units_per_layer) / C.hkv;
+  const int g = u % C.hkv;
+  const int tq = r / C.G, hl = r - (r / C.G) * C.G;
+  reinterpret_cast<float4*>(C.o[layer] + ((size_t(b) * C.T + tq) * C.hq + size_t(g) * C.G + hl) * D)[c4] =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
 template <int D>
 cudaError_t launch_t(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t stream) {
   auto kern = verify_kernel<D>;
   const size_t smem = Lay<D>::total;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (attr != cudaSuccess) return attr;
+  cudaError_t e = launch_pdl(kern, dim3(pl.grid), dim3(NTH), smem, stream, a);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(pl.grid), dim3(NTH), smem, stream, a);
+  VerifyCombineArgs c;
+  c.NQ = a.NQ;
+  c.T = a.T;
+  c.hq = a.hq;
+  c.hkv = a.hkv;
+  c.G = a.G;
+  c.units_per_layer = a.B * a.hkv;
+  c.tiles_u = a.tiles_u;
+  c.total = a.total;
+  c.main_grid = pl.grid;
+  c.max_seg = a.max_seg;
+  c.slot_floats = a.slot_floats;
+  c.partial = a.partial;
+  for (int l = 0; l < DUSTIN_MAX_LAYERS; ++l) c.o[l] = l < a.n_layers ? a.layer[l].o : nullptr;
+  const dim3 cgrid((a.NQ * (D / 4) + kCombineThreads - 1) / kCombineThreads, unsigned(pl.units));
+  return launch_pdl(verify_combine_kernel<D>, cgrid, dim3(kCombineThreads), 0, stream, c);
 }
 
 }  // namespace

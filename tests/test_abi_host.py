@@ -151,7 +151,7 @@ def test_step_rejects_null_and_too_many_layers(L):
 
 def test_step_launch_count(L):
     """The launch-count query plans like dustin_verify_step: two kernels per
-    scoring group, then select and verify."""
+    scoring group, then select, then verify and the merge of split units."""
     from sparse_kv_verify_gb300 import binding as bd
     lib = L.lib()
 
@@ -171,8 +171,8 @@ def test_step_launch_count(L):
         return st, n.value, g.value, (dft, tgt, srh, lay, kv_t, kv_d, q)
 
     st, n, g, _ = step(2, 4096)
-    assert (st, n, g) == (0, 4, 2)              # one group
+    assert (st, n, g) == (0, 5, 2)              # one group
     st, n, g, _ = step(16, 32832)               # 44 logits rows of 32 K positions per sequence
-    assert st == 0 and 1 <= g < 16 and n == 2 * (-(-16 // g)) + 2
+    assert st == 0 and 1 <= g < 16 and n == 2 * (-(-16 // g)) + 3
     assert lib.dustin_step_launches(None, ctypes.byref(ctypes.c_int32()),
                                     ctypes.byref(ctypes.c_int32())) == -1
