@@ -13,31 +13,33 @@
 // B, Hkv and k are.
 //
 // Roles inside a CTA (warp specialised, handing over through mbarriers):
-//   warps 4-7        loaders, each for every fourth tile: gather the tile's
-//   (loaders)        K and V rows with TMA row gathers (four rows per
-//                    instruction, 128-byte swizzle) into a five-stage ring,
-//                    and a segment's query rows with one tiled TMA load into
-//                    one of two query buffers (a TMA instruction costs its
-//                    warp tens of cycles, so the issue is spread over warps);
-//   warp 8 (MMA)     one thread issues the tensor-core MMAs: S = Q K^T of the
-//                    next tile into one of two S buffers in tensor memory as
-//                    soon as its rows have landed, then O += P V of the
-//                    current tile with P read from tensor memory;
+//   warps 4-7        loaders: warp w copies keys [16 w, 16 w + 16) of every
+//   (loaders)        tile, K and V rows, with 16-byte cp.async straight into
+//                    the 128-byte-swizzled K-major layout the MMA reads (rows
+//                    the tile does not use are zero-filled) through a ring of
+//                    five 32 KB stages (eight 16 KB ones for d = 64; the loads
+//                    take about 3 us under full load, so the stages in flight
+//                    set the pace); each copy's completion arrives on the
+//                    stage's barrier (cp.async.mbarrier.arrive).  A segment's
+//                    query rows come with one tiled TMA load into one of two
+//                    query buffers;
+//   warp 8 (MMA)     one thread issues the tensor-core MMAs (after a proxy
+//                    fence, since the rows were written through the generic
+//                    proxy): S = Q K^T of the next tile into one of two S
+//                    buffers in tensor memory as soon as its rows have landed,
+//                    then O += P V of the current tile with P read from tensor
+//                    memory;
 //   warps 0-3        one thread per query row (tensor-memory lane; warps with
-//                    no query row sit the loop out): online
-//                    softmax of its S row in the log2 domain, with the
-//                    reference max moved only when a tile passes it by more
-//                    than 2^8 (so O is rarely rescaled), P rounded to bf16 and
-//                    stored back to tensor memory; then the epilogue.
+//                    no query row sit the loop out): online softmax of its S
+//                    row in the log2 domain, with the reference max moved only
+//                    when a tile passes it by more than 2^8 (so O is rarely
+//                    rescaled), P rounded to bf16 and stored back to tensor
+//                    memory; then the epilogue.
 //
-// Rows a tile does not use (I_verify padding, positions past seq_len, block
-// rows past gamma) are loaded from a valid row of the same sequence and given
-// probability zero, so the MMAs only ever see finite data.
-//
-// Combine: a segment that covers a whole unit writes O directly; otherwise it
-// writes (row max, row sum, unnormalised O) to the workspace and the last CTA
-// to finish a segment of that unit (an atomic counter, no waiting) merges the
-// segments with a log-sum-exp combine and resets the counter.
+// Merge: a segment that covers a whole unit writes O directly; otherwise it
+// writes (row max, row sum, unnormalised O) to the workspace, and a second,
+// small kernel launched right behind this one merges each split unit's
+// segments with a log-sum-exp combine (one thread per output float4).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -46,7 +48,6 @@ namespace dustin {
 namespace {
 
 constexpr int TK = 64;           // keys per tile (and the largest draft block)
-constexpr int NSTAGE = 5;        // K/V ring stages
 constexpr int kSoftmaxWarps = 4;    // one thread per tensor-memory lane
 constexpr int kLoaders = 4;         // loader warps, each issuing every fourth tile
 constexpr int kLoaderWarp0 = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + kLoaders;
@@ -179,15 +180,19 @@ struct Lay {
   static constexpr int NP = D / 64;                    // 64-column panels per row
   static constexpr size_t q_panel = 128 * 128;         // [128 rows][64 columns]
   static constexpr size_t q_buf = NP * q_panel;
-  static constexpr size_t q_off = 0;                   // two query buffers
-  static constexpr size_t ring_off = q_off + 2 * q_buf;
+  // two query buffers (the next segment's rows load while this one runs) and
+  // as many K/V stages as the rest of the shared memory holds
+  static constexpr int NQB = 2;
+  static constexpr int NST = D == 128 ? 5 : 8;
+  static constexpr size_t q_off = 0;
+  static constexpr size_t ring_off = q_off + NQB * q_buf;
   static constexpr size_t kv_panel = size_t(TK) * 128;    // [64 keys][64 columns]
   static constexpr size_t half_bytes = NP * kv_panel;     // K (or V) of one tile
   static constexpr size_t stage_bytes = 2 * half_bytes;
-  static constexpr size_t mask_off = ring_off + NSTAGE * stage_bytes;   // [NSTAGE][4] words
-  static constexpr size_t bar_off = mask_off + NSTAGE * 16;
-  // full[NSTAGE], empty[NSTAGE], s_full[2], p_full[2], q_full[2], q_empty[2]
-  static constexpr int n_bars = 2 * NSTAGE + 8;
+  static constexpr size_t mask_off = ring_off + NST * stage_bytes;   // [NST][4] words
+  static constexpr size_t bar_off = mask_off + NST * 16;
+  // full[NST], empty[NST], s_full[2], p_full[2], q_full[NQB], q_empty[NQB]
+  static constexpr int n_bars = 2 * NST + 4 + 2 * NQB;
   static constexpr size_t misc_off = bar_off + n_bars * 8;   // tmem base, abort
   static constexpr size_t total = misc_off + 16 + 1024;      // + slack for the 1024-byte base
 };
@@ -216,6 +221,7 @@ template <int D>
 __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ VerifyArgs A) {
   using Ly = Lay<D>;
   using Tm = TmemCfg<D>;
+  constexpr int NSTAGE = Ly::NST, NQB = Ly::NQB;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
   uint64_t* s_full = empty + NSTAGE;
   uint64_t* p_full = s_full + 2;
   uint64_t* q_full = p_full + 2;
-  uint64_t* q_empty = q_full + 2;
+  uint64_t* q_empty = q_full + NQB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::misc_off + 8);
 
@@ -241,6 +247,8 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
       mbar_init(&p_full[x], 32 * n_act);
+    }
+    for (int x = 0; x < NQB; ++x) {
       mbar_init(&q_full[x], 1);
       mbar_init(&q_empty[x], 1);
     }
@@ -252,7 +260,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     // < NQ only), so their scores are exactly zero
     for (int q = NQ * 8 + tid; q < 128 * 8; q += kSoftmaxWarps * 32)
 #pragma unroll
-      for (int x = 0; x < 2 * Ly::NP; ++x)
+      for (int x = 0; x < NQB * Ly::NP; ++x)
         *reinterpret_cast<uint4*>(smem + Ly::q_off + x * Ly::q_panel + size_t(q) * 16) =
             make_uint4(0, 0, 0, 0);
     fence_proxy_async();
@@ -307,10 +315,11 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
           flag_error(A.err, DUSTIN_DEV_SEQLEN);
         L = 0;
       }
-      // this segment's query rows -> query buffer s % 2
-      const int qb = s & 1;
+      // this segment's query rows -> query buffer s % NQB, once the MMAs of the
+      // segment that used it last are done
+      const int qb = s % NQB;
       if (s % kLoaders == lw && lane == 0) {
-        if (s >= 2) mbar_wait(&q_empty[qb], uint32_t((s >> 1) - 1) & 1u, A.err, abort_flag);
+        if (s >= NQB) mbar_wait(&q_empty[qb], uint32_t(s / NQB - 1) & 1u, A.err, abort_flag);
         mbar_arrive_expect_tx(&q_full[qb], uint32_t(NQ) * D * 2);
 #pragma unroll
         for (int h = 0; h < Ly::NP; ++h)
@@ -367,8 +376,8 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     cp_async_wait_all();
     // the query loads this warp issued have landed before the CTA may exit
     if (lane == 0)
-      for (int x = s - 2 < 0 ? 0 : s - 2; x < s; ++x)
-        if (x % kLoaders == lw) mbar_drain(&q_full[x & 1], uint32_t(x >> 1) & 1u);
+      for (int x = s - NQB < 0 ? 0 : s - NQB; x < s; ++x)
+        if (x % kLoaders == lw) mbar_drain(&q_full[x % NQB], uint32_t(x / NQB) & 1u);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // =================================================================== MMA
@@ -396,9 +405,9 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       };
       for (long long t = t0; t < t1; ++s) {
         const Seg sg = next_seg(t, t1, tiles_u);
-        const int qb = s & 1;
+        const int qb = s % NQB;
         const uint32_t qbuf = sbase + uint32_t(Ly::q_off + qb * Ly::q_buf);
-        mbar_wait(&q_full[qb], uint32_t(s >> 1) & 1u, A.err, abort_flag);
+        mbar_wait(&q_full[qb], uint32_t(s / NQB) & 1u, A.err, abort_flag);
         issue_s(gi, qbuf);
         for (int i = 0; i < sg.n; ++i, ++gi) {
           if (i + 1 < sg.n) issue_s(gi + 1, qbuf);
@@ -418,7 +427,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
         tc_commit(&q_empty[qb]);
       }
       // every MMA of this CTA has completed
-      if (s > 0) mbar_drain(&q_empty[(s - 1) & 1], uint32_t((s - 1) >> 1) & 1u);
+      if (s > 0) mbar_drain(&q_empty[(s - 1) % NQB], uint32_t((s - 1) / NQB) & 1u);
     }
     __syncwarp();
   } else if (warp < n_act) {
@@ -627,7 +636,7 @@ VerifyLaunch verify_plan(int D, int NQ, int nkeys_cap, int B, int hkv, int n_lay
   VerifyLaunch pl{};
   pl.D = D;
   pl.MT = (NQ + 15) / 16;
-  pl.NST = NSTAGE;
+  pl.NST = D == 128 ? Lay<128>::NST : Lay<64>::NST;
   pl.ctx_tiles = (nkeys_cap + TK - 1) / TK;
   pl.tiles_u = pl.ctx_tiles + 1;
   pl.units = (long long)B * hkv * n_layers;
