@@ -193,6 +193,31 @@ def test_verify_gamma_range(gamma):
     assert_attention(od, c.oracle_dense())
 
 
+@pytest.mark.parametrize("d,hq,hkv", [(64, 2, 1), (128, 16, 8)])
+def test_verify_largest_draft_block(d, hq, hkv):
+    """gamma + 1 = 64 draft-block rows (one whole block tile under the causal
+    mask) and (gamma + 1) * Hq/Hkv = 128 query rows, the largest shape; one
+    more draft row is refused with DUSTIN_ERANGE before anything runs."""
+    wl = WORKLOADS["tiny"].with_(gamma=63, Hq=hq, Hkv=hkv, d=d, L=1024, k=256, sinks=4,
+                                 window=64, m=64)
+    c = Case(wl)
+    x = c.x
+    rng = np.random.default_rng(63)
+    I_ref = np.stack([np.sort(rng.choice(wl.L, wl.k, replace=False))]).astype(np.int64)
+    I = torch.as_tensor(I_ref.astype(np.int32), device="cuda")
+    ws = dk.workspace(c.p, verify=(hq, hkv, d, 1))
+    o = dk.dustin_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], I, c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    assert_attention(o, c.oracle_verify(I_ref))
+    od = dk.dense_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], c.seq, ws=ws)
+    assert_attention(od, c.oracle_dense())
+    p65 = params_of(wl, gamma=64)
+    q65 = torch.zeros((wl.B, 65, hq, d), dtype=torch.bfloat16, device="cuda")
+    kb65 = torch.zeros((wl.B, hkv, 65, d), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dk.DustinError):
+        dk.dustin_verify_attn(p65, q65, x.K[0], x.V[0], kb65, kb65, I, c.seq, ws=ws)
+
+
 def test_verify_full_budget_matches_dense():
     """k >= L: I_verify is every context row, so sparse equals dense."""
     wl = WORKLOADS["tiny"].with_(k=1100)
