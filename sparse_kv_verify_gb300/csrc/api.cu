@@ -22,7 +22,8 @@ using namespace dustin;
 namespace {
 
 constexpr size_t kHeader = 256;
-constexpr size_t kCounterBytes = 65536;             // reserved; verify units <= 16384
+constexpr size_t kCounterBytes = 65536;             // reserved
+constexpr long long kVerifyUnitsMax = 16384;        // B * Hkv * layers per verification call
 constexpr size_t kScratch = kHeader + kCounterBytes;
 
 int num_sms() {
@@ -381,7 +382,7 @@ VerifyLaunch plan_verify(const dustin_params* p, const VerifyShape& v, int dense
 size_t verify_ws_bytes(const dustin_params* p, const VerifyShape& v, int dense) {
   if (v.n_layers <= 0) return kScratch;
   const VerifyLaunch pl = plan_verify(p, v, dense);
-  if (pl.units * 4 > (long long)kCounterBytes) return 0;
+  if (pl.units > kVerifyUnitsMax) return 0;
   return kScratch + round256(verify_scratch_bytes(pl));
 }
 
@@ -394,7 +395,7 @@ int run_verify(const dustin_params* p, int32_t hq, int hkv, int D, int n_layers,
   vs.d = D;
   vs.n_layers = n_layers;
   const VerifyLaunch pl = plan_verify(p, vs, dense);
-  if (pl.units * 4 > (long long)kCounterBytes) return DUSTIN_ERANGE;
+  if (pl.units > kVerifyUnitsMax) return DUSTIN_ERANGE;
   if (!ws_ok(ws, ws_bytes, kScratch + verify_scratch_bytes(pl))) return DUSTIN_EWORKSPACE;
   static thread_local VerifyArgs a;
   std::memset(&a, 0, sizeof(a));

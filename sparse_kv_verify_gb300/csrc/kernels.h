@@ -70,7 +70,7 @@ struct VerifyCombineArgs {
 };
 
 struct VerifyLaunch {
-  int D, MT, NST;
+  int D, NST;
   int ctx_tiles, tiles_u, grid, max_seg;
   long long units, total, slot_floats;
   size_t smem;

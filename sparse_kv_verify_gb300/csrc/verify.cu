@@ -635,7 +635,6 @@ VerifyLaunch verify_plan(int D, int NQ, int nkeys_cap, int B, int hkv, int n_lay
   (void)dense;
   VerifyLaunch pl{};
   pl.D = D;
-  pl.MT = (NQ + 15) / 16;
   pl.NST = D == 128 ? Lay<128>::NST : Lay<64>::NST;
   pl.ctx_tiles = (nkeys_cap + TK - 1) / TK;
   pl.tiles_u = pl.ctx_tiles + 1;
