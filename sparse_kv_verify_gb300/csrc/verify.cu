@@ -49,7 +49,7 @@ namespace {
 
 constexpr int TK = 64;           // keys per tile (and the largest draft block)
 constexpr int kSoftmaxWarps = 4;    // one thread per tensor-memory lane
-constexpr int kLoaders = 4;         // loader warps, each issuing every fourth tile
+constexpr int kLoaders = 4;         // loader warps, 16 keys of every tile each
 constexpr int kLoaderWarp0 = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + kLoaders;
 constexpr int NTH = 32 * (kMmaWarp + 1);
 constexpr int kSCol = 0;         // S buffers: columns [0, 64) and [64, 128)
