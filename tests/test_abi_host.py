@@ -125,6 +125,14 @@ def test_invalid_verify_arguments_rejected(L):
                                   0x5000, 0x6000, ws, 1 << 20, None) == -2
     assert lib.dense_verify_attn(ctypes.byref(p), 64, 0x1000, k, k, 0x2000, 0x3000, None,
                                  0x6000, ws, 1 << 20, None) == -1
+    # the draft block is one 64-key tile: gamma + 1 = 65 rows is refused even
+    # when the query rows fit (Hq / Hkv = 1)
+    k1 = bd.CKV(0x10000, 8, 128, 8 * 1024 * 128, 1024 * 128, 128)
+    p64 = bd.CParams(2, 1024, 64, 4, 32, 32, 128)
+    assert lib.dustin_verify_attn(ctypes.byref(p64), 8, 0x1000, k1, k1, 0x2000, 0x3000, 0x4000,
+                                  0x5000, 0x6000, ws, 1 << 20, None) == -2
+    assert lib.dense_verify_attn(ctypes.byref(p64), 8, 0x1000, k1, k1, 0x2000, 0x3000, 0x5000,
+                                 0x6000, ws, 1 << 20, None) == -2
 
 
 def test_invalid_append_arguments_rejected(L):
