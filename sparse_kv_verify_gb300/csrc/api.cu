@@ -2,11 +2,14 @@
 // and kernel launches for the calls declared in include/dustin.h.  Nothing
 // here allocates device memory; scratch lives in the caller's workspace:
 //   [0, 256)                 header: the sticky device error word (int32 at 0)
-//   [256, 256 + 64 KiB)      reserved (cleared by dustin_workspace_init)
+//   [256, 256 + 64 KiB)      selection arrival counters, one int per sequence;
+//                            zero between calls (cleared by dustin_workspace_init)
 //   [kScratch, ...)          scratch shared by the stages of one call:
 //                            score: logits of one group of sequences
 //                                   [n_slab][nb][pairs][LSP] (kept in L2) and
 //                                   per-segment (max, sum) statistics
+//                            select (after the score scratch in the fused
+//                                   step): histograms, candidate lists, bitmaps
 //                            verify: segment partials [units][max_seg][slot]
 #include <cudaTypedefs.h>
 
@@ -22,7 +25,7 @@ using namespace dustin;
 namespace {
 
 constexpr size_t kHeader = 256;
-constexpr size_t kCounterBytes = 65536;             // reserved
+constexpr size_t kCounterBytes = size_t(kSelectCountersMax) * 4;   // selection counters
 constexpr long long kVerifyUnitsMax = 16384;        // B * Hkv * layers per verification call
 constexpr size_t kScratch = kHeader + kCounterBytes;
 
@@ -167,8 +170,12 @@ struct ScorePlan {
   int LSP = 0;           // logits row stride (floats, multiple of 32)
   int nb = 0;            // sequences per group
   int max_seg = 0;
+  int n_rows = 0, n_rows0 = 0;
   ScoreLaunch launch{};
   size_t logits_off = 0, logits_bytes = 0, stats_off = 0, stats_bytes = 0, total = 0;
+  // selection scratch of the fused step, after the score scratch
+  SelectPlan sel{};
+  size_t hist_off = 0, total_step = 0;
 };
 
 const dustin_signal* sig_of(int ch, const dustin_signal* draft, const dustin_signal* target) {
@@ -281,14 +288,27 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
     pl->slab[t].logit_off = off;
     off += (long long)pl->nb * pl->slab[t].npairs * pl->LSP;
   }
+  // logits rows per sequence (channel 0 first)
+  for (int t = 0; t < pl->n_slab; ++t) {
+    pl->n_rows += pl->slab[t].npairs;
+    if (pl->slab[t].channel == 0) pl->n_rows0 += pl->slab[t].npairs;
+  }
+  // the fused step's selection scratch (its histograms first) follows the
+  // score scratch: the normalise kernel fills the histograms
+  pl->sel = select_plan(p->B, p->Lcap, pl->total);
+  pl->hist_off = pl->sel.hist_off;
+  pl->total_step = pl->sel.end;
   pl->launch.NT = (pl->np_max + 7) / 8;
   pl->launch.smem = score_stream_smem();
+  pl->launch.norm_smem = score_norm_smem(pl->n_rows);
   return DUSTIN_OK;
 }
 
+// hist: the selection histograms to build (fused step), or nullptr.
 int launch_score(const dustin_params* p, const dustin_signal* draft, const dustin_signal* target,
                  const ScorePlan& pl, const int32_t* seq_len, float* importance, void* ws,
-                 cudaStream_t stream, cudaEvent_t after_first_stream = nullptr) {
+                 cudaStream_t stream, cudaEvent_t after_first_stream = nullptr,
+                 int* hist = nullptr) {
   static thread_local ScoreArgs a;   // large (tensor maps): keep it off the stack
   std::memset(&a, 0, sizeof(a));
   int rank[DUSTIN_MAX_SRH];
@@ -313,6 +333,11 @@ int launch_score(const dustin_params* p, const dustin_signal* draft, const dusti
   a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.logits_off);
   a.stats = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.stats_off);
   a.importance = importance;
+  a.hist = hist;
+  a.sinks = p->sinks;
+  a.window = p->window;
+  a.n_rows = pl.n_rows;
+  a.n_rows0 = pl.n_rows0;
   const int sms = num_sms() > 0 ? num_sms() : 148;
   for (int b0 = 0; b0 < p->B; b0 += pl.nb) {
     a.b0 = b0;
@@ -328,6 +353,23 @@ int launch_score(const dustin_params* p, const dustin_signal* draft, const dusti
     a.cost_start[pl.n_slab] = cost;
     a.total = acc;
     a.total_cost = cost;
+    // the slabs in logits-row order: channel 0 first
+    int n_info = 0, row = 0;
+    for (int ch = 0; ch < 2; ++ch)
+      for (int t = 0; t < pl.n_slab; ++t) {
+        if (pl.slab[t].channel != ch) continue;
+        SlabInfo& I = a.info[n_info++];
+        I.logit_off = pl.slab[t].logit_off;
+        I.first_tile = a.slab_start[t];
+        I.cost_start = a.cost_start[t];
+        I.npairs = pl.slab[t].npairs;
+        I.tiles = pl.slab[t].tiles;
+        I.cost = pl.slab[t].cost;
+        I.row0 = row;
+        I.slab = t;
+        I.pad = 0;
+        row += pl.slab[t].npairs;
+      }
     // every CTA's share of the cost must reach the largest tile cost, so that
     // each CTA owns at least one tile (the normalise kernel relies on it)
     long long wmax = 1;
@@ -438,11 +480,11 @@ size_t dustin_workspace_bytes(const dustin_params* p, const dustin_signal* draft
                               const dustin_signal* target, const dustin_srh* srh, int32_t n_srh,
                               int32_t hq, int32_t hkv, int32_t d, int32_t n_layers) {
   if (!params_ok(p)) return 0;
-  size_t need = kScratch;
+  size_t need = select_plan(p->B, p->Lcap, kScratch).end;   // dustin_select
   if (n_srh != 0) {
     static thread_local ScorePlan pl;
     if (build_score_plan(p, draft, target, srh, n_srh, &pl) != DUSTIN_OK) return 0;
-    need = pl.total > need ? pl.total : need;
+    need = pl.total_step > need ? pl.total_step : need;
   }
   if (n_layers != 0) {
     if (n_layers < 0 || n_layers > DUSTIN_MAX_LAYERS || hkv < 1 || hq < 1 || hq % hkv ||
@@ -493,12 +535,28 @@ int dustin_score(const dustin_params* p, const dustin_signal* draft, const dusti
   return launch_score(p, draft, target, pl, seq_len, importance, ws, stream);
 }
 
-int dustin_select(const dustin_params* p, const float* importance, const int32_t* seq_len,
-                  int32_t* i_verify, void* ws, size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// sel: the selection scratch; fused: its histograms were built by the score
+// kernels of this call (otherwise select_launch counts them first).
+int run_select(const dustin_params* p, const float* importance, const int32_t* seq_len,
+               int32_t* i_verify, const SelectPlan& sel, bool fused, void* ws, size_t ws_bytes,
+               cudaStream_t stream) {
   if (!params_ok(p)) return DUSTIN_EINVAL;
   if (!importance || !seq_len || !i_verify) return DUSTIN_EINVAL;
-  if (!ws_ok(ws, ws_bytes, kScratch)) return DUSTIN_EWORKSPACE;
+  if (!ws_ok(ws, ws_bytes, sel.end)) return DUSTIN_EWORKSPACE;
+  char* w = static_cast<char*>(ws);
   SelectArgs a{};
+  a.hist = reinterpret_cast<int*>(w + sel.hist_off);
+  a.lists = reinterpret_cast<uint2*>(w + sel.lists_off);
+  a.list_counts = reinterpret_cast<int*>(w + sel.counts_off);
+  a.bits = reinterpret_cast<uint32_t*>(w + sel.bits_off);
+  a.counters = reinterpret_cast<int*>(w + kHeader);   // reserved area, zero between calls
+  a.cs = sel.cs;
+  a.list_cap = sel.list_cap;
+  a.bits_words = sel.bits_words;
   a.B = p->B;
   a.Lcap = p->Lcap;
   a.k = p->k;
@@ -509,7 +567,18 @@ int dustin_select(const dustin_params* p, const float* importance, const int32_t
   a.seq_len = seq_len;
   a.out = i_verify;
   a.err = err_word(ws);
-  return select_launch(a, stream) == cudaSuccess ? DUSTIN_OK : DUSTIN_ECUDA;
+  return select_launch(a, !fused, stream) == cudaSuccess ? DUSTIN_OK : DUSTIN_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dustin_select(const dustin_params* p, const float* importance, const int32_t* seq_len,
+                  int32_t* i_verify, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!params_ok(p)) return DUSTIN_EINVAL;
+  return run_select(p, importance, seq_len, i_verify, select_plan(p->B, p->Lcap, kScratch), false, ws,
+                    ws_bytes, stream);
 }
 
 int dustin_verify_attn(const dustin_params* p, int32_t hq, const void* q, dustin_kv k,
@@ -649,14 +718,15 @@ int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStre
   vs.n_layers = s->n_layers;
   const size_t vneed = verify_ws_bytes(p, vs, 0);
   if (vneed == 0) return DUSTIN_ERANGE;
-  if (!ws_ok(ws, ws_bytes, pl.total > vneed ? pl.total : vneed)) return DUSTIN_EWORKSPACE;
+  if (!ws_ok(ws, ws_bytes, pl.total_step > vneed ? pl.total_step : vneed)) return DUSTIN_EWORKSPACE;
+  int* hist = reinterpret_cast<int*>(static_cast<char*>(ws) + pl.hist_off);
   cudaEvent_t* ev = s->stage_events;
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return DUSTIN_ECUDA;
   st = launch_score(p, s->draft, s->target, pl, s->seq_len, s->importance, ws, stream,
-                    ev ? ev[1] : nullptr);
+                    ev ? ev[1] : nullptr, hist);
   if (st != DUSTIN_OK) return st;
   if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return DUSTIN_ECUDA;
-  st = dustin_select(p, s->importance, s->seq_len, s->i_verify, ws, ws_bytes, stream);
+  st = run_select(p, s->importance, s->seq_len, s->i_verify, pl.sel, true, ws, ws_bytes, stream);
   if (st != DUSTIN_OK) return st;
   if (ev && cudaEventRecord(ev[3], stream) != cudaSuccess) return DUSTIN_ECUDA;
   st = run_verify(p, s->hq, hkv, D, s->n_layers, layers, s->i_verify, s->seq_len, 0, ws, ws_bytes,

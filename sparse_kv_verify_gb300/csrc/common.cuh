@@ -66,8 +66,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs (sets DUSTIN_DEV_TIMEOUT and *abort) so that a broken
-// transaction count can never hang the GPU.  Returns false on give-up.
+// kWaitLimitNs (sets DUSTIN_DEV_TIMEOUT and, if given, *abort, which makes the
+// CTA's other waits give up too) so that a broken transaction count can never
+// hang the GPU.  Returns false on give-up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
                                           volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -75,10 +76,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
-      if (*abort) return false;
+      if (abort && *abort) return false;
       if (globaltimer() - t0 > kWaitLimitNs) {
         flag_error(err, DUSTIN_DEV_TIMEOUT);
-        *abort = 1;
+        if (abort) *abort = 1;
         return false;
       }
     }
@@ -193,6 +194,22 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
+
+// Selection key of an importance value: its bit pattern, which orders like
+// the value for non-negative floats.  NaN and negative values (importance is a
+// sum of probabilities, so neither can arise from valid inputs) rank as 0 and
+// are flagged.  The scoring kernel bins the keys it writes with this mapping
+// and the selection kernel reads them back with it, so their histograms agree.
+__device__ __forceinline__ uint32_t importance_key(float v, int* err) {
+  const uint32_t u = __float_as_uint(v);
+  if (u <= 0x7F800000u) return u;     // +0 .. +inf
+  if (u != 0x80000000u) flag_error(err, DUSTIN_DEV_NAN);
+  return 0u;
+}
+
+// Level-1 selection histogram: the top 12 key bits.
+constexpr int kSelectBins = 4096;
+__device__ __forceinline__ uint32_t select_bin(uint32_t key) { return key >> 20; }
 
 constexpr float kLog2e = 1.4426950408889634f;
 

@@ -103,6 +103,17 @@ struct ScoreSlab {
   const uint16_t* q;     // [B][nq][hq][D]
 };
 
+// Per-slab facts of one group launch in a compact form: the normalise kernel
+// copies the table to shared memory once (kernel-parameter reads with a
+// per-thread index are slow) and walks it there.
+struct SlabInfo {
+  long long logit_off;   // float offset of the slab's logits
+  long long first_tile;  // first flattened tile of the slab
+  long long cost_start;  // cost before that tile
+  int npairs, tiles, cost, row0;   // row0: the slab's first logits row (channel 0 first)
+  int slab, pad;         // index of the slab in ScoreArgs::slab
+};
+
 struct ScoreArgs {
   CUtensorMap map[DUSTIN_MAX_SRH];   // one per (channel, layer) cache; box 64 x 128
   ScoreSlab slab[DUSTIN_MAX_SRH];
@@ -111,6 +122,8 @@ struct ScoreArgs {
   long long total;                            // tiles of this group
   long long total_cost;                       // sum of tile costs of this group
   int B, Lcap, LSP, n_slab, np_max;
+  int n_rows, n_rows0;   // logits rows (slab, pair) per sequence, channel 0 first; rows of channel 0
+  int sinks, window;     // the unprotected range of the selection histograms
   int b0, nb;            // the group of sequences handled by this launch
   int grid;              // CTAs of the stream kernel
   int max_seg;           // statistics slots per (slab, sequence)
@@ -119,15 +132,19 @@ struct ScoreArgs {
   float* logits;         // scratch, stays in L2 between the two kernels
   float* stats;          // [n_slab][nb][max_seg][np_max][2]
   float* importance;     // [B][2][Lcap]
+  int* hist;             // [B][2][4096] selection histograms, or nullptr
+  SlabInfo info[DUSTIN_MAX_SRH];   // in row order (channel 0 slabs first)
 };
 
 struct ScoreLaunch {
   int NT;
   size_t smem;
+  size_t norm_smem;      // dynamic shared memory of the normalise kernel
 };
 
 constexpr int kScoreGridMax = 256;
 size_t score_stream_smem();
+size_t score_norm_smem(int n_rows);
 int score_rows_per_tile(int D);
 int score_tile_cost(int D, int npairs);
 // Launches the stream and normalise kernels of one sequence group; records
@@ -137,17 +154,36 @@ cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t
 
 // ------------------------------------------------------------------ select
 
+constexpr int kMaxSelectCtas = 8;          // scan CTAs per sequence
+constexpr int kSelectCountersMax = 16384;  // sequences whose arrival counters fit the reserved area
+
 struct SelectArgs {
   int B, Lcap, k, sinks, window, m;
-  int cache_keys;        // set by select_launch: 1 = stage keys in shared memory
-  int slice_cap;         // set by select_launch: positions per CTA slice
+  int vec4;              // set by select_launch: rows read as float4
+  int cs;                // scan CTAs per sequence
+  int list_cap;          // list entries per (sequence, channel, scan CTA)
+  int bits_words;        // bitmap words per sequence (general path)
   const float* imp;      // [B][2][Lcap]
+  int* hist;             // [B][2][4096] level-1 histograms over the unprotected
+                         // positions (built by the score kernels in the fused
+                         // step, by select_launch otherwise)
   const int32_t* seq_len;
   int32_t* out;          // [B][k]
   int* err;
+  uint2* lists;          // [B][2][cs][list_cap] (key, position)
+  int* list_counts;      // [B][2][cs]; -1: overflow
+  int* counters;         // [B] arrival counters, zero between calls
+  uint32_t* bits;        // [B][bits_words]
 };
-int select_cluster_size(const SelectArgs& a);   // CTAs per sequence select_launch uses
-cudaError_t select_launch(const SelectArgs& a, cudaStream_t stream);
+
+// Workspace layout of the selection scratch starting at byte offset off.
+struct SelectPlan {
+  int cs, list_cap, bits_words;
+  size_t hist_off, lists_off, counts_off, bits_off, end;
+};
+SelectPlan select_plan(int B, int Lcap, size_t off);
+// build_hist: count the histograms first (standalone call).
+cudaError_t select_launch(const SelectArgs& a, bool build_hist, cudaStream_t stream);
 
 // ------------------------------------------------------------------ append
 

@@ -37,9 +37,7 @@ constexpr int kStages = 6;
 constexpr int kConsumers = 8;                        // 8 warps x 16 rows = 128 rows
 constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int kMaxKs = 8;                            // d / 16 for d = 128
-constexpr int kNormThreads = 256;
-constexpr int kNormChunk = 1024;                     // positions per normalise CTA
-constexpr int kNormRows = 16;                        // logits rows in flight per thread
+constexpr int kNormThreads = 256;                    // and positions per normalise CTA
 
 __device__ __forceinline__ uint32_t tile_addr(uint32_t st, int D, int r, int c) {
   // element (row r, column c) of a tile stored as two TMA boxes of
@@ -191,6 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
   }
   pdl_launch_dependents();
   pdl_wait();
+  // clear this group's selection histograms (the normalise kernel that
+  // follows fills them; the selection of the previous call has completed)
+  if (A.hist) {
+    int* h = A.hist + size_t(A.b0) * 2 * kSelectBins;
+    const int n = A.nb * 2 * kSelectBins;
+    for (int j = blockIdx.x * kThreads + threadIdx.x; j < n; j += G * kThreads) h[j] = 0;
+  }
   __syncthreads();
   if (t0 >= t1) return;
 
@@ -350,124 +355,141 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
   }
 }
 
-__global__ void __launch_bounds__(kNormThreads, 2) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
-  // one row per (slab, pair): logits offset, merged max M and 1 / sum
-  __shared__ long long roff[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
-  __shared__ float Mg[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
-  __shared__ float Ig[DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS];
-  __shared__ int nrow[2];
-  __shared__ int nseg[DUSTIN_MAX_SRH];
-  pdl_launch_dependents();
-  pdl_wait();
+// Normalise: one CTA per (256 positions, sequence).  Warp 0 pulls the CTA's
+// slice of every logits row (1 KB per row) into shared memory with one bulk
+// copy per row, so all of a CTA's loads are in flight at once and the bytes
+// in flight per SM are bounded by shared memory, not registers; meanwhile the
+// first threads merge each row's segment statistics into M and 1/S.  Then
+// thread t owns position t of the slice: it sums exp2(l - M) / S over the
+// rows of each channel, writes both importance values and, in the fused step,
+// adds their keys to the sequence's selection histograms (unprotected
+// positions only; one reduction per distinct bin of a warp).
+constexpr int kNormRowsMax = 48;   // logits rows staged per batch
+
+__device__ __forceinline__ void hist_red(int* h, uint32_t bin, bool ok, int lane) {
+  const uint32_t mask = __match_any_sync(0xffffffffu, ok ? bin : 0xFFFFFFFFu);
+  if (ok && lane == __ffs(mask) - 1) atomicAdd(h + bin, __popc(mask));
+}
+
+// CTA of the stream kernel that owns the tile whose cost prefix is P.
+__device__ __forceinline__ int owner_at_cost(long long P, long long total_cost, int G) {
+  return int(((P + 1) * G + total_cost - 1) / total_cost) - 1;
+}
+
+// Slab (index into the table) holding logits row r.
+__device__ __forceinline__ int slab_of_row(const SlabInfo* si, int ns, int r) {
+  int j = 0;
+  while (j + 1 < ns && si[j + 1].row0 <= r) ++j;
+  return j;
+}
+
+__global__ void __launch_bounds__(kNormThreads) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
+  extern __shared__ __align__(128) unsigned char nsm[];
+  __shared__ SlabInfo si[DUSTIN_MAX_SRH];
+  const int nr = A.n_rows, n0 = A.n_rows0, ns = A.n_slab;
+  const int nbatch_rows = nr < kNormRowsMax ? nr : kNormRowsMax;
+  float* lg = reinterpret_cast<float*>(nsm);                       // [rows][256]
+  float* Mg = lg + size_t(nbatch_rows) * kNormThreads;            // [nr]
+  float* Ig = Mg + nr;                                              // [nr]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(Ig + nr);   // 8-byte aligned: 2 nr floats above
+  const int tid = threadIdx.x, lane = tid & 31;
   const int bl = blockIdx.y;
   const int b = A.b0 + bl;
+  const int base = blockIdx.x * kNormThreads;
+  const int npos = min(kNormThreads, A.LSP - base);   // a multiple of 32
+  const int lines = npos * 4 / 128;
+  // the slab table: one parameter word per thread, all loads in flight at once
+  constexpr int kInfoWords = int(sizeof(SlabInfo) / 4);
+  for (int j = tid; j < ns * kInfoWords; j += kNormThreads)
+    reinterpret_cast<int*>(si)[j] = reinterpret_cast<const int*>(A.info)[j];
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(bar, uint32_t(nbatch_rows) * npos * 4);
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  __syncthreads();
+  // Rows [r0, r0 + n): one bulk copy of npos floats per row.  Row r0 + q is
+  // issued by thread 32 (q % 8) + q / 8, so eight warps share the issue.
+  const float* my_src = nullptr;   // this thread's row of the current batch
+  auto issue = [&](int r0, int n) {
+    const int q = (tid & 31) * 8 + (tid >> 5);
+    my_src = nullptr;
+    if ((tid >> 5) < 8 && q < n) {
+      const int r = r0 + q;
+      const int j = slab_of_row(si, ns, r);
+      const int p = r - si[j].row0;
+      my_src = A.logits + si[j].logit_off + (size_t(bl) * si[j].npairs + p) * A.LSP + base;
+      bulk_g2s(lg + size_t(q) * kNormThreads, my_src, uint32_t(npos) * 4, bar);
+    }
+  };
+  issue(0, nbatch_rows);
   int L = A.seq_len[b];
   if (L < 0 || L > A.Lcap) L = 0;
-  const int G = A.grid;
-  if (threadIdx.x < 2) {
-    int n = 0;
-    for (int s = 0; s < A.n_slab; ++s)
-      if (A.slab[s].channel == int(threadIdx.x)) n += A.slab[s].npairs;
-    nrow[threadIdx.x] = n;
-  }
-  // per slab: how many CTAs own tiles of this sequence (the host sizes the
-  // grid so that every CTA owns at least one tile, so each of them wrote its
-  // statistics slot)
-  if (threadIdx.x >= 32 && int(threadIdx.x) < 32 + A.n_slab) {
-    const int s = threadIdx.x - 32;
-    const long long first = A.slab_start[s] + (long long)bl * A.slab[s].tiles;
-    nseg[s] = owner_of(A, first + A.slab[s].tiles - 1, G) - owner_of(A, first, G) + 1;
-  }
-  __syncthreads();
-  for (int q = threadIdx.x; q < A.n_slab * DUSTIN_MAX_PAIRS; q += blockDim.x) {
-    const int s = q / DUSTIN_MAX_PAIRS, p = q - s * DUSTIN_MAX_PAIRS;
-    const ScoreSlab& S = A.slab[s];
-    if (p >= S.npairs) continue;
-    // row index: channel-major, slabs in order, then pairs
-    int r = 0;
-    for (int s2 = 0; s2 < A.n_slab; ++s2) {
-      if (A.slab[s2].channel < S.channel || (A.slab[s2].channel == S.channel && s2 < s))
-        r += A.slab[s2].npairs;
-    }
-    r += p;
+  // merged statistics, one row per thread: M and 1 / S over the segments
+  // (the CTAs owning the first to the last tile of (slab, sequence bl))
+  for (int r = tid; r < nr; r += kNormThreads) {
+    const int j = slab_of_row(si, ns, r);
+    const int p = r - si[j].row0, tiles = si[j].tiles;
+    const long long P0 = si[j].cost_start + (long long)bl * tiles * si[j].cost;
+    const int seg0 = owner_at_cost(P0, A.total_cost, A.grid);
+    const int n_seg = owner_at_cost(P0 + (long long)(tiles - 1) * si[j].cost, A.total_cost, A.grid) - seg0 + 1;
+    const float* slots = A.stats + (size_t(si[j].slab) * A.nb + bl) * A.max_seg * size_t(A.np_max) * 2;
     float m = -INFINITY, sm = 0.f;
-    const int n_seg = nseg[s];
-    const float* slots = A.stats + (size_t(s) * A.nb + bl) * A.max_seg * size_t(A.np_max) * 2;
     for (int g = 0; g < n_seg; g += 4) {
       float2 v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (g + u < n_seg)
-          v[u] = __ldcg(reinterpret_cast<const float2*>(slots + (size_t(g + u) * A.np_max + p) * 2));
+        if (g + u < n_seg) v[u] = __ldcg(reinterpret_cast<const float2*>(slots + (size_t(g + u) * A.np_max + p) * 2));
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         if (g + u < n_seg) stat_merge(m, sm, v[u].x, v[u].y);
     }
-    roff[r] = S.logit_off + (long long)(size_t(bl) * S.npairs + p) * A.LSP;
     Mg[r] = m;
     Ig[r] = sm > 0.f ? 1.f / sm : 0.f;
   }
   __syncthreads();
-  const int base = blockIdx.x * kNormChunk;
-  // A warp covers 32 positions per pass: lane = (row group rg, position quad);
-  // a thread sums rows rg, rg + 4, ... of its 4 positions with every load of
-  // a batch in flight, then the 4 row groups are reduced with shuffles.
-  // (Rows are padded to a multiple of 32 floats, so the float4 loads are
-  // aligned and in bounds.)
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int quad = lane & 7, rg = lane >> 3;
-  const int n0 = nrow[0], nr = nrow[0] + nrow[1];
-  for (int sub = 0; sub < kNormChunk; sub += kNormThreads) {
-    const int pos = base + sub + warp * 32 + quad * 4;
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    if (pos < L) {
-      for (int rb = rg; rb < nr; rb += 4 * kNormRows) {
-        float4 l[kNormRows];
-#pragma unroll
-        for (int u = 0; u < kNormRows; ++u) {
-          const int r = rb + 4 * u;
-          if (r < nr) l[u] = __ldcs(reinterpret_cast<const float4*>(A.logits + roff[r] + pos));
-        }
-#pragma unroll
-        for (int u = 0; u < kNormRows; ++u) {
-          const int r = rb + 4 * u;
-          if (r < nr) {
-            const float M = Mg[r], I = Ig[r];
-            const int c = r < n0 ? 0 : 1;
-            acc[c][0] += fast_exp2(l[u].x - M) * I;
-            acc[c][1] += fast_exp2(l[u].y - M) * I;
-            acc[c][2] += fast_exp2(l[u].z - M) * I;
-            acc[c][3] += fast_exp2(l[u].w - M) * I;
-          }
-        }
-      }
+  float acc0 = 0.f, acc1 = 0.f;
+  uint32_t phase = 0;
+  for (int r0 = 0; r0 < nr; r0 += kNormRowsMax, phase ^= 1u) {
+    const int n = min(kNormRowsMax, nr - r0);
+    if (r0 > 0) {
+      __syncthreads();   // every thread is done with the previous batch
+      if (tid == 0) mbar_arrive_expect_tx(bar, uint32_t(n) * npos * 4);
+      __syncthreads();
+      issue(r0, n);
     }
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc[c][e] += __shfl_xor_sync(0xffffffffu, acc[c][e], 8);
-        acc[c][e] += __shfl_xor_sync(0xffffffffu, acc[c][e], 16);
-      }
-    if (rg == 0) {
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float* out = A.importance + (size_t(b) * 2 + c) * A.Lcap;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (pos + e < A.Lcap) out[pos + e] = (pos + e < L) ? acc[c][e] : 0.f;
+    mbar_wait(bar, phase, A.err, nullptr);
+    // the slice of this thread's row has landed: drop it from L2 without
+    // write-back (the logits are dead once staged)
+    if (my_src)
+      for (int ln = 0; ln < lines; ++ln)
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(my_src + ln * 32) : "memory");
+    if (tid < npos) {
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) {
+        const int r = r0 + j;
+        const float v = fast_exp2(lg[size_t(j) * kNormThreads + tid] - Mg[r]) * Ig[r];
+        if (r < n0) acc0 += v;
+        else acc1 += v;
       }
     }
   }
-  // the logits of this chunk are dead: drop them from L2 without write-back
-  __syncthreads();
-  const int lines_per_row = kNormChunk * 4 / 128;
-  const int nrows = nrow[0] + nrow[1];
-  for (int q = threadIdx.x; q < nrows * lines_per_row; q += blockDim.x) {
-    const int r = q / lines_per_row;
-    const int ln = q - r * lines_per_row;
-    if (base + ln * 32 < A.LSP)
-      asm volatile("discard.global.L2 [%0], 128;" ::"l"(A.logits + roff[r] + base + ln * 32) : "memory");
+  const int pos = base + tid;
+  const bool live = pos < L;
+  if (pos < A.Lcap) {
+    A.importance[(size_t(b) * 2 + 0) * A.Lcap + pos] = live ? acc0 : 0.f;
+    A.importance[(size_t(b) * 2 + 1) * A.Lcap + pos] = live ? acc1 : 0.f;
+  }
+  if (A.hist) {
+    const int s_eff = min(A.sinks, L);
+    const int w0 = max(L - A.window, s_eff);
+    const bool in_u = pos >= s_eff && pos < w0;
+    int* h = A.hist + size_t(b) * 2 * kSelectBins;
+    // (positions past seq_len hold stale logits: they are never keyed)
+    hist_red(h, in_u ? select_bin(importance_key(acc0, A.err)) : 0u, in_u, lane);
+    hist_red(h + kSelectBins, in_u ? select_bin(importance_key(acc1, A.err)) : 0u, in_u, lane);
   }
 }
 
@@ -483,6 +505,11 @@ cudaError_t launch_stream(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_
 
 size_t score_stream_smem() {
   return size_t(kStages) * kTileBytes + kConsumers * 32 * 2 * 4 + kStages * 16 + 16 + 1024;
+}
+
+size_t score_norm_smem(int n_rows) {
+  const int nb = n_rows < kNormRowsMax ? n_rows : kNormRowsMax;
+  return size_t(nb) * kNormThreads * 4 + size_t(2 * n_rows + 2) * 4 + 16;
 }
 
 int score_rows_per_tile(int D) { return D == 128 ? kBoxRows : 2 * kBoxRows; }
@@ -506,8 +533,11 @@ cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t
   }
   if (e != cudaSuccess) return e;
   if (after_stream && (e = cudaEventRecord(after_stream, stream)) != cudaSuccess) return e;
-  dim3 grid((a.Lcap + kNormChunk - 1) / kNormChunk, a.nb);
-  return launch_pdl(score_norm_kernel, grid, dim3(kNormThreads), 0, stream, a);
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      score_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(score_norm_smem(DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS)));
+  if (attr != cudaSuccess) return attr;
+  dim3 grid((a.LSP + kNormThreads - 1) / kNormThreads, a.nb);
+  return launch_pdl(score_norm_kernel, grid, dim3(kNormThreads), pl.norm_smem, stream, a);
 }
 
 }  // namespace dustin

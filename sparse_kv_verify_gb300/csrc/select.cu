@@ -4,147 +4,150 @@
 // by the draft signal, then the most relevant remaining tokens by the target
 // signal).
 //
-// One thread-block cluster of CS CTAs per sequence (CS = 8, 4, 2 or 1: the
-// largest size whose B clusters are all resident at once); CTA r owns a
-// contiguous slice of the unprotected positions.  Importance values are
-// non-negative fp32, so their bit patterns order like the values.  Each tier
-// finds the exact threshold key T of its top-cnt (descending key, ties to the
-// lower index):
-//   level 1  4096-bin histograms of the top 12 bits (sign, exponent and 3
-//            mantissa bits) of both channels are built while the keys are
-//            staged in shared memory; per tier they are merged across the
-//            cluster through distributed shared memory (each rank merges one
-//            slice of the bins), which gives the bin b1 that holds the cnt-th
-//            key.  The draft tier's winners are taken out of the target
-//            histogram as they are written.
-//   pass A   one pass over the CTA's keys gathers the keys of bin b1 with their
-//            positions and counts, per warp chunk, the keys above bin b1.
-//   exact T  every CTA pulls all ranks' bin-b1 keys and finds T and the number
-//            of keys equal to T that are taken with two local 10-bit radix
-//            passes -- no cluster barrier -- and, from the same lists, how many
-//            keys above T and equal to T lower ranks and lower warp chunks hold.
-//   write    one ordered pass writes every key above T and the lowest-index
-//            keys equal to T at their offsets (the draft tier also marks them
-//            in a per-slice bitmap that the target tier skips).
-// If the threshold bin holds more keys than the candidate lists take (heavy
-// ties), T is found with histograms merged across the cluster instead, over
-// the candidate lists where they fit and over whole slices where they do not.
-#include <cooperative_groups.h>
-
-#include <mutex>
-#include <vector>
-
+// Importance values are non-negative fp32, so their bit patterns order like the
+// values.  A tier takes the top cnt keys of its channel (descending key, ties
+// to the lower position) among the unprotected positions U = [sinks, L -
+// window) not taken by an earlier tier; the draft tier takes m1 keys of
+// channel 0, the target tier f keys of channel 1.
+//
+// Input: 4096-bin histograms of the top 12 key bits of both channels over U,
+// per sequence (built by the scoring kernel while it writes the importance,
+// or by select_hist_kernel for a standalone call).
+//
+// select_kernel: CS CTAs of 1024 threads per sequence, each owning one
+// contiguous run of U (each warp a run of whole 128-position rows).
+//   scan     every CTA finds, from the histograms, the bin b0 holding the m1-th
+//            draft key and the bin b1 holding the (m1 + f)-th target key, and
+//            in one pass (float4 loads) lists, in position order, the draft
+//            keys of bins >= b0 and the target keys of bins >= b1 of its run.
+//            Every draft winner is listed, and so is every target winner: the
+//            f-th target key outside the draft tier is at least the (m1+f)-th
+//            target key of U, because at most m1 of the top m1+f are taken
+//            by the draft tier.  The lists go to the workspace.
+//   finish   the last CTA of the sequence to arrive (an atomic counter; no CTA
+//            waits for another) gathers the lists and selects exactly:
+//            draft tier -- two 10-bit radix passes over the listed keys of bin
+//            b0 give the threshold key T and how many keys equal to T are
+//            taken (the lowest positions), then one ordered compaction of the
+//            list writes the tier; target tier -- the same over the target
+//            list minus the draft tier, with the target histogram corrected by
+//            the draft tier's target keys.
+// If a list outgrows its buffer (heavy ties) or the draft tier is larger than
+// the on-chip copy of it, the finishing CTA selects that sequence with the
+// general path: candidates of the threshold bin in a shared list (or, past its
+// capacity, refinement over the whole range) and ordered passes over all keys.
+// Every path gives the same set.
 #include "common.cuh"
 #include "kernels.h"
-
-namespace cg = cooperative_groups;
 
 namespace dustin {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBins1 = 4096;      // top 12 bits
-constexpr int kBins2 = 1024;      // 10 bits
-constexpr int kCandCap = 2048;    // (key, position) candidates per CTA
-constexpr int kPullCap = 4096;    // candidate keys of all ranks pulled into one CTA
-constexpr int kBatch = 8;         // independent key loads in flight per thread
-constexpr size_t kSmemBudget = 220 * 1024;
+constexpr int kBins1 = kSelectBins;   // top 12 bits
+constexpr int kBins2 = 1024;          // 10 bits per refinement pass
+constexpr int kListCap = 128;         // entries per warp list and channel (scan)
+constexpr int kCandCap = 4096;        // candidates of the general path
+constexpr int kFinCap = 8192;         // list entries gathered on chip (finish)
+constexpr int kDCap = 8192;           // draft-tier positions kept on chip (finish)
+constexpr int kBatch = 8;             // rows of 32 keys loaded before use (general path)
+constexpr int kHistThreads = 1024;    // select_hist_kernel: positions per CTA
 
-// CS: CTAs per sequence (the cluster size); rank r merges level-1 bins
-// [r * 4096 / CS, (r + 1) * 4096 / CS)
-template <int CS>
 struct SelShared {
-  static constexpr int kSliceBins = kBins1 / CS;
-  static constexpr int kScratch = kSliceBins > kBins2 ? kSliceBins : kBins2;
-  int h1[2][kBins1];         // level-1 histograms of this CTA's keys, per channel
-  int gsl[kSliceBins];       // merged level-1 counts of this rank's bin slice
-  int scratch[kScratch];     // a merged slice copy / local radix histograms
+  int h[2][kBins1];          // level-1 histograms of the tiers' positions
+  int h2[kBins2];            // refinement histogram
   union {
-    uint32_t pulled[kPullCap];   // every rank's threshold-bin keys, in rank order
-    int hist2[2][kBins2];        // or: cluster-merged refinement histograms (heavy ties)
-  };
-  uint32_t ckey[kCandCap];   // this CTA's keys of the threshold bin ...
-  int cpos[kCandCap];        // ... and their positions
-  int wabove[kWarps];        // per warp chunk: keys above the threshold bin
-  int wgt[kWarps], weq[kWarps], wsum[kWarps];
-  int rgt[CS], req[CS];      // per rank: pulled keys above / equal to T
-  int poff[CS + 1];          // offsets of the ranks' lists in pulled
-  int gsl_total, ncand, n_above;
-  int bin, need, slice, need1;
-  int gt_before, eq_before, cnt_gt, cnt_eq;
-  int overflow;
+    struct {                 // scan: per-warp ordered lists of both channels
+      uint32_t key[2][kWarps][kListCap];
+      int pos[2][kWarps][kListCap];
+    } l;
+    struct {                 // general path: threshold-bin candidates
+      uint32_t key[kCandCap];
+      int pos[kCandCap];
+    } c;
+    struct {                 // finish: one channel's gathered list
+      uint32_t key[kFinCap];
+      int pos[kFinCap];
+    } e;
+  } u;
+  int dpos[kDCap];           // finish: the draft tier, ascending
+  uint32_t drop[kFinCap / 32];    // finish: target-list entries in the draft tier
+  int lcnt[2][kWarps];
+  int wsum[kWarps];          // scan scratch
+  int wgt[kWarps], weq[kWarps];   // per warp: keys above / equal to T
+  int gtb[kWarps], eqb[kWarps];   // exclusive prefixes of wgt, weq
+  int goff[kMaxSelectCtas + 1];   // finish: list offsets of the scan CTAs
+  int ncand, bin, need, found, overflow, last, tot;
 };
 
-__device__ __forceinline__ uint32_t key_of(float v, int* err) {
-  const uint32_t u = __float_as_uint(v);
-  if (v != v) {
-    flag_error(err, DUSTIN_DEV_NAN);
-    return 0u;
-  }
-  if (u & 0x80000000u) {
-    if (u != 0x80000000u) flag_error(err, DUSTIN_DEV_NAN);
-    return 0u;
-  }
-  return u;
-}
+// ------------------------------------------------------------------ helpers
 
-struct KeySrc {
-  const uint32_t* cached;  // shared-memory copy of the slice (indexed from its start)
-  const float* global;     // importance row of this channel (indexed by position)
-  int base;                // first position of the slice
+// Key of position i of one channel's importance row.
+struct Keys {
+  const float* row;
   int* err;
-  __device__ __forceinline__ uint32_t operator()(int i) const {
-    return cached ? cached[i - base] : key_of(global[i], err);
-  }
+  __device__ __forceinline__ uint32_t operator()(int i) const { return importance_key(__ldg(row + i), err); }
 };
 
+// Positions taken by the draft tier (general path): bit (i - b0) of a bitmap.
 struct Excl {
-  const uint32_t* bits;    // bitmap of the slice (bit i - base), or nullptr
-  int base;
+  const uint32_t* bits;
+  int b0;
   __device__ __forceinline__ bool operator()(int i) const {
     if (!bits) return false;
-    const int o = i - base;
+    const int o = i - b0;
     return (bits[o >> 5] >> (o & 31)) & 1u;
   }
 };
 
-// The slice [s0, s1) cut into one contiguous, 32-aligned chunk per warp (the
-// order in which positions are written).
+// [s0, s1) cut into one contiguous run of whole 32-position rows per warp,
+// starting at the 32-aligned a0 <= s0.
 struct Chunks {
-  int a0, chunk;
-  __device__ Chunks(int s0, int s1) {
+  int s0, s1, a0, chunk;
+  __device__ Chunks(int s0_, int s1_) : s0(s0_), s1(s1_) {
     a0 = s0 & ~31;
-    chunk = (((s1 - a0 + kWarps - 1) / kWarps) + 31) & ~31;
-    if (chunk == 0) chunk = 32;
+    chunk = ((((s1 - a0) + kWarps - 1) / kWarps) + 31) & ~31;
+    if (chunk <= 0) chunk = 32;
   }
-  __device__ __forceinline__ int of(int i) const { return (i - a0) / chunk; }
+  __device__ __forceinline__ int w0(int w) const { return a0 + w * chunk; }
+  __device__ __forceinline__ int w1(int w) const { return min(a0 + (w + 1) * chunk, s1); }
+  __device__ __forceinline__ int warp_of(int i) const { return (i - a0) / chunk; }
 };
 
-// Calls f(i, key, valid) for every i in [u0, u1), block-strided, kBatch loads
-// in flight before use; every lane of every warp makes the same calls.
+// Adds one to h[bin] for every lane with ok, one atomic per distinct bin of
+// the warp (h in shared or global memory).
+__device__ __forceinline__ void hist_add(int* h, uint32_t bin, bool ok, int lane) {
+  const uint32_t mask = __match_any_sync(0xffffffffu, ok ? bin : 0xFFFFFFFFu);
+  if (ok && lane == __ffs(mask) - 1) atomicAdd(&h[bin], __popc(mask));
+}
+
+// Calls f(i, key, ok) for every position of this warp's rows of 32 (general
+// path); ok = i in [s0, s1) and not excluded.  kBatch rows in flight.
 template <typename F>
-__device__ __forceinline__ void for_keys(const KeySrc& key, int u0, int u1, const Excl& ex, F f) {
-  for (int base = u0; base < u1; base += kThreads * kBatch) {
+__device__ __forceinline__ void for_rows(const Keys& key, const Chunks& ck, const Excl& ex, F f) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w0 = ck.w0(warp), w1 = ck.w1(warp);
+  for (int gb = w0; gb < w1; gb += 32 * kBatch) {
     uint32_t kv[kBatch];
     bool ok[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * kThreads + int(threadIdx.x);
-      ok[u] = i >= key.base && i < u1 && !ex(i);
+      const int i = gb + 32 * u + lane;
+      ok[u] = i >= ck.s0 && i < w1 && !ex(i);
       kv[u] = ok[u] ? key(i) : 0u;
     }
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) f(base + u * kThreads + int(threadIdx.x), kv[u], ok[u]);
+    for (int u = 0; u < kBatch; ++u)
+      if (gb + 32 * u < w1) f(gb + 32 * u + lane, kv[u], ok[u]);
   }
 }
 
 // Over hist[0..nbins) in descending bin order: the bin holding the need-th
-// key, and how many keys of that bin are needed (written to sh.bin, sh.need).
-// Whole-block call; nbins is a multiple of kThreads.
-template <typename Sh>
-__device__ void find_bin(Sh& sh, const int* hist, int nbins, int need) {
+// key and how many keys of it are needed (sh.bin, sh.need; sh.found = 0 if the
+// histogram holds fewer than need keys).  Whole-block call.
+__device__ void find_bin(SelShared& sh, const int* hist, int nbins, int need) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q = nbins / kThreads;
   int local = 0;
@@ -156,16 +159,17 @@ __device__ void find_bin(Sh& sh, const int* hist, int nbins, int need) {
     if (lane >= o) incl += y;
   }
   if (lane == 31) sh.wsum[warp] = incl;
+  if (tid == 0) sh.found = 0;
   __syncthreads();
   if (warp == 0) {
-    const int w = lane < kWarps ? sh.wsum[lane] : 0;
+    const int w = sh.wsum[lane];
     int wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, wi, o);
       if (lane >= o) wi += y;
     }
-    if (lane < kWarps) sh.wsum[lane] = wi - w;   // exclusive prefix
+    sh.wsum[lane] = wi - w;   // exclusive prefix
   }
   __syncthreads();
   const int before = sh.wsum[warp] + incl - local;
@@ -177,6 +181,7 @@ __device__ void find_bin(Sh& sh, const int* hist, int nbins, int need) {
       if (acc + h >= need) {
         sh.bin = bin;
         sh.need = need - acc;
+        sh.found = 1;
         break;
       }
       acc += h;
@@ -185,334 +190,327 @@ __device__ void find_bin(Sh& sh, const int* hist, int nbins, int need) {
   __syncthreads();
 }
 
-// Heavy ties: the threshold key T below bin b1 from 10-bit histograms merged
-// across the cluster (over the candidate lists where every CTA's fits, over
-// the whole slice where it does not), then the per-warp and per-rank counts
-// of keys above / equal to T.  Whole-cluster call; returns T, sets need.
-template <int CS>
-__device__ uint32_t slow_threshold(cg::cluster_group& cluster, const KeySrc& key, int s0, int s1,
-                                   const Excl& ex, const Chunks& ck, uint32_t b1, int& need,
-                                   SelShared<CS>& sh, int& hbuf) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rank = int(cluster.block_rank());
-  const int ncand = sh.ncand;
-  const bool listed = ncand <= kCandCap;
+// Exclusive prefixes of the per-warp counts wgt, weq into gtb, eqb.
+__device__ void warp_prefixes(SelShared& sh) {
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    const int g = sh.wgt[tid], e = sh.weq[tid];
+    int gi = g, ei = e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, gi, o);
+      const int z = __shfl_up_sync(0xffffffffu, ei, o);
+      if (tid >= o) {
+        gi += y;
+        ei += z;
+      }
+    }
+    sh.gtb[tid] = gi - g;
+    sh.eqb[tid] = ei - e;
+  }
+  __syncthreads();
+}
+
+// Two 10-bit radix passes below the 12-bit prefix b1: the exact threshold key
+// T and, in *need, how many keys equal to T are taken.  visit(f) calls
+// f(key, ok) for every candidate key (keys outside bin b1 must have ok false).
+template <typename V>
+__device__ uint32_t refine(SelShared& sh, uint32_t b1, int* need, V visit) {
   uint32_t prefix = b1 << 20;
   for (int pass = 0; pass < 2; ++pass) {
     const int shift = 10 - 10 * pass;
     const uint32_t hi_mask = 0xFFFFFFFFu << (shift + 10);
-    int* h = sh.hist2[hbuf];
-    for (int b = tid; b < kBins2; b += kThreads) h[b] = 0;
+    sh.h2[threadIdx.x] = 0;
     __syncthreads();
-    if (listed) {
-      for (int c = tid; c < ncand; c += kThreads) {
-        const uint32_t kv = sh.ckey[c];
-        if ((kv & hi_mask) == prefix) atomicAdd(&h[(kv >> shift) & 1023u], 1);
-      }
-    } else {
-      for_keys(key, s0, s1, ex, [&](int, uint32_t kv, bool ok) {
-        if (ok && (kv & hi_mask) == prefix) atomicAdd(&h[(kv >> shift) & 1023u], 1);
-      });
-    }
-    cluster.sync();
-    for (int j = tid; j < kBins2; j += kThreads) {
-      int v[CS];
-#pragma unroll
-      for (int q = 0; q < CS; ++q) v[q] = *cluster.map_shared_rank(&h[j], q);
-      int g = 0;
-#pragma unroll
-      for (int q = 0; q < CS; ++q) g += v[q];
-      sh.scratch[j] = g;
-    }
+    visit([&](uint32_t kv, bool ok) {
+      if (ok && (kv & hi_mask) == prefix) atomicAdd(&sh.h2[(kv >> shift) & 1023u], 1);
+    });
     __syncthreads();
-    find_bin(sh, sh.scratch, kBins2, need);
+    find_bin(sh, sh.h2, kBins2, *need);
     prefix |= uint32_t(sh.bin) << shift;
-    need = sh.need;
-    hbuf ^= 1;   // the other buffer next: remote readers of this one may still run
+    *need = sh.need;
   }
-  const uint32_t T = prefix;
-  // per-warp counts of keys above / equal to T in this CTA's chunks
-  int ngt = 0, neq = 0;
-  const int w0 = ck.a0 + warp * ck.chunk, w1 = min(w0 + ck.chunk, s1);
-  for (int gb = w0; gb < w1; gb += 32 * kBatch) {
-    uint32_t kv[kBatch];
-    bool cv[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = gb + 32 * u + lane;
-      cv[u] = i >= s0 && i < w1 && !ex(i);
-      kv[u] = cv[u] ? key(i) : 0u;
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      ngt += __popc(__ballot_sync(0xffffffffu, cv[u] && kv[u] > T));
-      neq += __popc(__ballot_sync(0xffffffffu, cv[u] && kv[u] == T));
-    }
-  }
-  if (lane == 0) {
-    sh.wgt[warp] = ngt;
-    sh.weq[warp] = neq;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int g = 0, e = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      g += sh.wgt[w];
-      e += sh.weq[w];
-    }
-    sh.cnt_gt = g;
-    sh.cnt_eq = e;
-  }
-  cluster.sync();
-  if (tid == 0) {
-    int g = 0, e = 0;
-    for (int q = 0; q < rank; ++q) {
-      g += *cluster.map_shared_rank(&sh.cnt_gt, q);
-      e += *cluster.map_shared_rank(&sh.cnt_eq, q);
-    }
-    sh.gt_before = g;
-    sh.eq_before = e;
-  }
-  __syncthreads();
-  return T;
+  return prefix;
 }
 
-// Top `cnt` of the cluster's candidates (this CTA: [s0, s1) of key, minus ex)
-// by (key desc, index asc), given this CTA's level-1 histogram h of them;
-// writes this CTA's selected positions to out at its offset, and for the draft
-// tier sets their bits in setbits and takes their target keys (sub) out of the
-// target histogram.  Whole-cluster call.
-template <int CS>
-__device__ void tier_select(cg::cluster_group& cluster, const KeySrc& key, int s0, int s1,
-                            const Excl& ex, int cnt, int* h, int32_t* out, uint32_t* setbits,
-                            const KeySrc* sub, SelShared<CS>& sh, int& hbuf) {
-  constexpr int kSliceBins = SelShared<CS>::kSliceBins;
+// Writes one selected position: its slot (guarded: a histogram that disagreed
+// with the keys could otherwise push it past the tier), the draft tier's
+// bitmap bit and its target key taken out of the target histogram.
+struct Emit {
+  int32_t* out;
+  int cnt;
+  uint32_t* bits;    // draft tier: bitmap to mark, else nullptr
+  int b0;
+  const Keys* sub1;  // draft tier: target keys to take out, else nullptr
+  int* h1;
+  int* err;
+  __device__ __forceinline__ void operator()(int o, int i) const {
+    if (o < cnt) out[o] = i;
+    else flag_error(err, DUSTIN_DEV_NAN);
+    if (bits) atomicOr(&bits[(i - b0) >> 5], 1u << ((i - b0) & 31));
+    if (sub1) atomicSub(&h1[select_bin((*sub1)(i))], 1);
+  }
+};
+
+// ----------------------------------------------------------- general path
+
+// One tier over the whole range [s0, s1) minus ex, given the level-1
+// histogram h of exactly those keys.
+__device__ void tier_general(SelShared& sh, const Keys& key, const Excl& ex, int s0, int s1, int cnt,
+                             const int* h, const Emit& emit, int* err) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rank = int(cluster.block_rank());
-  if (cnt <= 0) return;   // same for every CTA of the cluster
+  const uint32_t lt = (1u << lane) - 1u;
   const Chunks ck(s0, s1);
-
-  // ---- level 1: merge this rank's bin slice of every rank's histogram
-  cluster.sync();                                   // A: every histogram complete
-  // (ncand is reset only now: until every rank has passed barrier A, another
-  // rank may still be reading this rank's previous candidate list)
-  if (tid < kWarps) sh.wabove[tid] = 0;
-  if (tid == 0) sh.ncand = 0;
-  {
-    int part = 0;
-    for (int j = tid; j < kSliceBins; j += kThreads) {
-      const int bin = rank * kSliceBins + j;
-      int v[CS];
-#pragma unroll
-      for (int q = 0; q < CS; ++q) v[q] = *cluster.map_shared_rank(&h[bin], q);
-      int g = 0;
-#pragma unroll
-      for (int q = 0; q < CS; ++q) g += v[q];
-      sh.gsl[j] = g;
-      part += g;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    if (lane == 0) sh.wsum[warp] = part;
+  find_bin(sh, h, kBins1, cnt);
+  if (!sh.found) {   // inconsistent histogram: cannot happen with matching keys
+    if (tid == 0) flag_error(err, DUSTIN_DEV_NAN);
+    for (int j = tid; j < cnt; j += kThreads) emit.out[j] = -1;
     __syncthreads();
-    if (tid == 0) {
-      int t = 0;
-      for (int w = 0; w < kWarps; ++w) t += sh.wsum[w];
-      sh.gsl_total = t;
-    }
+    return;
   }
-  cluster.sync();                                   // B: every slice merged
-  if (tid == 0) {   // which rank's bin slice holds the cnt-th key (slices in descending order)
-    int acc = 0;
-    sh.slice = 0;
-    sh.need1 = cnt;
-    for (int q = CS - 1; q >= 0; --q) {
-      const int t = *cluster.map_shared_rank(&sh.gsl_total, q);
-      if (acc + t >= cnt) {
-        sh.slice = q;
-        sh.need1 = cnt - acc;
-        break;
-      }
-      acc += t;
-    }
-  }
-  __syncthreads();
-  const int rs = sh.slice;
-  for (int j = tid; j < kSliceBins; j += kThreads) sh.scratch[j] = *cluster.map_shared_rank(&sh.gsl[j], rs);
-  __syncthreads();
-  find_bin(sh, sh.scratch, kSliceBins, sh.need1);
-  const uint32_t b1 = uint32_t(rs * kSliceBins + sh.bin);
+  const uint32_t b1 = uint32_t(sh.bin);
   int need = sh.need;
+  if (tid == 0) sh.ncand = 0;
+  __syncthreads();
 
-  // ---- pass A: keys of bin b1 (with positions); per chunk, keys above bin b1
-  // (walked from the 32-aligned slice start: a warp row of 32 positions lies in
-  // one chunk, so the above-bin count takes one ballot and one atomic per row)
-  const Excl exA{ex.bits, ex.base};
-  for_keys(key, ck.a0, s1, exA, [&](int i, uint32_t kv, bool ok0) {
-    const bool ok = ok0 && i >= s0;
-    const uint32_t bin = kv >> 20;
-    const uint32_t above = __ballot_sync(0xffffffffu, ok && bin > b1);
-    if (above && lane == 0) atomicAdd(&sh.wabove[ck.of(i)], __popc(above));
+  // ---- pass A: keys above bin b1 per warp; the keys of bin b1
+  int above = 0;
+  for_rows(key, ck, ex, [&](int i, uint32_t kv, bool ok) {
+    const uint32_t bin = select_bin(kv);
+    above += __popc(__ballot_sync(0xffffffffu, ok && bin > b1));
     const bool hit = ok && bin == b1;
     const uint32_t ball = __ballot_sync(0xffffffffu, hit);
     if (ball) {
       int slot0 = 0;
       if (lane == 0) slot0 = atomicAdd(&sh.ncand, __popc(ball));
       slot0 = __shfl_sync(0xffffffffu, slot0, 0);
-      const int slot = slot0 + __popc(ball & ((1u << lane) - 1u));
+      const int slot = slot0 + __popc(ball & lt);
       if (hit && slot < kCandCap) {
-        sh.ckey[slot] = kv;
-        sh.cpos[slot] = i;
+        sh.u.c.key[slot] = kv;
+        sh.u.c.pos[slot] = i;
       }
     }
   });
-  __syncthreads();
-  if (tid == 0) {
-    int a = 0;
-    for (int w = 0; w < kWarps; ++w) a += sh.wabove[w];
-    sh.n_above = a;
-  }
-  cluster.sync();                                   // C: candidate lists published
-  if (tid == 0) {
-    int off = 0, over = 0;
-    for (int q = 0; q < CS; ++q) {
-      const int n = *cluster.map_shared_rank(&sh.ncand, q);
-      sh.poff[q] = off;
-      if (n > kCandCap) over = 1;
-      off += n;
-    }
-    sh.poff[CS] = off;
-    sh.overflow = over || off > kPullCap;
+  if (lane == 0) {
+    sh.wgt[warp] = above;
+    sh.weq[warp] = 0;
   }
   __syncthreads();
+  const int ncand = sh.ncand;
+  const bool listed = ncand <= kCandCap;
 
-  uint32_t T;
-  if (!sh.overflow) {
-    // ---- exact threshold from every rank's bin-b1 keys, locally
-    const int total = sh.poff[CS];
-#pragma unroll
-    for (int q = 0; q < CS; ++q) {
-      const int o = sh.poff[q], n = sh.poff[q + 1] - o;
-      const uint32_t* src = cluster.map_shared_rank(sh.ckey, q);
-      for (int j = tid; j < n; j += kThreads) sh.pulled[o + j] = src[j];
+  // ---- refine
+  const uint32_t T = refine(sh, b1, &need, [&](auto f) {
+    if (listed) {
+      for (int c = tid; c < ncand; c += kThreads) f(sh.u.c.key[c], true);
+    } else {
+      for_rows(key, ck, ex, [&](int, uint32_t kv, bool ok) { f(kv, ok && select_bin(kv) == b1); });
     }
-    uint32_t prefix = b1 << 20;
-    for (int pass = 0; pass < 2; ++pass) {
-      const int shift = 10 - 10 * pass;
-      const uint32_t hi_mask = 0xFFFFFFFFu << (shift + 10);
-      for (int b = tid; b < kBins2; b += kThreads) sh.scratch[b] = 0;
-      __syncthreads();
-      for (int j = tid; j < total; j += kThreads) {
-        const uint32_t kv = sh.pulled[j];
-        if ((kv & hi_mask) == prefix) atomicAdd(&sh.scratch[(kv >> shift) & 1023u], 1);
-      }
-      __syncthreads();
-      find_bin(sh, sh.scratch, kBins2, need);
-      prefix |= uint32_t(sh.bin) << shift;
-      need = sh.need;
-    }
-    T = prefix;
-    // per rank and per warp chunk: keys above / equal to T
-    if (tid < CS) {
-      sh.rgt[tid] = 0;
-      sh.req[tid] = 0;
-    }
-    if (tid < kWarps) {
-      sh.wgt[tid] = sh.wabove[tid];
-      sh.weq[tid] = 0;
-    }
-    __syncthreads();
-    for (int j = tid; j < total; j += kThreads) {
-      const uint32_t kv = sh.pulled[j];
-      if (kv >= T) {
-        int q = 0;
-        while (j >= sh.poff[q + 1]) ++q;
-        atomicAdd(kv > T ? &sh.rgt[q] : &sh.req[q], 1);
-      }
-    }
-    const int ncand = sh.ncand;
+  });
+  const int need_eq = need;
+
+  // ---- per warp chunk: keys of bin b1 above / equal to T
+  if (listed) {
     for (int c = tid; c < ncand; c += kThreads) {
-      const uint32_t kv = sh.ckey[c];
-      if (kv >= T) atomicAdd(kv > T ? &sh.wgt[ck.of(sh.cpos[c])] : &sh.weq[ck.of(sh.cpos[c])], 1);
+      const uint32_t kv = sh.u.c.key[c];
+      const int w = ck.warp_of(sh.u.c.pos[c]);
+      if (kv >= T) atomicAdd(kv > T ? &sh.wgt[w] : &sh.weq[w], 1);
     }
-    __syncthreads();
-    if (tid == 0) {
-      int g = 0, e = 0;
-      for (int q = 0; q < rank; ++q) {
-        g += *cluster.map_shared_rank(&sh.n_above, q) + sh.rgt[q];
-        e += sh.req[q];
-      }
-      sh.gt_before = g;
-      sh.eq_before = e;
-    }
-    __syncthreads();
   } else {
-    T = slow_threshold(cluster, key, s0, s1, ex, ck, b1, need, sh, hbuf);
-  }
-
-  // ---- ordered write: every key above T and the lowest-index keys equal to T
-  int gt_before = sh.gt_before, eq_before = sh.eq_before;
-  for (int w = 0; w < warp; ++w) {
-    gt_before += sh.wgt[w];
-    eq_before += sh.weq[w];
-  }
-  int pos = gt_before + min(eq_before, need);
-  int eq_run = eq_before;
-  const uint32_t lt = (1u << lane) - 1u;
-  const int w0 = ck.a0 + warp * ck.chunk, w1 = min(w0 + ck.chunk, s1);
-  for (int gb = w0; gb < w1; gb += 32 * kBatch) {
-    uint32_t kv[kBatch];
-    bool cv[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = gb + 32 * u + lane;
-      cv[u] = i >= s0 && i < w1 && !ex(i);
-      kv[u] = cv[u] ? key(i) : 0u;
+    int ngt = 0, neq = 0;
+    for_rows(key, ck, ex, [&](int, uint32_t kv, bool ok) {
+      const bool inb = ok && select_bin(kv) == b1;
+      ngt += __popc(__ballot_sync(0xffffffffu, inb && kv > T));
+      neq += __popc(__ballot_sync(0xffffffffu, inb && kv == T));
+    });
+    if (lane == 0) {
+      sh.wgt[warp] += ngt;
+      sh.weq[warp] = neq;
     }
+  }
+  __syncthreads();
+  warp_prefixes(sh);
+
+  // ---- ordered write over every key
+  int o = sh.gtb[warp] + min(sh.eqb[warp], need_eq);
+  int eq_run = sh.eqb[warp];
+  for_rows(key, ck, ex, [&](int i, uint32_t kv, bool ok) {
+    const bool isgt = ok && kv > T;
+    const bool iseq = ok && kv == T;
+    const uint32_t eqm = __ballot_sync(0xffffffffu, iseq);
+    const bool sel = isgt || (iseq && eq_run + __popc(eqm & lt) < need_eq);
+    const uint32_t selm = __ballot_sync(0xffffffffu, sel);
+    if (sel) emit(o + __popc(selm & lt), i);
+    o += __popc(selm);
+    eq_run += __popc(eqm);
+  });
+  __syncthreads();
+}
+
+// Both tiers of one sequence by the general path (one CTA): the histograms
+// are reloaded; a bitmap in the workspace marks the draft tier.
+__device__ void select_general(SelShared& sh, const SelectArgs& A, int b, int s_eff, int w0, int nP,
+                               int m1, int f, int32_t* out) {
+  const int tid = threadIdx.x;
+  uint32_t* gbits = A.bits + size_t(b) * A.bits_words;
+  const int* gh = A.hist + size_t(b) * 2 * kBins1;
+  for (int j = tid; j < 2 * kBins1; j += kThreads) (&sh.h[0][0])[j] = __ldcg(gh + j);
+  const int bm0 = s_eff & ~127;
+  const int nwords = (w0 - bm0 + 31) / 32;
+  for (int j = tid; j < nwords; j += kThreads) gbits[j] = 0u;
+  __syncthreads();
+  const float* row0 = A.imp + (size_t(b) * 2 + 0) * A.Lcap;
+  const float* row1 = A.imp + (size_t(b) * 2 + 1) * A.Lcap;
+  const Keys key0{row0, A.err}, key1{row1, A.err};
+  if (m1 > 0) {
+    const Emit emit{out + nP, m1, f > 0 ? gbits : nullptr, bm0, f > 0 ? &key1 : nullptr, sh.h[1], A.err};
+    tier_general(sh, key0, Excl{nullptr, bm0}, s_eff, w0, m1, sh.h[0], emit, A.err);
+  }
+  if (f > 0) {
+    const Emit emit{out + nP + m1, f, nullptr, bm0, nullptr, nullptr, A.err};
+    tier_general(sh, key1, Excl{m1 > 0 ? gbits : nullptr, bm0}, s_eff, w0, f, sh.h[1], emit, A.err);
+  }
+}
+
+// ------------------------------------------------------------ fast finish
+
+// Block-wide exclusive prefixes of two per-thread counts (in place).
+__device__ void block_prefix2(SelShared& sh, int& a, int& b) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int ia = a, ib = b;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int g0 = gb + 32 * u;
-      const int i = g0 + lane;
-      const bool isgt = cv[u] && kv[u] > T;
-      const bool iseq = cv[u] && kv[u] == T;
-      const uint32_t eqb = __ballot_sync(0xffffffffu, iseq);
-      const bool sel = isgt || (iseq && (eq_run + __popc(eqb & lt)) < need);
-      const uint32_t selb = __ballot_sync(0xffffffffu, sel);
-      if (sel) {
-        out[pos + __popc(selb & lt)] = i;
-        if (sub) atomicAdd(&sh.h1[1][(*sub)(i) >> 20], -1);
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, ia, o);
+    const int z = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) {
+      ia += y;
+      ib += z;
+    }
+  }
+  if (lane == 31) {
+    sh.wgt[warp] = ia;
+    sh.weq[warp] = ib;
+  }
+  __syncthreads();
+  warp_prefixes(sh);   // gtb, eqb: exclusive prefixes over the warps
+  a = sh.gtb[warp] + ia - a;
+  b = sh.eqb[warp] + ib - b;
+}
+
+// Exact top cnt of the gathered list sh.u.e[0..n) (in position order), minus
+// the entries marked in dropbits (if given), given the tier's level-1 bin b1
+// and how many of its keys are taken (need): written in position order to
+// out[0..cnt), and to dcopy if given.
+__device__ void finish_tier(SelShared& sh, int n, uint32_t b1, int need, int cnt, int32_t* out,
+                            int* dcopy, const uint32_t* dropbits) {
+  auto drop = [&](int j) { return dropbits && ((dropbits[j >> 5] >> (j & 31)) & 1u); };
+  const int tid = threadIdx.x;
+  const uint32_t T = refine(sh, b1, &need, [&](auto f) {
+    for (int j = tid; j < n; j += kThreads) {
+      const uint32_t kv = sh.u.e.key[j];
+      f(kv, select_bin(kv) == b1 && !drop(j));
+    }
+  });
+  const int need_eq = need;
+  // one contiguous run of entries per thread, in order
+  const int q = (n + kThreads - 1) / kThreads;
+  const int j0 = min(n, tid * q), j1 = min(n, j0 + q);
+  int ngt = 0, neq = 0;
+  for (int j = j0; j < j1; ++j) {
+    if (drop(j)) continue;
+    const uint32_t kv = sh.u.e.key[j];
+    ngt += kv > T;
+    neq += kv == T;
+  }
+  block_prefix2(sh, ngt, neq);
+  int o = ngt + min(neq, need_eq);
+  int eq_run = neq;
+  for (int j = j0; j < j1; ++j) {
+    if (drop(j)) continue;
+    const uint32_t kv = sh.u.e.key[j];
+    bool sel = kv > T;
+    if (kv == T) sel = eq_run++ < need_eq;
+    if (sel) {
+      if (o < cnt) {
+        out[o] = sh.u.e.pos[j];
+        if (dcopy) dcopy[o] = sh.u.e.pos[j];
       }
-      // slice-local bitmap word of positions g0 .. g0 + 31 (g0 - a0 is 32-aligned)
-      if (setbits && lane == 0 && g0 < w1) setbits[(g0 - ck.a0) >> 5] |= selb;
-      pos += __popc(selb);
-      eq_run += __popc(eqb);
+      ++o;
     }
   }
   __syncthreads();
 }
 
-template <int CS>
-__global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_constant__ SelectArgs A) {
+// Gathers channel c's lists of the scan CTAs of sequence b into sh.u.e, in
+// CTA order; returns the entry count, or -1 if a list overflowed or the total
+// does not fit.  The counts are read one per lane and every entry load is in
+// flight at once.
+__device__ int gather(SelShared& sh, const SelectArgs& A, int b, int c) {
+  constexpr int kPer = kFinCap / kThreads;   // entries per thread at most
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    const int n = tid < A.cs ? __ldcg(A.list_counts + (size_t(b) * 2 + c) * A.cs + tid) : 0;
+    const bool bad = __any_sync(0xffffffffu, n < 0);
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (tid >= o) incl += y;
+    }
+    if (tid <= A.cs) sh.goff[tid] = incl - n;   // goff[cs] = total
+    if (tid == 31) sh.tot = (bad || incl > kFinCap) ? -1 : incl;
+  }
+  __syncthreads();
+  const int total = sh.tot;
+  if (total < 0) return -1;
+  const uint2* base = A.lists + (size_t(b) * 2 + c) * A.cs * A.list_cap;
+  uint2 e[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int j = tid + u * kThreads;
+    e[u] = make_uint2(0u, 0u);
+    if (j < total) {
+      int r = 0;
+      while (r + 1 < A.cs && sh.goff[r + 1] <= j) ++r;
+      e[u] = __ldcg(base + size_t(r) * A.list_cap + (j - sh.goff[r]));
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int j = tid + u * kThreads;
+    if (j < total) {
+      sh.u.e.key[j] = e[u].x;
+      sh.u.e.pos[j] = int(e[u].y);
+    }
+  }
+  __syncthreads();
+  return total;
+}
+
+// ------------------------------------------------------------------ kernels
+
+__global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_constant__ SelectArgs A) {
   extern __shared__ __align__(16) unsigned char dsm[];
-  SelShared<CS>& sh = *reinterpret_cast<SelShared<CS>*>(dsm);
-  unsigned char* rest = dsm + ((sizeof(SelShared<CS>) + 15) & ~size_t(15));
+  SelShared& sh = *reinterpret_cast<SelShared*>(dsm);
   pdl_launch_dependents();
   pdl_wait();
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = int(cluster.block_rank());
-  const int b = blockIdx.x / CS;
-  const int tid = threadIdx.x;
+  const int CS = A.cs;
+  const int b = blockIdx.x / CS, r = blockIdx.x - (blockIdx.x / CS) * CS;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t lt = (1u << lane) - 1u;
   int32_t* out = A.out + size_t(b) * A.k;
   const int L = A.seq_len[b];
-  // the early cases below are decided per sequence, so every CTA of the
-  // cluster leaves together, before any cluster barrier
+  // the early cases depend on the sequence only: all its CTAs leave together
   if (L < 0 || L > A.Lcap) {
-    if (tid == 0 && rank == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
-    for (int j = rank * kThreads + tid; j < A.k; j += CS * kThreads) out[j] = -1;
+    if (r == 0) {
+      if (tid == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
+      for (int j = tid; j < A.k; j += kThreads) out[j] = -1;
+    }
     return;
   }
   if (A.k >= L) {
-    for (int j = rank * kThreads + tid; j < A.k; j += CS * kThreads) out[j] = j < L ? j : -1;
+    if (r == 0)
+      for (int j = tid; j < A.k; j += kThreads) out[j] = j < L ? j : -1;
     return;
   }
   const int s_eff = min(A.sinks, L);
@@ -520,145 +518,243 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   const int nP = s_eff + (L - w0);
   const int m1 = min(A.m, A.k - nP);
   const int f = A.k - nP - m1;
-  if (rank == 0)
+  if (r == 0)
     for (int j = tid; j < nP; j += kThreads) out[j] = j < s_eff ? j : w0 + (j - s_eff);
 
-  // this CTA's slice of the unprotected positions [s_eff, w0)
-  const int per = (((w0 - s_eff) + CS - 1) / CS + 31) & ~31;
-  const int s0 = min(w0, s_eff + rank * per);
-  const int s1 = min(w0, s0 + per);
-  const int nwords = (per + 63) / 32;   // bits of positions from (s0 & ~31)
-  uint32_t* keys0 = A.cache_keys ? reinterpret_cast<uint32_t*>(rest) : nullptr;
-  uint32_t* keys1 = A.cache_keys ? keys0 + A.slice_cap : nullptr;
-  uint32_t* bitmap =
-      reinterpret_cast<uint32_t*>(rest + (A.cache_keys ? size_t(2) * A.slice_cap * 4 : 0));
-  for (int w = tid; w < nwords; w += kThreads) bitmap[w] = 0u;
-  for (int j = tid; j < 2 * kBins1; j += kThreads) (&sh.h1[0][0])[j] = 0;
-  int hbuf = 0;
+  // ---- scan: thresholds from the histograms
+  const int* gh = A.hist + size_t(b) * 2 * kBins1;
+  for (int j = tid; j < 2 * kBins1; j += kThreads) (&sh.h[0][0])[j] = __ldcg(gh + j);
+  if (tid == 0) sh.overflow = 0;
   __syncthreads();
+  uint32_t b0 = 0xFFFFFFFFu, b1 = 0xFFFFFFFFu;   // no key reaches these bins
+  int need0 = 0;
+  if (m1 > 0) {
+    find_bin(sh, sh.h[0], kBins1, m1);
+    if (sh.found) {
+      b0 = uint32_t(sh.bin);
+      need0 = sh.need;
+    } else if (tid == 0) {
+      sh.overflow = 1;
+    }
+  }
+  if (f > 0) {
+    find_bin(sh, sh.h[1], kBins1, m1 + f);
+    if (sh.found) b1 = uint32_t(sh.bin);
+    else if (tid == 0) sh.overflow = 1;
+  }
 
-  // stage both channels' keys (when they fit) and build their level-1 histograms
+  // ---- scan: this CTA's run of U, whole 128-position rows per warp
+  const int a0 = s_eff & ~127;
+  const int span = ((((w0 - a0) + CS - 1) / CS) + 127) & ~127;
+  const int c0 = a0 + r * span, c1 = min(c0 + span, w0);
+  const int wspan = c1 > c0 ? ((((c1 - c0) + kWarps - 1) / kWarps) + 127) & ~127 : 128;
+  const int x0 = c0 + warp * wspan, x1 = min(x0 + wspan, c1);
   const float* row0 = A.imp + (size_t(b) * 2 + 0) * A.Lcap;
   const float* row1 = A.imp + (size_t(b) * 2 + 1) * A.Lcap;
-  for (int base = s0; base < s1; base += kThreads * kBatch) {
-    float v0[kBatch], v1[kBatch];
+  int n0 = 0, n1 = 0;   // list entries of this warp (warp-uniform)
+  bool bad = false;
+  for (int gb = x0; gb < x1; gb += 128) {
+    const int i0 = gb + 4 * lane;
+    float v[2][4];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * kThreads + tid;
-      v0[u] = i < s1 ? row0[i] : 0.f;
-      v1[u] = i < s1 ? row1[i] : 0.f;
-    }
+    for (int c = 0; c < 2; ++c) {
+      const float* row = c ? row1 : row0;
+      if (A.vec4) {
+        const float4 x = i0 < x1 ? __ldg(reinterpret_cast<const float4*>(row + i0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[c][0] = x.x;
+        v[c][1] = x.y;
+        v[c][2] = x.z;
+        v[c][3] = x.w;
+      } else {
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * kThreads + tid;
-      if (i < s1) {
-        const uint32_t k0 = key_of(v0[u], A.err), k1 = key_of(v1[u], A.err);
-        if (keys0) {
-          keys0[i - s0] = k0;
-          keys1[i - s0] = k1;
-        }
-        atomicAdd(&sh.h1[0][k0 >> 20], 1);
-        atomicAdd(&sh.h1[1][k1 >> 20], 1);
+        for (int e = 0; e < 4; ++e) v[c][e] = i0 + e < x1 ? __ldg(row + i0 + e) : 0.f;
       }
     }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint32_t thr = c ? b1 : b0;
+      uint32_t kv[4], m[4];
+      int before = 0, total = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = i0 + e;
+        const bool ok = i >= s_eff && i < x1;
+        const uint32_t bits = __float_as_uint(v[c][e]);
+        bad |= ok && bits > 0x7F800000u && bits != 0x80000000u;
+        kv[e] = (ok && bits <= 0x7F800000u) ? bits : 0u;   // importance_key; flag raised once below
+        m[e] = __ballot_sync(0xffffffffu, ok && select_bin(kv[e]) >= thr);
+        before += __popc(m[e] & lt);
+        total += __popc(m[e]);
+      }
+      if (total == 0) continue;   // warp-uniform: nothing of this row is listed
+      int& n = c ? n1 : n0;
+      int slot = n + before;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if ((m[e] >> lane) & 1u) {
+          if (slot < kListCap) {
+            sh.u.l.key[c][warp][slot] = kv[e];
+            sh.u.l.pos[c][warp][slot] = i0 + e;
+          }
+          ++slot;
+        }
+      }
+      n += total;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(A.err, DUSTIN_DEV_NAN);
+  if (lane == 0) {
+    sh.lcnt[0][warp] = n0;
+    sh.lcnt[1][warp] = n1;
+    if (n0 > kListCap || n1 > kListCap) atomicOr(&sh.overflow, 1);
   }
   __syncthreads();
-  const KeySrc src0{keys0, row0, s0, A.err}, src1{keys1, row1, s0, A.err};
-  tier_select(cluster, src0, s0, s1, Excl{nullptr, 0}, m1, &sh.h1[0][0], out + nP, bitmap, &src1,
-              sh, hbuf);
-  tier_select(cluster, src1, s0, s1, Excl{bitmap, s0 & ~31}, f, &sh.h1[1][0], out + nP + m1,
-              nullptr, static_cast<const KeySrc*>(nullptr), sh, hbuf);
-  cluster.sync();   // no CTA leaves while another may still read its shared memory
-}
-
-template <int CS>
-size_t smem_bytes(int slice_cap, int cache_keys) {
-  return ((sizeof(SelShared<CS>) + 15) & ~size_t(15)) + (cache_keys ? size_t(2) * slice_cap * 4 : 0) +
-         size_t(slice_cap + 64) / 32 * 4;
-}
-
-int slice_cap_of(int Lcap, int cs) { return int(size_t((Lcap + cs - 1) / cs + 31) & ~size_t(31)); }
-
-// Shared-memory bytes of one CTA for cluster size CS; sets cache_keys and slice_cap.
-template <int CS>
-size_t plan_smem(SelectArgs& a) {
-  a.slice_cap = slice_cap_of(a.Lcap, CS);
-  a.cache_keys = smem_bytes<CS>(a.slice_cap, 1) <= kSmemBudget ? 1 : 0;
-  return smem_bytes<CS>(a.slice_cap, a.cache_keys);
-}
-
-template <int CS>
-cudaError_t launch_cs(const SelectArgs& a0, cudaStream_t stream, bool query_only, int* max_clusters) {
-  SelectArgs a = a0;
-  const size_t smem = plan_smem<CS>(a);
-  auto kern = select_kernel<CS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(a.B * CS);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute at[2];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = CS;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 2;
-  if (query_only) {
-    cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(max_clusters, kern, &cfg);
+  // ---- scan: this CTA's lists to the workspace, in warp order
+  for (int c = 0; c < 2; ++c) {
+    if (tid < 32) {
+      const int n = min(sh.lcnt[c][tid], kListCap);
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += y;
+      }
+      sh.wsum[tid] = incl - n;
+      if (tid == 31) sh.tot = incl;
+    }
+    __syncthreads();
+    const int total = sh.tot;
+    const bool ok = !sh.overflow && total <= A.list_cap;
+    uint2* dst = A.lists + ((size_t(b) * 2 + c) * CS + r) * A.list_cap;
+    const int n = min(sh.lcnt[c][warp], kListCap);
+    if (ok)
+      for (int j = lane; j < n; j += 32)
+        dst[sh.wsum[warp] + j] = make_uint2(sh.u.l.key[c][warp][j], uint32_t(sh.u.l.pos[c][warp][j]));
+    if (tid == 0) A.list_counts[(size_t(b) * 2 + c) * CS + r] = ok ? total : -1;
+    __syncthreads();
   }
-  return cudaLaunchKernelEx(&cfg, kern, a);
-}
+  // ---- the last CTA of the sequence to get here finishes it
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = CS > 1 ? atomicAdd(A.counters + b, 1) : 0;
+    sh.last = prev == CS - 1;
+    if (sh.last && CS > 1) A.counters[b] = 0;   // ready for the next call
+  }
+  __syncthreads();
+  if (!sh.last) return;
+  __threadfence();
 
-cudaError_t launch_any(int cs, const SelectArgs& a, cudaStream_t stream, bool query_only, int* n) {
-  switch (cs) {
-    case 1: return launch_cs<1>(a, stream, query_only, n);
-    case 2: return launch_cs<2>(a, stream, query_only, n);
-    case 4: return launch_cs<4>(a, stream, query_only, n);
-    case 8: return launch_cs<8>(a, stream, query_only, n);
-    default: return cudaErrorInvalidValue;
+  // ---- finish
+  bool general = m1 > kDCap;
+  if (!general && m1 > 0) {
+    const int ne0 = gather(sh, A, b, 0);
+    general = ne0 < 0;
+    if (!general)
+      finish_tier(sh, ne0, b0, need0, m1, out + nP, f > 0 ? sh.dpos : nullptr, nullptr);
+  }
+  int ne1 = 0;
+  if (!general && f > 0) {
+    ne1 = gather(sh, A, b, 1);
+    general = ne1 < 0;
+  }
+  if (general) {
+    select_general(sh, A, b, s_eff, w0, nP, m1, f, out);
+    return;
+  }
+  if (f > 0) {
+    // the target histogram of U minus the draft tier, and its threshold bin
+    for (int j = tid; j < m1; j += kThreads)
+      atomicSub(&sh.h[1][select_bin(importance_key(__ldg(row1 + sh.dpos[j]), A.err))], 1);
+    __syncthreads();
+    find_bin(sh, sh.h[1], kBins1, f);
+    if (!sh.found) {   // cannot happen with matching keys
+      if (tid == 0) flag_error(A.err, DUSTIN_DEV_NAN);
+      return;
+    }
+    const uint32_t bt = uint32_t(sh.bin);
+    const int needt = sh.need;
+    // mark the list entries that the draft tier took (both lists ascending:
+    // one binary search per entry)
+    for (int j = tid; j < (ne1 + 31) / 32; j += kThreads) sh.drop[j] = 0u;
+    __syncthreads();
+    for (int j = tid; j < ne1; j += kThreads) {
+      const int p = sh.u.e.pos[j];
+      int lo = 0, hi = m1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sh.dpos[mid] < p) lo = mid + 1;
+        else hi = mid;
+      }
+      if (lo < m1 && sh.dpos[lo] == p) atomicOr(&sh.drop[j >> 5], 1u << (j & 31));
+    }
+    __syncthreads();
+    finish_tier(sh, ne1, bt, needt, f, out + nP + m1, nullptr, m1 > 0 ? sh.drop : nullptr);
   }
 }
 
-// How many clusters of cs CTAs can run at once for this Lcap on the current
-// device (cached per device, cluster size and Lcap).
-int max_active_clusters(int cs, const SelectArgs& a) {
-  struct Entry {
-    int dev, cs, Lcap, n;
-  };
-  static std::mutex mu;
-  static std::vector<Entry> cache;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  std::lock_guard<std::mutex> lock(mu);
-  for (const Entry& e : cache)
-    if (e.dev == dev && e.cs == cs && e.Lcap == a.Lcap) return e.n;
-  int n = 0;
-  if (launch_any(cs, a, nullptr, true, &n) != cudaSuccess) {
-    cudaGetLastError();
-    n = 0;
+// Standalone selection: the level-1 histograms of both channels over each
+// sequence's unprotected positions (the fused step builds them while scoring).
+__global__ void __launch_bounds__(kHistThreads) select_hist_kernel(const __grid_constant__ SelectArgs A) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int b = blockIdx.y;
+  const int i = blockIdx.x * kHistThreads + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  int L = A.seq_len[b];
+  if (L < 0 || L > A.Lcap) L = 0;
+  const int s_eff = min(A.sinks, L);
+  const int w0 = max(L - A.window, s_eff);
+  const bool in_u = i >= s_eff && i < w0;
+  int* h = A.hist + size_t(b) * 2 * kBins1;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint32_t kv = in_u ? importance_key(A.imp[(size_t(b) * 2 + c) * A.Lcap + i], A.err) : 0u;
+    hist_add(h + c * kBins1, select_bin(kv), in_u, lane);
   }
-  cache.push_back({dev, cs, a.Lcap, n});
-  return n;
 }
 
 }  // namespace
 
-int select_cluster_size(const SelectArgs& a) {
-  // the largest cluster whose B clusters are all resident at once; one CTA
-  // per sequence when even pairs do not fit
-  for (int cs = 8; cs >= 2; cs /= 2)
-    if (a.B <= max_active_clusters(cs, a)) return cs;
-  return 1;
+int select_ctas_per_sequence(int B) {
+  // spread the scan over about 128 CTAs; the counters in the reserved
+  // workspace area bound the batches that use more than one per sequence
+  int cs = 128 / (B > 0 ? B : 1);
+  if (cs > kMaxSelectCtas) cs = kMaxSelectCtas;
+  if (cs < 1 || B > kSelectCountersMax) cs = 1;
+  return cs;
 }
 
-cudaError_t select_launch(const SelectArgs& a, cudaStream_t stream) {
-  return launch_any(select_cluster_size(a), a, stream, false, nullptr);
+SelectPlan select_plan(int B, int Lcap, size_t off) {
+  SelectPlan s{};
+  s.cs = select_ctas_per_sequence(B);
+  const int span = ((((Lcap + 128) + s.cs - 1) / s.cs) + 127) & ~127;
+  s.list_cap = span < kFinCap ? span : kFinCap;
+  s.bits_words = (Lcap + 127) / 32 + 2;
+  auto r256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+  s.hist_off = off;
+  s.lists_off = s.hist_off + r256(size_t(B) * 2 * kBins1 * 4);
+  s.counts_off = s.lists_off + r256(size_t(B) * 2 * s.cs * s.list_cap * 8);
+  s.bits_off = s.counts_off + r256(size_t(B) * 2 * s.cs * 4);
+  s.end = s.bits_off + r256(size_t(B) * s.bits_words * 4);
+  return s;
+}
+
+cudaError_t select_launch(const SelectArgs& a0, bool build_hist, cudaStream_t stream) {
+  SelectArgs a = a0;
+  a.vec4 = (a.Lcap % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.imp) & 15u) == 0);
+  cudaError_t e;
+  if (build_hist) {
+    if ((e = cudaMemsetAsync(a.hist, 0, size_t(a.B) * 2 * kBins1 * 4, stream)) != cudaSuccess) return e;
+    e = launch_pdl(select_hist_kernel, dim3((a.Lcap + kHistThreads - 1) / kHistThreads, a.B),
+                   dim3(kHistThreads), 0, stream, a);
+    if (e != cudaSuccess) return e;
+  }
+  const size_t smem = sizeof(SelShared);
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (attr != cudaSuccess) return attr;
+  return launch_pdl(select_kernel, dim3(a.B * a.cs), dim3(kThreads), smem, stream, a);
 }
 
 }  // namespace dustin

@@ -563,6 +563,9 @@ constexpr int kCombineThreads = 128;
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) verify_combine_kernel(const __grid_constant__ VerifyCombineArgs C) {
   pdl_launch_dependents();
+  // every CTA waits for the stream-K kernel before it leaves, so that this
+  // kernel completes only after it (the next launch waits on this one)
+  pdl_wait();
   const int u = blockIdx.y;
   const int seg_first = cta_of((long long)u * C.tiles_u, C.total, C.main_grid);
   const int seg_last = cta_of((long long)u * C.tiles_u + C.tiles_u - 1, C.total, C.main_grid);
@@ -570,7 +573,6 @@ __global__ void __launch_bounds__(kCombineThreads) verify_combine_kernel(const _
   if (n_seg == 1) return;
   const int q = blockIdx.x * kCombineThreads + threadIdx.x;
   if (q >= C.NQ * (D / 4)) return;
-  pdl_wait();
   const int r = q / (D / 4), c4 = q - r * (D / 4);
   const size_t slot = size_t(C.slot_floats);
   const float* base0 = C.partial + size_t(u) * C.max_seg * slot;
