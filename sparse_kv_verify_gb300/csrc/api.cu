@@ -457,6 +457,7 @@ int run_verify(const dustin_params* p, int32_t hq, int hkv, int D, int n_layers,
   a.max_seg = pl.max_seg;
   a.slot_floats = pl.slot_floats;
   a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(D)));
+  a.lay = pl.lay;
   a.ivf = ivf;
   a.seq_len = seq_len;
   a.err = err_word(ws);

@@ -40,6 +40,14 @@ struct VerifyLayerDev {
   int64_t ksb, ksh, ksl, vsb, vsh, vsl;
 };
 
+// Shared-memory layout of the verification kernel (bytes from its 1024-byte
+// aligned base), chosen on the host per launch.
+struct VLay {
+  int NP, nst;           // 64-column panels per row; K/V stages
+  uint32_t q_panel, q_buf, ring_off, kv_panel, half_bytes, stage_bytes;
+  uint32_t mask_off, bar_off, misc_off, total;
+};
+
 struct VerifyArgs {
   int B, Lcap, T, hq, hkv, G, NQ;
   int k;                // budget (sparse); unused for dense
@@ -51,6 +59,7 @@ struct VerifyArgs {
   int max_seg;          // partial slots per unit
   long long slot_floats;  // floats per partial slot (multiple of 4)
   float scale_log2;     // log2(e) / sqrt(D)
+  VLay lay;
   const int32_t* ivf;   // [B][k] (sparse)
   const int32_t* seq_len;
   int* err;
@@ -71,6 +80,7 @@ struct VerifyCombineArgs {
 
 struct VerifyLaunch {
   int D, NST;
+  VLay lay;
   int ctx_tiles, tiles_u, grid, max_seg;
   long long units, total, slot_floats;
   size_t smem;

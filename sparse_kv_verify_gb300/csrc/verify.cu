@@ -49,7 +49,8 @@ namespace {
 
 constexpr int TK = 64;           // keys per tile (and the largest draft block)
 constexpr int kSoftmaxWarps = 4;    // one thread per tensor-memory lane
-constexpr int kLoaders = 4;         // loader warps, 16 keys of every tile each
+constexpr int kLoaders = 8;         // loader warps, kKpw keys of every tile each
+constexpr int kKpw = TK / kLoaders;  // keys per loader warp and tile
 constexpr int kLoaderWarp0 = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + kLoaders;
 constexpr int NTH = 32 * (kMmaWarp + 1);
 constexpr int kSCol = 0;         // S buffers: columns [0, 64) and [64, 128)
@@ -175,27 +176,44 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
 }
 
 
+// Shared-memory layout (bytes from the 1024-aligned base), fixed per launch
+// by the head dimension D and the query rows NQ:
+//   two query buffers [NP panels][q_rows rows][128 B] (q_rows = NQ rounded up
+//   to 8; the next segment's rows load while this one runs), then as many
+//   K/V stages [K panels | V panels] of 64 keys as the rest holds, then the
+//   valid-key masks, the mbarriers and two words (tensor-memory base, abort).
+// The S MMA reads 128 query rows per panel; the rows past q_rows fall on the
+// next buffer or the ring (whatever they hold only reaches S and O rows that
+// are never used: the softmax treats rows >= NQ as empty).
+constexpr int NQB = 2;
+constexpr uint32_t kVerifySmem = 227 * 1024;
+
+// K/V stages per head dimension (compile-time: the stage and phase of tile
+// gi are gi % n and gi / n on the hot paths).  More than five 32 KB stages
+// measured no faster at d = 128 (the MMA issue rate bounds a tile, not the
+// bytes in flight) and slower for contiguous rows.
 template <int D>
-struct Lay {
-  static constexpr int NP = D / 64;                    // 64-column panels per row
-  static constexpr size_t q_panel = 128 * 128;         // [128 rows][64 columns]
-  static constexpr size_t q_buf = NP * q_panel;
-  // two query buffers (the next segment's rows load while this one runs) and
-  // as many K/V stages as the rest of the shared memory holds
-  static constexpr int NQB = 2;
-  static constexpr int NST = D == 128 ? 5 : 8;
-  static constexpr size_t q_off = 0;
-  static constexpr size_t ring_off = q_off + NQB * q_buf;
-  static constexpr size_t kv_panel = size_t(TK) * 128;    // [64 keys][64 columns]
-  static constexpr size_t half_bytes = NP * kv_panel;     // K (or V) of one tile
-  static constexpr size_t stage_bytes = 2 * half_bytes;
-  static constexpr size_t mask_off = ring_off + NST * stage_bytes;   // [NST][4] words
-  static constexpr size_t bar_off = mask_off + NST * 16;
-  // full[NST], empty[NST], s_full[2], p_full[2], q_full[NQB], q_empty[NQB]
-  static constexpr int n_bars = 2 * NST + 4 + 2 * NQB;
-  static constexpr size_t misc_off = bar_off + n_bars * 8;   // tmem base, abort
-  static constexpr size_t total = misc_off + 16 + 1024;      // + slack for the 1024-byte base
+struct StagesOf {
+  static constexpr int n = D == 128 ? 5 : 8;
 };
+
+inline VLay make_lay(int D, int NQ) {
+  VLay L{};
+  L.NP = D / 64;
+  const int q_rows = NQ < 8 ? 8 : (NQ + 7) & ~7;
+  L.q_panel = uint32_t(q_rows) * 128;
+  L.q_buf = uint32_t(L.NP) * L.q_panel;
+  L.ring_off = (NQB * L.q_buf + 1023u) & ~1023u;
+  L.kv_panel = uint32_t(TK) * 128;
+  L.half_bytes = uint32_t(L.NP) * L.kv_panel;
+  L.stage_bytes = 2 * L.half_bytes;
+  L.nst = D == 128 ? StagesOf<128>::n : StagesOf<64>::n;
+  L.mask_off = L.ring_off + uint32_t(L.nst) * L.stage_bytes;
+  L.bar_off = L.mask_off + ((uint32_t(L.nst) * kLoaders + 7u) & ~7u);
+  L.misc_off = L.bar_off + uint32_t(2 * L.nst + 4 + 2 * NQB) * 8;
+  L.total = L.misc_off + 16 + 1024;
+  return L;
+}
 
 // CTA that owns flattened tile x, for start(c) = c * total / G.
 __device__ __forceinline__ int cta_of(long long x, long long total, int G) {
@@ -219,21 +237,21 @@ __device__ __forceinline__ Seg next_seg(long long& t, long long t1, int tiles_u)
 
 template <int D>
 __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ VerifyArgs A) {
-  using Ly = Lay<D>;
   using Tm = TmemCfg<D>;
-  constexpr int NSTAGE = Ly::NST, NQB = Ly::NQB;
+  const VLay& Ly = A.lay;
+  constexpr int NSTAGE = StagesOf<D>::n;   // == A.lay.nst
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  uint32_t* masks = reinterpret_cast<uint32_t*>(smem + Ly::mask_off);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Ly::bar_off);
+  uint8_t* masks = smem + Ly.mask_off;   // [NSTAGE][kLoaders]: valid-key bits, kKpw per byte
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Ly.bar_off);
   uint64_t* empty = full + NSTAGE;
   uint64_t* s_full = empty + NSTAGE;
   uint64_t* p_full = s_full + 2;
   uint64_t* q_full = p_full + 2;
   uint64_t* q_empty = q_full + NQB;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::misc_off);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::misc_off + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly.misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly.misc_off + 8);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -254,16 +272,6 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     }
     *abort_flag = 0;
     fence_barrier_init();
-  }
-  if (warp < kSoftmaxWarps) {
-    // query rows past NQ stay zero in both query buffers (the loads write rows
-    // < NQ only), so their scores are exactly zero
-    for (int q = NQ * 8 + tid; q < 128 * 8; q += kSoftmaxWarps * 32)
-#pragma unroll
-      for (int x = 0; x < NQB * Ly::NP; ++x)
-        *reinterpret_cast<uint4*>(smem + Ly::q_off + x * Ly::q_panel + size_t(q) * 16) =
-            make_uint4(0, 0, 0, 0);
-    fence_proxy_async();
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -298,10 +306,10 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     const int lw = warp - kLoaderWarp0;
     constexpr int CH = D / 8;             // 16-byte chunks per row
     constexpr int KPI = 32 / CH;          // rows per warp instruction
-    constexpr int NI = 16 / KPI;          // instructions per tensor
+    constexpr int NI = kKpw / KPI;        // instructions per tensor
     const int c = lane % CH;
     const int ksub = lane / CH;
-    long long gi = 0;
+    int gi = 0;
     int s = 0;
     for (long long t = t0; t < t1; ++s) {
       const Seg sg = next_seg(t, t1, tiles_u);
@@ -322,15 +330,15 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
         if (s >= NQB) mbar_wait(&q_empty[qb], uint32_t(s / NQB - 1) & 1u, A.err, abort_flag);
         mbar_arrive_expect_tx(&q_full[qb], uint32_t(NQ) * D * 2);
 #pragma unroll
-        for (int h = 0; h < Ly::NP; ++h)
-          tma_load_3d(sbase + uint32_t(Ly::q_off + qb * Ly::q_buf + h * Ly::q_panel), &A.qmap[layer], h * 64,
+        for (int h = 0; h < Ly.NP; ++h)
+          tma_load_3d(sbase + uint32_t(qb * Ly.q_buf + h * Ly.q_panel), &A.qmap[layer], h * 64,
                       g * GQ, b * T, &q_full[qb]);
       }
       __syncwarp();
       const uint16_t* kbase = Lr.k + size_t(b) * Lr.ksb + size_t(g) * Lr.ksh;
       const uint16_t* vbase = Lr.v + size_t(b) * Lr.vsb + size_t(g) * Lr.vsh;
       const size_t blk_off = (size_t(b) * A.hkv + g) * T * D;
-      const int kk = 16 * lw + (lane & 15);   // key whose index this lane reads
+      const int kk = kKpw * lw + (lane % kKpw);   // key whose index this lane reads
       for (int i = 0; i < sg.n; ++i, ++gi) {
         const int tt = sg.ta + i;
         const bool blk = tt >= ctx_tiles;
@@ -349,10 +357,10 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
         else if (A.dense) valid = raw < L;
         else {
           valid = raw >= 0 && raw < L;
-          if (lane < 16 && (raw < -1 || raw >= L)) flag_error(A.err, DUSTIN_DEV_INDEX);
+          if (lane < kKpw && (raw < -1 || raw >= L)) flag_error(A.err, DUSTIN_DEV_INDEX);
         }
-        const uint32_t vbits = __ballot_sync(0xffffffffu, valid) & 0xFFFFu;
-        const uint32_t stage = sbase + uint32_t(Ly::ring_off + size_t(st) * Ly::stage_bytes);
+        const uint32_t vbits = __ballot_sync(0xffffffffu, valid) & ((1u << kKpw) - 1u);
+        const uint32_t stage = sbase + uint32_t(Ly.ring_off + size_t(st) * Ly.stage_bytes);
 #pragma unroll
         for (int m = 0; m < 2 * NI; ++m) {
           const int which = m / NI;
@@ -364,11 +372,11 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
           if (blk) src = (which ? Lr.vb : Lr.kb) + blk_off + size_t(rr) * D + c * 8;
           else if (which) src = vbase + size_t(rr) * Lr.vsl + c * 8;
           else src = kbase + size_t(rr) * Lr.ksl + c * 8;
-          const int key = 16 * lw + kl;
-          cp_async16(stage + uint32_t(which * Ly::half_bytes + (c >> 3) * Ly::kv_panel) + swz(key, c & 7),
+          const int key = kKpw * lw + kl;
+          cp_async16(stage + uint32_t(which * Ly.half_bytes + (c >> 3) * Ly.kv_panel) + swz(key, c & 7),
                      src, ok ? 16u : 0u);
         }
-        if (lane == 0) masks[st * 4 + lw] = vbits;
+        if (lane == 0) masks[st * kLoaders + lw] = uint8_t(vbits);
         cp_async_arrive_noinc(&full[st]);
         if (lane == 0) mbar_arrive(&full[st]);
       }
@@ -385,20 +393,20 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       constexpr uint32_t kIdS = tc_idesc(128, TK, 0);
       constexpr uint32_t kIdPV = tc_idesc(128, D, 1);
       const uint32_t o_tmem = tmem + Tm::o_col;
-      long long gi = 0;
+      int gi = 0;
       int s = 0;
       // S = Q K^T of tile g2 into S buffer g2 % 2, once its rows have landed
-      auto issue_s = [&](long long g2, uint32_t qbuf) {
+      auto issue_s = [&](int g2, uint32_t qbuf) {
         const int st = int(g2 % NSTAGE);
         mbar_wait(&full[st], uint32_t(g2 / NSTAGE) & 1u, A.err, abort_flag);
         fence_proxy_async();   // the rows were written by cp.async (generic proxy)
         tc_fence_after();
-        const uint32_t kst = sbase + uint32_t(Ly::ring_off + size_t(st) * Ly::stage_bytes);
+        const uint32_t kst = sbase + uint32_t(Ly.ring_off + size_t(st) * Ly.stage_bytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = uint32_t((kk & 3) * 32);
-          const uint64_t a = tc_desc(qbuf + uint32_t((kk >> 2) * Ly::q_panel) + koff, 16, 1024);
-          const uint64_t bd = tc_desc(kst + uint32_t((kk >> 2) * Ly::kv_panel) + koff, 16, 1024);
+          const uint64_t a = tc_desc(qbuf + uint32_t((kk >> 2) * Ly.q_panel) + koff, 16, 1024);
+          const uint64_t bd = tc_desc(kst + uint32_t((kk >> 2) * Ly.kv_panel) + koff, 16, 1024);
           tc_mma_ss(tmem + uint32_t(kSCol + (g2 & 1) * TK), a, bd, kIdS, kk > 0);
         }
         tc_commit(&s_full[g2 & 1]);
@@ -406,7 +414,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       for (long long t = t0; t < t1; ++s) {
         const Seg sg = next_seg(t, t1, tiles_u);
         const int qb = s % NQB;
-        const uint32_t qbuf = sbase + uint32_t(Ly::q_off + qb * Ly::q_buf);
+        const uint32_t qbuf = sbase + uint32_t(qb * Ly.q_buf);
         mbar_wait(&q_full[qb], uint32_t(s / NQB) & 1u, A.err, abort_flag);
         issue_s(gi, qbuf);
         for (int i = 0; i < sg.n; ++i, ++gi) {
@@ -415,11 +423,11 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
           tc_fence_after();
           const int st = int(gi % NSTAGE);
           const uint32_t vst =
-              sbase + uint32_t(Ly::ring_off + size_t(st) * Ly::stage_bytes + Ly::half_bytes);
+              sbase + uint32_t(Ly.ring_off + size_t(st) * Ly.stage_bytes + Ly.half_bytes);
           const uint32_t p_tmem = tmem + uint32_t(kPCol + (gi & 1) * (TK / 2));
 #pragma unroll
           for (int kk = 0; kk < TK / 16; ++kk) {
-            const uint64_t bd = tc_desc(vst + uint32_t(kk * 2048), uint32_t(Ly::kv_panel), 1024);
+            const uint64_t bd = tc_desc(vst + uint32_t(kk * 2048), uint32_t(Ly.kv_panel), 1024);
             tc_mma_ts(o_tmem, p_tmem + uint32_t(kk * 8), bd, kIdPV, (i > 0 || kk > 0) ? 1 : 0);
           }
           tc_commit(&empty[st]);   // P V of tile gi done: its stage is free
@@ -438,7 +446,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     const float scale = A.scale_log2;
     const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
     const uint32_t o_lane = lane_base + uint32_t(Tm::o_col);
-    long long gi = 0;
+    int gi = 0;
     for (long long t = t0; t < t1;) {
       const Seg sg = next_seg(t, t1, tiles_u);
       const int u = sg.u, n = sg.n;
@@ -450,20 +458,18 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       for (int i = 0; i < n; ++i, ++gi) {
         const int st = int(gi % NSTAGE);
         mbar_wait(&full[st], uint32_t(gi / NSTAGE) & 1u, A.err, abort_flag);
-        const uint32_t mw0 = masks[st * 4], mw1 = masks[st * 4 + 1], mw2 = masks[st * 4 + 2],
-                       mw3 = masks[st * 4 + 3];
+        const unsigned long long mw = *reinterpret_cast<const unsigned long long*>(masks + st * kLoaders);
         const bool blk = sg.ta + i >= ctx_tiles;
         mbar_wait(&s_full[gi & 1], uint32_t(gi >> 1) & 1u, A.err, abort_flag);
         tc_fence_after();
         float s[TK];
         tc_ld32(lane_base + uint32_t(kSCol + (gi & 1) * TK), reinterpret_cast<uint32_t*>(s));
         tc_ld32(lane_base + uint32_t(kSCol + (gi & 1) * TK + 32), reinterpret_cast<uint32_t*>(s + 32));
-        if (blk || (mw0 & mw1 & mw2 & mw3) != 0xFFFFu) {
+        if (blk || mw != ~0ull) {
           // rows the tile does not use (and, in the block tile, u > t) get -inf
 #pragma unroll
           for (int j = 0; j < TK; ++j) {
-            const uint32_t w = j < 16 ? mw0 : j < 32 ? mw1 : j < 48 ? mw2 : mw3;
-            const bool valid = ((w >> (j & 15)) & 1u) != 0 && (!blk || j <= tq_row);
+            const bool valid = ((mw >> j) & 1ull) != 0 && (!blk || j <= tq_row);
             s[j] = valid ? s[j] : -INFINITY;
           }
         }
@@ -473,9 +479,12 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
         for (int x = 0; x < 8; ++x)
           m8[x] = fmaxf(fmaxf(fmaxf(s[x], s[x + 8]), fmaxf(s[x + 16], s[x + 24])),
                         fmaxf(fmaxf(s[x + 32], s[x + 40]), fmaxf(s[x + 48], s[x + 56])));
-        const float mx =
-            fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) *
-            scale;
+        // (a query row past NQ has an S row computed from whatever lies past
+        // the query rows: its max is taken as -inf, so it never rescales O;
+        // its P and O rows are never read)
+        const float mx = active ? fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                        fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * scale
+                                : -INFINITY;
         float alpha = 1.f;
         if (mx > mref + 8.f) {   // also the first tile with a valid key
           alpha = fast_exp2(mref - mx);   // 0 while mref is -inf
@@ -606,11 +615,10 @@ __global__ void __launch_bounds__(kCombineThreads) verify_combine_kernel(const _
 template <int D>
 cudaError_t launch_t(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t stream) {
   auto kern = verify_kernel<D>;
-  const size_t smem = Lay<D>::total;
   static const cudaError_t attr =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kVerifySmem));
   if (attr != cudaSuccess) return attr;
-  cudaError_t e = launch_pdl(kern, dim3(pl.grid), dim3(NTH), smem, stream, a);
+  cudaError_t e = launch_pdl(kern, dim3(pl.grid), dim3(NTH), pl.smem, stream, a);
   if (e != cudaSuccess) return e;
   VerifyCombineArgs c;
   c.NQ = a.NQ;
@@ -637,7 +645,9 @@ VerifyLaunch verify_plan(int D, int NQ, int nkeys_cap, int B, int hkv, int n_lay
   (void)dense;
   VerifyLaunch pl{};
   pl.D = D;
-  pl.NST = D == 128 ? Lay<128>::NST : Lay<64>::NST;
+  const VLay lay = make_lay(D, NQ);
+  pl.lay = lay;
+  pl.NST = lay.nst;
   pl.ctx_tiles = (nkeys_cap + TK - 1) / TK;
   pl.tiles_u = pl.ctx_tiles + 1;
   pl.units = (long long)B * hkv * n_layers;
@@ -652,7 +662,7 @@ VerifyLaunch verify_plan(int D, int NQ, int nkeys_cap, int B, int hkv, int n_lay
   const long long per = pl.total / kVerifyGridMax;
   pl.max_seg = int(pl.tiles_u / (per > 0 ? per : 1)) + 2;
   pl.slot_floats = ((long long)NQ * D + 2LL * NQ + 3) / 4 * 4;   // 16-byte aligned slots
-  pl.smem = D == 128 ? Lay<128>::total : Lay<64>::total;
+  pl.smem = lay.total;
   return pl;
 }
 
