@@ -238,10 +238,9 @@ int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStre
  * call with these arguments launches, and how many sequences each scoring
  * group holds.  Scoring runs over groups of *group_size sequences so that a
  * group's logits stay resident in L2; each group takes two kernels (stream,
- * normalise), select takes one, and verification two (the stream-K kernel
- * and the merge of the units it split).  Returns DUSTIN_EINVAL /
- * DUSTIN_ERANGE for arguments dustin_verify_step would reject while planning
- * the scoring. */
+ * normalise), select takes one, and verification two (the stream-K kernel and
+ * the merge of the units it split).  Returns DUSTIN_EINVAL / DUSTIN_ERANGE for arguments
+ * dustin_verify_step would reject while planning the scoring. */
 int dustin_step_launches(const dustin_step* s, int32_t* n_launches, int32_t* group_size);
 
 /* Bytes of the library-owned scratch array used by dustin_score_noalloc. */

@@ -160,6 +160,13 @@ bool encode_query_map(CUtensorMap* m, const void* q, int d, int hq, int BT, int 
 // in L2 between the stream and the normalise kernels.
 constexpr size_t kScoreL2Budget = size_t(48) << 20;
 
+// Groups per normalise launch.  With two, the second group's stream kernel
+// starts on the SMs the first one's stragglers leave and one normalise covers
+// both; with a static split of each group's tiles the late-starting CTAs end
+// late, which measured slower (214.7 vs 209.3 us per step at B=16, L=32k), so
+// each group is normalised on its own.
+constexpr int kGroupsPerNorm = 1;
+
 struct ScorePlan {
   int n_slab = 0;
   int n_cache = 0;
@@ -172,7 +179,10 @@ struct ScorePlan {
   int max_seg = 0;
   int n_rows = 0, n_rows0 = 0;
   ScoreLaunch launch{};
-  size_t logits_off = 0, logits_bytes = 0, stats_off = 0, stats_bytes = 0, total = 0;
+  // logits and statistics buffers: one per group of a pair (the second group
+  // of a pair streams into its own buffers while the first one's complete)
+  int n_buf = 1;
+  size_t logits_off[2] = {0, 0}, logits_bytes = 0, stats_off[2] = {0, 0}, stats_bytes = 0, total = 0;
   // selection scratch of the fused step, after the score scratch
   SelectPlan sel{};
   size_t hist_off = 0, total_step = 0;
@@ -275,11 +285,14 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
     }
     pl->max_seg = int((long long)tmax * wmax / wmin) + 3;
     pl->nb = int(nb);
+    pl->n_buf = (kGroupsPerNorm > 1 && p->B > nb) ? 2 : 1;
     pl->logits_bytes = round256(per_b * nb);
     pl->stats_bytes = round256(size_t(pl->n_slab) * nb * pl->max_seg * pl->np_max * 2 * 4);
-    pl->logits_off = scratch_off;
-    pl->stats_off = pl->logits_off + pl->logits_bytes;
-    pl->total = pl->stats_off + pl->stats_bytes;
+    pl->logits_off[0] = scratch_off;
+    pl->logits_off[1] = scratch_off + pl->logits_bytes;
+    pl->stats_off[0] = scratch_off + pl->n_buf * pl->logits_bytes;
+    pl->stats_off[1] = pl->stats_off[0] + pl->stats_bytes;
+    pl->total = pl->stats_off[0] + pl->n_buf * pl->stats_bytes;
     if (!scratch_max || pl->total <= scratch_max) break;
     --nb;
   }
@@ -330,8 +343,6 @@ int launch_score(const dustin_params* p, const dustin_signal* draft, const dusti
   a.max_seg = pl.max_seg;
   a.seq_len = seq_len;
   a.err = err_word(ws);
-  a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.logits_off);
-  a.stats = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.stats_off);
   a.importance = importance;
   a.hist = hist;
   a.sinks = p->sinks;
@@ -339,48 +350,77 @@ int launch_score(const dustin_params* p, const dustin_signal* draft, const dusti
   a.n_rows = pl.n_rows;
   a.n_rows0 = pl.n_rows0;
   const int sms = num_sms() > 0 ? num_sms() : 148;
-  for (int b0 = 0; b0 < p->B; b0 += pl.nb) {
-    a.b0 = b0;
-    a.nb = p->B - b0 < pl.nb ? p->B - b0 : pl.nb;
-    long long acc = 0, cost = 0;
-    for (int t = 0; t < pl.n_slab; ++t) {
-      a.slab_start[t] = acc;
-      a.cost_start[t] = cost;
-      acc += (long long)a.nb * pl.slab[t].tiles;
-      cost += (long long)a.nb * pl.slab[t].tiles * pl.slab[t].cost;
-    }
-    a.slab_start[pl.n_slab] = acc;
-    a.cost_start[pl.n_slab] = cost;
-    a.total = acc;
-    a.total_cost = cost;
-    // the slabs in logits-row order: channel 0 first
-    int n_info = 0, row = 0;
-    for (int ch = 0; ch < 2; ++ch)
+  long long wmax = 1;   // every CTA's share must reach the largest tile cost,
+  for (int t = 0; t < pl.n_slab; ++t)   // so that each CTA owns a tile
+    if (pl.slab[t].cost > wmax) wmax = pl.slab[t].cost;
+  const int nchunks = (pl.LSP + 255) / 256;
+  // Groups of nb sequences go kGroupsPerNorm at a time: their stream kernels
+  // (each group but the first of a batch into its own buffers, started
+  // without waiting so that it fills the SMs the previous group's stragglers
+  // leave), then one normalise over them.
+  for (int pb = 0; pb < p->B; pb += kGroupsPerNorm * pl.nb) {
+    a.n_groups = 0;
+    for (int gr = 0; gr < kGroupsPerNorm; ++gr) {
+      const int b0 = pb + gr * pl.nb;
+      if (b0 >= p->B) break;
+      a.b0 = b0;
+      a.nb = p->B - b0 < pl.nb ? p->B - b0 : pl.nb;
+      a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.logits_off[gr]);
+      a.stats = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.stats_off[gr]);
+      a.wait_at_end = gr;
+      long long acc = 0, cost = 0;
       for (int t = 0; t < pl.n_slab; ++t) {
-        if (pl.slab[t].channel != ch) continue;
-        SlabInfo& I = a.info[n_info++];
-        I.logit_off = pl.slab[t].logit_off;
-        I.first_tile = a.slab_start[t];
-        I.cost_start = a.cost_start[t];
-        I.npairs = pl.slab[t].npairs;
-        I.tiles = pl.slab[t].tiles;
-        I.cost = pl.slab[t].cost;
-        I.row0 = row;
-        I.slab = t;
-        I.pad = 0;
-        row += pl.slab[t].npairs;
+        a.slab_start[t] = acc;
+        a.cost_start[t] = cost;
+        acc += (long long)a.nb * pl.slab[t].tiles;
+        cost += (long long)a.nb * pl.slab[t].tiles * pl.slab[t].cost;
       }
-    // every CTA's share of the cost must reach the largest tile cost, so that
-    // each CTA owns at least one tile (the normalise kernel relies on it)
-    long long wmax = 1;
-    for (int t = 0; t < pl.n_slab; ++t)
-      if (pl.slab[t].cost > wmax) wmax = pl.slab[t].cost;
-    long long grid = sms < kScoreGridMax ? sms : kScoreGridMax;
-    if (grid > a.total_cost / wmax) grid = a.total_cost / wmax;
-    if (grid < 1) grid = 1;
-    a.grid = int(grid);
-    if (score_launch(a, pl.launch, stream, b0 == 0 ? after_first_stream : nullptr) != cudaSuccess)
-      return DUSTIN_ECUDA;
+      a.slab_start[pl.n_slab] = acc;
+      a.cost_start[pl.n_slab] = cost;
+      a.total = acc;
+      a.total_cost = cost;
+      long long grid = sms < kScoreGridMax ? sms : kScoreGridMax;
+      if (grid > a.total_cost / wmax) grid = a.total_cost / wmax;
+      if (grid < 1) grid = 1;
+      a.grid = int(grid);
+      // this group as the normalise kernel sees it
+      NormGroup& g = a.ng[gr];
+      g.b0 = a.b0;
+      g.nb = a.nb;
+      g.grid = a.grid;
+      g.total_cost = a.total_cost;
+      g.logits = a.logits;
+      g.stats = a.stats;
+      int n_info = 0, row = 0;   // the slabs in logits-row order: channel 0 first
+      for (int ch = 0; ch < 2; ++ch)
+        for (int t = 0; t < pl.n_slab; ++t) {
+          if (pl.slab[t].channel != ch) continue;
+          SlabInfo& I = a.info[gr][n_info++];
+          I.logit_off = pl.slab[t].logit_off;
+          I.first_tile = a.slab_start[t];
+          I.cost_start = a.cost_start[t];
+          I.npairs = pl.slab[t].npairs;
+          I.tiles = pl.slab[t].tiles;
+          I.cost = pl.slab[t].cost;
+          I.row0 = row;
+          I.slab = t;
+          I.pad = 0;
+          row += pl.slab[t].npairs;
+        }
+      a.n_groups = gr + 1;
+      if (score_stream_launch(a, pl.launch, stream) != cudaSuccess) return DUSTIN_ECUDA;
+      if (pb == 0 && gr == 0 && after_first_stream &&
+          cudaEventRecord(after_first_stream, stream) != cudaSuccess)
+        return DUSTIN_ECUDA;
+    }
+    // normalise both: every CTA resident at once, spread over the sequences
+    int nseq = 0;
+    for (int gr = 0; gr < a.n_groups; ++gr) nseq += a.ng[gr].nb;
+    int cps = int((long long)sms * score_norm_ctas_per_sm(pl.n_rows) / nseq);
+    if (cps < 1) cps = 1;
+    if (cps > nchunks) cps = nchunks;
+    for (int gr = 0; gr < a.n_groups; ++gr) a.ng[gr].cps = cps;
+    if (score_norm_launch(a, pl.launch, stream) != cudaSuccess) return DUSTIN_ECUDA;
   }
   return DUSTIN_OK;
 }
@@ -688,7 +728,9 @@ int dustin_step_launches(const dustin_step* s, int32_t* n_launches, int32_t* gro
   const int st = build_score_plan(&s->p, s->draft, s->target, s->srh, s->n_srh, &pl);
   if (st != DUSTIN_OK) return st;
   const int groups = (s->p.B + pl.nb - 1) / pl.nb;
-  *n_launches = 2 * groups + 3;   // stream + normalise per group, select, verify + merge
+  // a stream kernel per group, a normalise per kGroupsPerNorm groups, select,
+  // verify + merge
+  *n_launches = groups + (groups + kGroupsPerNorm - 1) / kGroupsPerNorm + 3;
   *group_size = pl.nb;
   return DUSTIN_OK;
 }

@@ -124,6 +124,17 @@ struct SlabInfo {
   int slab, pad;         // index of the slab in ScoreArgs::slab
 };
 
+// One stream launch as the normalise kernel sees it.
+struct NormGroup {
+  int b0, nb;            // its sequences
+  int grid;              // CTAs of its stream kernel
+  int cps;               // normalise CTAs per sequence
+  long long total_cost;  // its partition's total cost
+  float* logits;         // its logits buffer
+  float* stats;          // its statistics buffer
+};
+
+
 struct ScoreArgs {
   CUtensorMap map[DUSTIN_MAX_SRH];   // one per (channel, layer) cache; box 64 x 128
   ScoreSlab slab[DUSTIN_MAX_SRH];
@@ -143,7 +154,16 @@ struct ScoreArgs {
   float* stats;          // [n_slab][nb][max_seg][np_max][2]
   float* importance;     // [B][2][Lcap]
   int* hist;             // [B][2][4096] selection histograms, or nullptr
-  SlabInfo info[DUSTIN_MAX_SRH];   // in row order (channel 0 slabs first)
+  // stream kernel: 0 -- wait for the previous launch before starting; 1 --
+  // start at once (the previous launch is the other stream kernel of a pair,
+  // writing other buffers) and wait for it only before exiting, so that this
+  // launch completes after it
+  int wait_at_end;
+  // normalise kernel: the groups it covers (one or two stream launches), each
+  // with its own logits and statistics buffers and partition
+  int n_groups;
+  NormGroup ng[2];
+  SlabInfo info[2][DUSTIN_MAX_SRH];   // per group, in row order (channel 0 slabs first)
 };
 
 struct ScoreLaunch {
@@ -155,12 +175,13 @@ struct ScoreLaunch {
 constexpr int kScoreGridMax = 256;
 size_t score_stream_smem();
 size_t score_norm_smem(int n_rows);
+int score_norm_ctas_per_sm(int n_rows);   // resident normalise CTAs per SM
 int score_rows_per_tile(int D);
 int score_tile_cost(int D, int npairs);
-// Launches the stream and normalise kernels of one sequence group; records
-// after_stream (if given) between the two.
-cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream,
-                         cudaEvent_t after_stream = nullptr);
+// Launches the stream kernel of the group in a (b0, nb, logits, stats, ...).
+cudaError_t score_stream_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream);
+// Launches the normalise kernel of the groups in a.ng[0 .. n_groups).
+cudaError_t score_norm_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream);
 
 // ------------------------------------------------------------------ select
 

@@ -175,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
+  // the range of this CTA (the group's tiles split by cost)
   const long long t0 = tile_at_cost(A, (long long)blockIdx.x * A.total_cost / G);
   const long long t1 = tile_at_cost(A, (long long)(blockIdx.x + 1) * A.total_cost / G);
 
@@ -187,8 +188,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
     fence_barrier_init();
     prefetch_tensormap(&A.map[0]);
   }
-  pdl_launch_dependents();
-  pdl_wait();
+  if (A.wait_at_end) {
+    pdl_launch_dependents();
+  } else {
+    pdl_wait();
+    pdl_launch_dependents();   // the next launch may start once this one may run
+  }
   // clear this group's selection histograms (the normalise kernel that
   // follows fills them; the selection of the previous call has completed)
   if (A.hist) {
@@ -197,21 +202,15 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
     for (int j = blockIdx.x * kThreads + threadIdx.x; j < n; j += G * kThreads) h[j] = 0;
   }
   __syncthreads();
-  if (t0 >= t1) return;
-
-  // The CTA's range as segments: (slab s, sequence bl, first tile, count).
-  int s0, bl0, tile0;
-  decode_tile(A, t0, s0, bl0, tile0);
 
   if (warp == kConsumers) {
     // ----------------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int s = s0, bl = bl0, tile = tile0;
       int i = 0;
-      for (long long t = t0; t < t1;) {
+      // tiles [tile, tile + n) of (slab s, sequence bl) into the ring
+      auto issue = [&](int s, int bl, int tile, int n) -> bool {
         const ScoreSlab& S = A.slab[s];
-        const int n = int(min((long long)(S.tiles - tile), t1 - t));
         const int b = A.b0 + bl;
         int L = A.seq_len[b];
         if (L < 0 || L > A.Lcap) L = 0;
@@ -219,15 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
         const CUtensorMap* map = &A.map[S.cache];
         const int rbase = row2d ? (b * row2d + g) * A.Lcap : 0;
         int r0 = tile * rows;
-        bool stop = false;
         for (int k = 0; k < n; ++k, ++i, r0 += rows) {
           const int st = i % kStages;
-          if (i >= kStages) {
-            if (!mbar_wait(&empty[st], ((i / kStages) - 1) & 1, A.err, abort_flag)) {
-              stop = true;
-              break;
-            }
-          }
+          if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) - 1) & 1, A.err, abort_flag)) return false;
           if (r0 >= L) {
             mbar_arrive(&full[st]);   // nothing to load: an empty tile
             continue;
@@ -248,12 +241,21 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
             if (two) load(dst + kBoxBytes, 0, r0 + kBoxRows);
           }
         }
-        if (stop) break;
-        t += n;
-        tile = 0;
-        if (++bl == A.nb) {
-          bl = 0;
-          ++s;
+        return true;
+      };
+      bool ok = true;
+      if (t0 < t1) {
+        int s, bl, tile;
+        decode_tile(A, t0, s, bl, tile);
+        for (long long t = t0; t < t1 && ok;) {
+          const int n = int(min((long long)(A.slab[s].tiles - tile), t1 - t));
+          ok = issue(s, bl, tile, n);
+          t += n;
+          tile = 0;
+          if (++bl == A.nb) {
+            bl = 0;
+            ++s;
+          }
         }
       }
     }
@@ -261,11 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
     // -------------------------------------------------------------- consumers
     uint32_t qb[NT][kMaxKs][2];
     float rm[NT][2], rs[NT][2];
-    int s = s0, bl = bl0, tile = tile0;
     int i = 0;
-    for (long long t = t0; t < t1;) {
+    // tiles [tile, tile + n) of (slab s, sequence bl); statistics to slot
+    auto segment = [&](int s, int bl, int tile, int n, int slot_idx) {
       const ScoreSlab& S = A.slab[s];
-      const int n = int(min((long long)(S.tiles - tile), t1 - t));
       const int b = A.b0 + bl;
       const int D = S.D, npairs = S.npairs;
       int L = A.seq_len[b];
@@ -338,34 +339,35 @@ __global__ void __launch_bounds__(kThreads, 1) score_stream_kernel(const __grid_
         float m = -INFINITY, sm = 0.f;
         for (int w = 0; w < kConsumers; ++w)
           stat_merge(m, sm, red[(w * 32 + lane) * 2], red[(w * 32 + lane) * 2 + 1]);
-        const long long first = A.slab_start[s] + (long long)bl * S.tiles;
-        const int seg = int(blockIdx.x) - owner_of(A, first, G);
-        float* slot = A.stats + ((size_t(s) * A.nb + bl) * A.max_seg + seg) * size_t(A.np_max) * 2;
+        float* slot = A.stats + ((size_t(s) * A.nb + bl) * A.max_seg + slot_idx) * size_t(A.np_max) * 2;
         slot[lane * 2] = m;
         slot[lane * 2 + 1] = sm;
       }
       named_bar(1, 32 * kConsumers);
-      t += n;
-      tile = 0;
-      if (++bl == A.nb) {
-        bl = 0;
-        ++s;
+    };
+    if (t0 < t1) {
+      int s, bl, tile;
+      decode_tile(A, t0, s, bl, tile);
+      for (long long t = t0; t < t1;) {
+        const int n = int(min((long long)(A.slab[s].tiles - tile), t1 - t));
+        const long long first = A.slab_start[s] + (long long)bl * A.slab[s].tiles;
+        segment(s, bl, tile, n, int(blockIdx.x) - owner_of(A, first, G));
+        t += n;
+        tile = 0;
+        if (++bl == A.nb) {
+          bl = 0;
+          ++s;
+        }
       }
     }
   }
+  if (A.wait_at_end) pdl_wait();   // complete only after the previous launch
 }
 
-// Normalise: one CTA per (256 positions, sequence).  Warp 0 pulls the CTA's
-// slice of every logits row (1 KB per row) into shared memory with one bulk
-// copy per row, so all of a CTA's loads are in flight at once and the bytes
-// in flight per SM are bounded by shared memory, not registers; meanwhile the
-// first threads merge each row's segment statistics into M and 1/S.  Then
-// thread t owns position t of the slice: it sums exp2(l - M) / S over the
-// rows of each channel, writes both importance values and, in the fused step,
-// adds their keys to the sequence's selection histograms (unprotected
-// positions only; one reduction per distinct bin of a warp).
 constexpr int kNormRowsMax = 48;   // logits rows staged per batch
 
+// Adds one to h[bin] for every lane with ok: one reduction per distinct bin
+// of the warp.
 __device__ __forceinline__ void hist_red(int* h, uint32_t bin, bool ok, int lane) {
   const uint32_t mask = __match_any_sync(0xffffffffu, ok ? bin : 0xFFFFFFFFu);
   if (ok && lane == __ffs(mask) - 1) atomicAdd(h + bin, __popc(mask));
@@ -383,59 +385,84 @@ __device__ __forceinline__ int slab_of_row(const SlabInfo* si, int ns, int r) {
   return j;
 }
 
-__global__ void __launch_bounds__(kNormThreads) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
+// Normalise kernel: over one or two stream launches' groups (a.ng), cps CTAs
+// per sequence, each owning the 256-position chunks x = r, r + cps, ... of its
+// sequence.  A work item is
+// (chunk, batch of up to kNormRowsMax logits rows); items go through two
+// shared-memory buffers, so the bulk copies of item i + 2 (one per row,
+// issued by eight warps) are in flight while item i is computed.  Each
+// issuing thread arms the buffer's mbarrier for its own row (arrive +
+// expected bytes), so a refill needs one block barrier.  Thread t owns
+// position t of a chunk.
+__global__ void __launch_bounds__(kNormThreads, 2) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
   extern __shared__ __align__(128) unsigned char nsm[];
   __shared__ SlabInfo si[DUSTIN_MAX_SRH];
   const int nr = A.n_rows, n0 = A.n_rows0, ns = A.n_slab;
-  const int nbatch_rows = nr < kNormRowsMax ? nr : kNormRowsMax;
-  float* lg = reinterpret_cast<float*>(nsm);                       // [rows][256]
-  float* Mg = lg + size_t(nbatch_rows) * kNormThreads;            // [nr]
+  const int nbr = nr < kNormRowsMax ? nr : kNormRowsMax;           // rows per batch
+  float* lg = reinterpret_cast<float*>(nsm);                       // [2][nbr][256]
+  float* Mg = lg + size_t(2) * nbr * kNormThreads;                 // [nr]
   float* Ig = Mg + nr;                                              // [nr]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(Ig + nr);   // 8-byte aligned: 2 nr floats above
+  uint64_t* bar = reinterpret_cast<uint64_t*>(Ig + nr);            // [2]; 2 nr floats above
   const int tid = threadIdx.x, lane = tid & 31;
-  const int bl = blockIdx.y;
-  const int b = A.b0 + bl;
-  const int base = blockIdx.x * kNormThreads;
-  const int npos = min(kNormThreads, A.LSP - base);   // a multiple of 32
-  const int lines = npos * 4 / 128;
+  const int gr = (A.n_groups > 1 && int(blockIdx.x) >= A.ng[0].nb * A.ng[0].cps) ? 1 : 0;
+  const NormGroup& NG = A.ng[gr];
+  const int cps = NG.cps;
+  const int cta = int(blockIdx.x) - (gr ? A.ng[0].nb * A.ng[0].cps : 0);
+  const int bl = cta / cps, r = cta - (cta / cps) * cps;
+  const int b = NG.b0 + bl;
+  float* const logits = NG.logits;
+  const int nchunks = (A.LSP + kNormThreads - 1) / kNormThreads;
+  const int nbat = (nr + kNormRowsMax - 1) / kNormRowsMax;
+  const int my_chunks = r < nchunks ? (nchunks - r + cps - 1) / cps : 0;
+  const int n_items = my_chunks * nbat;
   // the slab table: one parameter word per thread, all loads in flight at once
   constexpr int kInfoWords = int(sizeof(SlabInfo) / 4);
   for (int j = tid; j < ns * kInfoWords; j += kNormThreads)
-    reinterpret_cast<int*>(si)[j] = reinterpret_cast<const int*>(A.info)[j];
+    reinterpret_cast<int*>(si)[j] = reinterpret_cast<const int*>(A.info[gr])[j];
   if (tid == 0) {
-    mbar_init(bar, 1);
+    mbar_init(&bar[0], nbr);
+    mbar_init(&bar[1], nbr);
     fence_barrier_init();
-    mbar_arrive_expect_tx(bar, uint32_t(nbatch_rows) * npos * 4);
   }
   pdl_launch_dependents();
   pdl_wait();
   __syncthreads();
-  // Rows [r0, r0 + n): one bulk copy of npos floats per row.  Row r0 + q is
-  // issued by thread 32 (q % 8) + q / 8, so eight warps share the issue.
-  const float* my_src = nullptr;   // this thread's row of the current batch
-  auto issue = [&](int r0, int n) {
-    const int q = (tid & 31) * 8 + (tid >> 5);
-    my_src = nullptr;
-    if ((tid >> 5) < 8 && q < n) {
-      const int r = r0 + q;
-      const int j = slab_of_row(si, ns, r);
-      const int p = r - si[j].row0;
-      my_src = A.logits + si[j].logit_off + (size_t(bl) * si[j].npairs + p) * A.LSP + base;
-      bulk_g2s(lg + size_t(q) * kNormThreads, my_src, uint32_t(npos) * 4, bar);
+  // Item it = (chunk r + (it / nbat) cps, batch it % nbat) into buffer it % 2.
+  // Batch row q is issued by thread 32 (q % 8) + q / 8 (eight warps share it).
+  const int q = (tid & 31) * 8 + (tid >> 5);
+  const float* src0 = nullptr;   // this thread's row in buffer 0 ...
+  const float* src1 = nullptr;   // ... and in buffer 1
+  auto issue = [&](int it) {
+    const int x = r + (it / nbat) * cps, k = it - (it / nbat) * nbat;
+    const int r0 = k * kNormRowsMax, n = min(kNormRowsMax, nr - r0);
+    const int base = x * kNormThreads, npos = min(kNormThreads, A.LSP - base);
+    const int bf = it & 1;
+    const float* src = nullptr;
+    if (tid < 8 * 32 && q < nbr) {
+      if (q < n) {
+        const int row = r0 + q;
+        const int j = slab_of_row(si, ns, row);
+        src = logits + si[j].logit_off + (size_t(bl) * si[j].npairs + (row - si[j].row0)) * A.LSP + base;
+      }
+      mbar_arrive_expect_tx(&bar[bf], src ? uint32_t(npos) * 4 : 0u);
+      if (src) bulk_g2s(lg + (size_t(bf) * nbr + q) * kNormThreads, src, uint32_t(npos) * 4, &bar[bf]);
     }
+    if (bf) src1 = src;
+    else src0 = src;
   };
-  issue(0, nbatch_rows);
+  if (n_items > 0) issue(0);
+  if (n_items > 1) issue(1);
   int L = A.seq_len[b];
   if (L < 0 || L > A.Lcap) L = 0;
   // merged statistics, one row per thread: M and 1 / S over the segments
   // (the CTAs owning the first to the last tile of (slab, sequence bl))
-  for (int r = tid; r < nr; r += kNormThreads) {
-    const int j = slab_of_row(si, ns, r);
-    const int p = r - si[j].row0, tiles = si[j].tiles;
+  for (int row = tid; row < nr; row += kNormThreads) {
+    const int j = slab_of_row(si, ns, row);
+    const int p = row - si[j].row0, tiles = si[j].tiles;
     const long long P0 = si[j].cost_start + (long long)bl * tiles * si[j].cost;
-    const int seg0 = owner_at_cost(P0, A.total_cost, A.grid);
-    const int n_seg = owner_at_cost(P0 + (long long)(tiles - 1) * si[j].cost, A.total_cost, A.grid) - seg0 + 1;
-    const float* slots = A.stats + (size_t(si[j].slab) * A.nb + bl) * A.max_seg * size_t(A.np_max) * 2;
+    const int seg0 = owner_at_cost(P0, NG.total_cost, NG.grid);
+    const int n_seg = owner_at_cost(P0 + (long long)(tiles - 1) * si[j].cost, NG.total_cost, NG.grid) - seg0 + 1;
+    const float* slots = NG.stats + (size_t(si[j].slab) * NG.nb + bl) * A.max_seg * size_t(A.np_max) * 2;
     float m = -INFINITY, sm = 0.f;
     for (int g = 0; g < n_seg; g += 4) {
       float2 v[4];
@@ -446,50 +473,54 @@ __global__ void __launch_bounds__(kNormThreads) score_norm_kernel(const __grid_c
       for (int u = 0; u < 4; ++u)
         if (g + u < n_seg) stat_merge(m, sm, v[u].x, v[u].y);
     }
-    Mg[r] = m;
-    Ig[r] = sm > 0.f ? 1.f / sm : 0.f;
+    Mg[row] = m;
+    Ig[row] = sm > 0.f ? 1.f / sm : 0.f;
   }
   __syncthreads();
+  const int s_eff = min(A.sinks, L);
+  const int w0 = max(L - A.window, s_eff);
+  int* h = A.hist ? A.hist + size_t(b) * 2 * kSelectBins : nullptr;
   float acc0 = 0.f, acc1 = 0.f;
-  uint32_t phase = 0;
-  for (int r0 = 0; r0 < nr; r0 += kNormRowsMax, phase ^= 1u) {
-    const int n = min(kNormRowsMax, nr - r0);
-    if (r0 > 0) {
-      __syncthreads();   // every thread is done with the previous batch
-      if (tid == 0) mbar_arrive_expect_tx(bar, uint32_t(n) * npos * 4);
-      __syncthreads();
-      issue(r0, n);
-    }
-    mbar_wait(bar, phase, A.err, nullptr);
-    // the slice of this thread's row has landed: drop it from L2 without
-    // write-back (the logits are dead once staged)
-    if (my_src)
-      for (int ln = 0; ln < lines; ++ln)
-        asm volatile("discard.global.L2 [%0], 128;" ::"l"(my_src + ln * 32) : "memory");
+  for (int it = 0; it < n_items; ++it) {
+    const int bf = it & 1;
+    const int x = r + (it / nbat) * cps, k = it - (it / nbat) * nbat;
+    const int r0 = k * kNormRowsMax, n = min(kNormRowsMax, nr - r0);
+    const int base = x * kNormThreads, npos = min(kNormThreads, A.LSP - base);
+    mbar_wait(&bar[bf], uint32_t(it >> 1) & 1u, A.err, nullptr);
+    // this thread's row has landed: drop its lines from L2 without write-back
+    // (the logits are dead once staged)
+    if (const float* src = bf ? src1 : src0)
+      for (int ln = 0; ln < npos * 4 / 128; ++ln)
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(src + ln * 32) : "memory");
     if (tid < npos) {
+      const float* lb = lg + size_t(bf) * nbr * kNormThreads + tid;
 #pragma unroll 4
       for (int j = 0; j < n; ++j) {
-        const int r = r0 + j;
-        const float v = fast_exp2(lg[size_t(j) * kNormThreads + tid] - Mg[r]) * Ig[r];
-        if (r < n0) acc0 += v;
+        const int row = r0 + j;
+        const float v = fast_exp2(lb[size_t(j) * kNormThreads] - Mg[row]) * Ig[row];
+        if (row < n0) acc0 += v;
         else acc1 += v;
       }
     }
-  }
-  const int pos = base + tid;
-  const bool live = pos < L;
-  if (pos < A.Lcap) {
-    A.importance[(size_t(b) * 2 + 0) * A.Lcap + pos] = live ? acc0 : 0.f;
-    A.importance[(size_t(b) * 2 + 1) * A.Lcap + pos] = live ? acc1 : 0.f;
-  }
-  if (A.hist) {
-    const int s_eff = min(A.sinks, L);
-    const int w0 = max(L - A.window, s_eff);
-    const bool in_u = pos >= s_eff && pos < w0;
-    int* h = A.hist + size_t(b) * 2 * kSelectBins;
-    // (positions past seq_len hold stale logits: they are never keyed)
-    hist_red(h, in_u ? select_bin(importance_key(acc0, A.err)) : 0u, in_u, lane);
-    hist_red(h + kSelectBins, in_u ? select_bin(importance_key(acc1, A.err)) : 0u, in_u, lane);
+    if (k == nbat - 1) {   // the chunk's last batch: write it
+      const int pos = base + tid;
+      const bool live = pos < L;
+      if (pos < A.Lcap) {
+        A.importance[(size_t(b) * 2 + 0) * A.Lcap + pos] = live ? acc0 : 0.f;
+        A.importance[(size_t(b) * 2 + 1) * A.Lcap + pos] = live ? acc1 : 0.f;
+      }
+      if (h) {
+        const bool in_u = pos >= s_eff && pos < w0;
+        // (positions past seq_len hold stale logits: they are never keyed)
+        hist_red(h, in_u ? select_bin(importance_key(acc0, A.err)) : 0u, in_u, lane);
+        hist_red(h + kSelectBins, in_u ? select_bin(importance_key(acc1, A.err)) : 0u, in_u, lane);
+      }
+      acc0 = acc1 = 0.f;
+    }
+    if (it + 2 < n_items) {
+      __syncthreads();   // every thread is done with this buffer
+      issue(it + 2);
+    }
   }
 }
 
@@ -509,7 +540,15 @@ size_t score_stream_smem() {
 
 size_t score_norm_smem(int n_rows) {
   const int nb = n_rows < kNormRowsMax ? n_rows : kNormRowsMax;
-  return size_t(nb) * kNormThreads * 4 + size_t(2 * n_rows + 2) * 4 + 16;
+  return size_t(2) * nb * kNormThreads * 4 + size_t(2 * n_rows) * 4 + 2 * 8 + 16;
+}
+
+int score_norm_ctas_per_sm(int n_rows) {
+  const size_t per = score_norm_smem(n_rows) + sizeof(SlabInfo) * DUSTIN_MAX_SRH + 1024;
+  const int by_smem = int((size_t(228) * 1024) / per);
+  const int by_threads = 2048 / kNormThreads;
+  const int n = by_smem < by_threads ? by_smem : by_threads;
+  return n > 0 ? n : 1;
 }
 
 int score_rows_per_tile(int D) { return D == 128 ? kBoxRows : 2 * kBoxRows; }
@@ -521,23 +560,23 @@ int score_tile_cost(int D, int npairs) {
   return 1000 + score_rows_per_tile(D) * npairs;
 }
 
-cudaError_t score_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream,
-                         cudaEvent_t after_stream) {
-  cudaError_t e;
+cudaError_t score_stream_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream) {
   switch (pl.NT) {
-    case 1: e = launch_stream<1>(a, pl, stream); break;
-    case 2: e = launch_stream<2>(a, pl, stream); break;
-    case 3: e = launch_stream<3>(a, pl, stream); break;
-    case 4: e = launch_stream<4>(a, pl, stream); break;
+    case 1: return launch_stream<1>(a, pl, stream);
+    case 2: return launch_stream<2>(a, pl, stream);
+    case 3: return launch_stream<3>(a, pl, stream);
+    case 4: return launch_stream<4>(a, pl, stream);
     default: return cudaErrorInvalidValue;
   }
-  if (e != cudaSuccess) return e;
-  if (after_stream && (e = cudaEventRecord(after_stream, stream)) != cudaSuccess) return e;
+}
+
+cudaError_t score_norm_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream) {
   static const cudaError_t attr = cudaFuncSetAttribute(
       score_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(score_norm_smem(DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS)));
   if (attr != cudaSuccess) return attr;
-  dim3 grid((a.LSP + kNormThreads - 1) / kNormThreads, a.nb);
-  return launch_pdl(score_norm_kernel, grid, dim3(kNormThreads), pl.norm_smem, stream, a);
+  int ctas = 0;
+  for (int g = 0; g < a.n_groups; ++g) ctas += a.ng[g].nb * a.ng[g].cps;
+  return launch_pdl(score_norm_kernel, dim3(ctas), dim3(kNormThreads), pl.norm_smem, stream, a);
 }
 
 }  // namespace dustin

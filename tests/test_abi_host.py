@@ -169,7 +169,8 @@ def test_step_rejects_null_and_too_many_layers(L):
 
 def test_step_launch_count(L):
     """The launch-count query plans like dustin_verify_step: two kernels per
-    scoring group, then select, then verify and the merge of split units."""
+    scoring group (stream, normalise), then select, then verify and the merge
+    of split units."""
     from sparse_kv_verify_gb300 import binding as bd
     lib = L.lib()
 
