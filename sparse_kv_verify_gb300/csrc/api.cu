@@ -2,14 +2,13 @@
 // and kernel launches for the calls declared in include/dustin.h.  Nothing
 // here allocates device memory; scratch lives in the caller's workspace:
 //   [0, 256)                 header: the sticky device error word (int32 at 0)
-//   [256, 256 + 64 KiB)      selection arrival counters, one int per sequence;
-//                            zero between calls (cleared by dustin_workspace_init)
+//   [256, 256 + 64 KiB)      reserved (cleared by dustin_workspace_init)
 //   [kScratch, ...)          scratch shared by the stages of one call:
 //                            score: logits of one group of sequences
 //                                   [n_slab][nb][pairs][LSP] (kept in L2) and
 //                                   per-segment (max, sum) statistics
 //                            select (after the score scratch in the fused
-//                                   step): histograms, candidate lists, bitmaps
+//                                   step): histograms, bitmaps
 //                            verify: segment partials [units][max_seg][slot]
 #include <cudaTypedefs.h>
 
@@ -25,7 +24,7 @@ using namespace dustin;
 namespace {
 
 constexpr size_t kHeader = 256;
-constexpr size_t kCounterBytes = size_t(kSelectCountersMax) * 4;   // selection counters
+constexpr size_t kCounterBytes = 65536;   // reserved
 constexpr long long kVerifyUnitsMax = 16384;        // B * Hkv * layers per verification call
 constexpr size_t kScratch = kHeader + kCounterBytes;
 
@@ -591,12 +590,7 @@ int run_select(const dustin_params* p, const float* importance, const int32_t* s
   char* w = static_cast<char*>(ws);
   SelectArgs a{};
   a.hist = reinterpret_cast<int*>(w + sel.hist_off);
-  a.lists = reinterpret_cast<uint2*>(w + sel.lists_off);
-  a.list_counts = reinterpret_cast<int*>(w + sel.counts_off);
   a.bits = reinterpret_cast<uint32_t*>(w + sel.bits_off);
-  a.counters = reinterpret_cast<int*>(w + kHeader);   // reserved area, zero between calls
-  a.cs = sel.cs;
-  a.list_cap = sel.list_cap;
   a.bits_words = sel.bits_words;
   a.B = p->B;
   a.Lcap = p->Lcap;

@@ -185,14 +185,12 @@ cudaError_t score_norm_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStr
 
 // ------------------------------------------------------------------ select
 
-constexpr int kMaxSelectCtas = 8;          // scan CTAs per sequence
-constexpr int kSelectCountersMax = 16384;  // sequences whose arrival counters fit the reserved area
+constexpr int kMaxSelectCtas = 8;          // scan CTAs (cluster size) per sequence
 
 struct SelectArgs {
   int B, Lcap, k, sinks, window, m;
   int vec4;              // set by select_launch: rows read as float4
-  int cs;                // scan CTAs per sequence
-  int list_cap;          // list entries per (sequence, channel, scan CTA)
+  int cs;                // set by select_launch: scan CTAs per sequence (one cluster)
   int bits_words;        // bitmap words per sequence (general path)
   const float* imp;      // [B][2][Lcap]
   int* hist;             // [B][2][4096] level-1 histograms over the unprotected
@@ -201,16 +199,13 @@ struct SelectArgs {
   const int32_t* seq_len;
   int32_t* out;          // [B][k]
   int* err;
-  uint2* lists;          // [B][2][cs][list_cap] (key, position)
-  int* list_counts;      // [B][2][cs]; -1: overflow
-  int* counters;         // [B] arrival counters, zero between calls
   uint32_t* bits;        // [B][bits_words]
 };
 
 // Workspace layout of the selection scratch starting at byte offset off.
 struct SelectPlan {
-  int cs, list_cap, bits_words;
-  size_t hist_off, lists_off, counts_off, bits_off, end;
+  int bits_words;
+  size_t hist_off, bits_off, end;
 };
 SelectPlan select_plan(int B, int Lcap, size_t off);
 // build_hist: count the histograms first (standalone call).

@@ -14,31 +14,39 @@
 // per sequence (built by the scoring kernel while it writes the importance,
 // or by select_hist_kernel for a standalone call).
 //
-// select_kernel: CS CTAs of 1024 threads per sequence, each owning one
-// contiguous run of U (each warp a run of whole 128-position rows).
+// select_kernel: one thread-block cluster of CS CTAs (1024 threads each) per
+// sequence, each CTA owning one contiguous run of U (each warp a run of whole
+// 128-position rows).
 //   scan     every CTA finds, from the histograms, the bin b0 holding the m1-th
 //            draft key and the bin b1 holding the (m1 + f)-th target key, and
 //            in one pass (float4 loads) lists, in position order, the draft
-//            keys of bins >= b0 and the target keys of bins >= b1 of its run.
-//            Every draft winner is listed, and so is every target winner: the
-//            f-th target key outside the draft tier is at least the (m1+f)-th
-//            target key of U, because at most m1 of the top m1+f are taken
-//            by the draft tier.  The lists go to the workspace.
-//   finish   the last CTA of the sequence to arrive (an atomic counter; no CTA
-//            waits for another) gathers the lists and selects exactly:
-//            draft tier -- two 10-bit radix passes over the listed keys of bin
-//            b0 give the threshold key T and how many keys equal to T are
-//            taken (the lowest positions), then one ordered compaction of the
-//            list writes the tier; target tier -- the same over the target
-//            list minus the draft tier, with the target histogram corrected by
-//            the draft tier's target keys.
+//            keys of bins >= b0 (with the target key of the same position) and
+//            the target keys of bins >= b1 of its run.  Every draft winner is
+//            listed, and so is every target winner: the f-th target key
+//            outside the draft tier is at least the (m1+f)-th target key of U,
+//            because at most m1 of the top m1+f are taken by the draft tier.
+//   finish   after a cluster barrier, rank 0 gathers every rank's lists through
+//            distributed shared memory (a second barrier then lets the other
+//            ranks leave) and selects exactly: draft tier -- two 10-bit radix
+//            passes over the listed keys of bin b0 give the threshold key T and
+//            how many keys equal to T are taken (the lowest positions), then
+//            one ordered compaction of the list writes the tier; target tier
+//            -- the same over the target list minus the draft tier, with the
+//            target histogram corrected by the draft tier's target keys.
 // If a list outgrows its buffer (heavy ties) or the draft tier is larger than
-// the on-chip copy of it, the finishing CTA selects that sequence with the
-// general path: candidates of the threshold bin in a shared list (or, past its
-// capacity, refinement over the whole range) and ordered passes over all keys.
-// Every path gives the same set.
+// the on-chip copy of it, rank 0 selects that sequence with the general path:
+// candidates of the threshold bin in a shared list (or, past its capacity,
+// refinement over the whole range) and ordered passes over all keys.  Every
+// path gives the same set.
+#include <cooperative_groups.h>
+
+#include <mutex>
+#include <vector>
+
 #include "common.cuh"
 #include "kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace dustin {
 
@@ -50,36 +58,40 @@ constexpr int kBins1 = kSelectBins;   // top 12 bits
 constexpr int kBins2 = 1024;          // 10 bits per refinement pass
 constexpr int kListCap = 128;         // entries per warp list and channel (scan)
 constexpr int kCandCap = 4096;        // candidates of the general path
-constexpr int kFinCap = 8192;         // list entries gathered on chip (finish)
-constexpr int kDCap = 8192;           // draft-tier positions kept on chip (finish)
+constexpr int kFinCap = 6144;         // list entries of both channels gathered by rank 0
+constexpr int kDCap = kBins1;         // draft-tier positions kept on chip (in h[0])
 constexpr int kBatch = 8;             // rows of 32 keys loaded before use (general path)
 constexpr int kHistThreads = 1024;    // select_hist_kernel: positions per CTA
+constexpr int kCells = kMaxSelectCtas * kWarps;   // (rank, warp) lists per channel
 
 struct SelShared {
-  int h[2][kBins1];          // level-1 histograms of the tiers' positions
+  int h[2][kBins1];          // level-1 histograms (h[0] holds the draft tier's
+                             // positions once the scan is done)
   int h2[kBins2];            // refinement histogram
   union {
-    struct {                 // scan: per-warp ordered lists of both channels
-      uint32_t key[2][kWarps][kListCap];
-      int pos[2][kWarps][kListCap];
+    struct {                 // scan: per-warp ordered lists
+      uint32_t k0[kWarps][kListCap];    // draft keys ...
+      uint32_t k0t[kWarps][kListCap];   // ... the target keys of their positions ...
+      int p0[kWarps][kListCap];         // ... and the positions
+      uint32_t k1[kWarps][kListCap];    // target keys ...
+      int p1[kWarps][kListCap];         // ... and positions
     } l;
     struct {                 // general path: threshold-bin candidates
       uint32_t key[kCandCap];
       int pos[kCandCap];
     } c;
-    struct {                 // finish: one channel's gathered list
-      uint32_t key[kFinCap];
-      int pos[kFinCap];
-    } e;
   } u;
-  int dpos[kDCap];           // finish: the draft tier, ascending
-  uint32_t drop[kFinCap / 32];    // finish: target-list entries in the draft tier
+  // rank 0: the gathered lists, draft entries [0, n0) then target [n0, n0 + n1)
+  uint32_t ekey[kFinCap];
+  int epos[kFinCap];
+  uint32_t ek0t[kFinCap];    // target key of a draft entry
+  uint32_t drop[kFinCap / 32];    // target entries in the draft tier
+  int cell[2][kCells + 1];   // rank 0: list offsets per (rank, warp), then the total
   int lcnt[2][kWarps];
   int wsum[kWarps];          // scan scratch
   int wgt[kWarps], weq[kWarps];   // per warp: keys above / equal to T
   int gtb[kWarps], eqb[kWarps];   // exclusive prefixes of wgt, weq
-  int goff[kMaxSelectCtas + 1];   // finish: list offsets of the scan CTAs
-  int ncand, bin, need, found, overflow, last, tot;
+  int ncand, bin, need, found, overflow;
 };
 
 // ------------------------------------------------------------------ helpers
@@ -397,17 +409,19 @@ __device__ void block_prefix2(SelShared& sh, int& a, int& b) {
   b = sh.eqb[warp] + ib - b;
 }
 
-// Exact top cnt of the gathered list sh.u.e[0..n) (in position order), minus
-// the entries marked in dropbits (if given), given the tier's level-1 bin b1
-// and how many of its keys are taken (need): written in position order to
-// out[0..cnt), and to dcopy if given.
-__device__ void finish_tier(SelShared& sh, int n, uint32_t b1, int need, int cnt, int32_t* out,
-                            int* dcopy, const uint32_t* dropbits) {
+// Exact top cnt of the gathered entries key/pos[0..n) (in position order),
+// minus the entries marked in dropbits (if given), given the tier's level-1
+// bin b1 and how many of its keys are taken (need): written in position order
+// to out[0..cnt); to dcopy if given; and, with sub (the target keys of the
+// entries), each selected entry's target key is taken out of h1.
+__device__ void finish_tier(SelShared& sh, const uint32_t* key, const int* pos, int n, uint32_t b1,
+                            int need, int cnt, int32_t* out, int* dcopy, const uint32_t* dropbits,
+                            const uint32_t* sub, int* h1) {
   auto drop = [&](int j) { return dropbits && ((dropbits[j >> 5] >> (j & 31)) & 1u); };
   const int tid = threadIdx.x;
   const uint32_t T = refine(sh, b1, &need, [&](auto f) {
     for (int j = tid; j < n; j += kThreads) {
-      const uint32_t kv = sh.u.e.key[j];
+      const uint32_t kv = key[j];
       f(kv, select_bin(kv) == b1 && !drop(j));
     }
   });
@@ -418,7 +432,7 @@ __device__ void finish_tier(SelShared& sh, int n, uint32_t b1, int need, int cnt
   int ngt = 0, neq = 0;
   for (int j = j0; j < j1; ++j) {
     if (drop(j)) continue;
-    const uint32_t kv = sh.u.e.key[j];
+    const uint32_t kv = key[j];
     ngt += kv > T;
     neq += kv == T;
   }
@@ -427,64 +441,19 @@ __device__ void finish_tier(SelShared& sh, int n, uint32_t b1, int need, int cnt
   int eq_run = neq;
   for (int j = j0; j < j1; ++j) {
     if (drop(j)) continue;
-    const uint32_t kv = sh.u.e.key[j];
+    const uint32_t kv = key[j];
     bool sel = kv > T;
     if (kv == T) sel = eq_run++ < need_eq;
     if (sel) {
       if (o < cnt) {
-        out[o] = sh.u.e.pos[j];
-        if (dcopy) dcopy[o] = sh.u.e.pos[j];
+        out[o] = pos[j];
+        if (dcopy) dcopy[o] = pos[j];
       }
+      if (sub) atomicSub(&h1[select_bin(sub[j])], 1);
       ++o;
     }
   }
   __syncthreads();
-}
-
-// Gathers channel c's lists of the scan CTAs of sequence b into sh.u.e, in
-// CTA order; returns the entry count, or -1 if a list overflowed or the total
-// does not fit.  The counts are read one per lane and every entry load is in
-// flight at once.
-__device__ int gather(SelShared& sh, const SelectArgs& A, int b, int c) {
-  constexpr int kPer = kFinCap / kThreads;   // entries per thread at most
-  const int tid = threadIdx.x;
-  if (tid < 32) {
-    const int n = tid < A.cs ? __ldcg(A.list_counts + (size_t(b) * 2 + c) * A.cs + tid) : 0;
-    const bool bad = __any_sync(0xffffffffu, n < 0);
-    int incl = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (tid >= o) incl += y;
-    }
-    if (tid <= A.cs) sh.goff[tid] = incl - n;   // goff[cs] = total
-    if (tid == 31) sh.tot = (bad || incl > kFinCap) ? -1 : incl;
-  }
-  __syncthreads();
-  const int total = sh.tot;
-  if (total < 0) return -1;
-  const uint2* base = A.lists + (size_t(b) * 2 + c) * A.cs * A.list_cap;
-  uint2 e[kPer];
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int j = tid + u * kThreads;
-    e[u] = make_uint2(0u, 0u);
-    if (j < total) {
-      int r = 0;
-      while (r + 1 < A.cs && sh.goff[r + 1] <= j) ++r;
-      e[u] = __ldcg(base + size_t(r) * A.list_cap + (j - sh.goff[r]));
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int j = tid + u * kThreads;
-    if (j < total) {
-      sh.u.e.key[j] = e[u].x;
-      sh.u.e.pos[j] = int(e[u].y);
-    }
-  }
-  __syncthreads();
-  return total;
 }
 
 // ------------------------------------------------------------------ kernels
@@ -494,8 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   SelShared& sh = *reinterpret_cast<SelShared*>(dsm);
   pdl_launch_dependents();
   pdl_wait();
-  const int CS = A.cs;
-  const int b = blockIdx.x / CS, r = blockIdx.x - (blockIdx.x / CS) * CS;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CS = A.cs;   // the cluster size
+  const int b = blockIdx.x / CS, r = int(cluster.block_rank());
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t lt = (1u << lane) - 1u;
   int32_t* out = A.out + size_t(b) * A.k;
@@ -570,19 +540,26 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
         for (int e = 0; e < 4; ++e) v[c][e] = i0 + e < x1 ? __ldg(row + i0 + e) : 0.f;
       }
     }
+    uint32_t kv[2][4];
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const uint32_t thr = c ? b1 : b0;
-      uint32_t kv[4], m[4];
-      int before = 0, total = 0;
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = i0 + e;
         const bool ok = i >= s_eff && i < x1;
         const uint32_t bits = __float_as_uint(v[c][e]);
         bad |= ok && bits > 0x7F800000u && bits != 0x80000000u;
-        kv[e] = (ok && bits <= 0x7F800000u) ? bits : 0u;   // importance_key; flag raised once below
-        m[e] = __ballot_sync(0xffffffffu, ok && select_bin(kv[e]) >= thr);
+        kv[c][e] = (ok && bits <= 0x7F800000u) ? bits : 0u;   // importance_key; flag raised once below
+      }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint32_t thr = c ? b1 : b0;
+      uint32_t m[4];
+      int before = 0, total = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool ok = i0 + e >= s_eff && i0 + e < x1;
+        m[e] = __ballot_sync(0xffffffffu, ok && select_bin(kv[c][e]) >= thr);
         before += __popc(m[e] & lt);
         total += __popc(m[e]);
       }
@@ -593,8 +570,14 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
       for (int e = 0; e < 4; ++e) {
         if ((m[e] >> lane) & 1u) {
           if (slot < kListCap) {
-            sh.u.l.key[c][warp][slot] = kv[e];
-            sh.u.l.pos[c][warp][slot] = i0 + e;
+            if (c) {
+              sh.u.l.k1[warp][slot] = kv[1][e];
+              sh.u.l.p1[warp][slot] = i0 + e;
+            } else {
+              sh.u.l.k0[warp][slot] = kv[0][e];
+              sh.u.l.k0t[warp][slot] = kv[1][e];
+              sh.u.l.p0[warp][slot] = i0 + e;
+            }
           }
           ++slot;
         }
@@ -608,65 +591,81 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
     sh.lcnt[1][warp] = n1;
     if (n0 > kListCap || n1 > kListCap) atomicOr(&sh.overflow, 1);
   }
-  __syncthreads();
-  // ---- scan: this CTA's lists to the workspace, in warp order
-  for (int c = 0; c < 2; ++c) {
-    if (tid < 32) {
-      const int n = min(sh.lcnt[c][tid], kListCap);
-      int incl = n;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (tid >= o) incl += y;
+  // ---- hand-off: every rank's lists are complete
+  cluster.sync();
+  if (r == 0) {
+    // list offsets per (rank, warp), in position order
+    if (tid < 2 * 32) {
+      const int c = tid >> 5, w = tid & 31;
+      int run = 0;
+      for (int rr = 0; rr < CS; ++rr) {
+        const SelShared* rs = cluster.map_shared_rank(&sh, rr);
+        const int n = min(rs->lcnt[c][w], kListCap);
+        if (w == 0 && rs->overflow) atomicOr(&sh.overflow, 1);
+        sh.cell[c][rr * kWarps + w] = n;   // counts first
+        run += n;
       }
-      sh.wsum[tid] = incl - n;
-      if (tid == 31) sh.tot = incl;
     }
     __syncthreads();
-    const int total = sh.tot;
-    const bool ok = !sh.overflow && total <= A.list_cap;
-    uint2* dst = A.lists + ((size_t(b) * 2 + c) * CS + r) * A.list_cap;
-    const int n = min(sh.lcnt[c][warp], kListCap);
-    if (ok)
-      for (int j = lane; j < n; j += 32)
-        dst[sh.wsum[warp] + j] = make_uint2(sh.u.l.key[c][warp][j], uint32_t(sh.u.l.pos[c][warp][j]));
-    if (tid == 0) A.list_counts[(size_t(b) * 2 + c) * CS + r] = ok ? total : -1;
+    if (tid < 2 * 32) {   // exclusive prefix over the CS * 32 cells of each channel
+      const int c = tid >> 5, lane2 = tid & 31;
+      int carry = 0;
+      for (int base = 0; base < CS * kWarps; base += 32) {
+        const int v = sh.cell[c][base + lane2];
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane2 >= o) incl += y;
+        }
+        sh.cell[c][base + lane2] = carry + incl - v;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane2 == 0) sh.cell[c][CS * kWarps] = carry;
+    }
     __syncthreads();
+    const int n0t = sh.cell[0][CS * kWarps], n1t = sh.cell[1][CS * kWarps];
+    if (!sh.overflow && n0t + n1t <= kFinCap) {
+      // every rank's entries into ekey/epos (draft, then target), in order
+      for (int j = tid; j < n0t + n1t; j += kThreads) {
+        const int c = j < n0t ? 0 : 1, jj = c ? j - n0t : j;
+        int lo = 0, hi = CS * kWarps - 1;   // the last cell starting at or before jj
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (sh.cell[c][mid] <= jj) lo = mid;
+          else hi = mid - 1;
+        }
+        const int rr = lo / kWarps, w = lo - rr * kWarps, slot = jj - sh.cell[c][lo];
+        const SelShared* rs = cluster.map_shared_rank(&sh, rr);
+        if (c == 0) {
+          sh.ekey[j] = rs->u.l.k0[w][slot];
+          sh.ek0t[j] = rs->u.l.k0t[w][slot];
+          sh.epos[j] = rs->u.l.p0[w][slot];
+        } else {
+          sh.ekey[j] = rs->u.l.k1[w][slot];
+          sh.epos[j] = rs->u.l.p1[w][slot];
+        }
+      }
+    } else if (tid == 0) {
+      sh.overflow = 1;
+    }
   }
-  // ---- the last CTA of the sequence to get here finishes it
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = CS > 1 ? atomicAdd(A.counters + b, 1) : 0;
-    sh.last = prev == CS - 1;
-    if (sh.last && CS > 1) A.counters[b] = 0;   // ready for the next call
-  }
-  __syncthreads();
-  if (!sh.last) return;
-  __threadfence();
+  cluster.sync();   // rank 0 has read every rank's lists: the others may leave
+  if (r != 0) return;
 
-  // ---- finish
-  bool general = m1 > kDCap;
-  if (!general && m1 > 0) {
-    const int ne0 = gather(sh, A, b, 0);
-    general = ne0 < 0;
-    if (!general)
-      finish_tier(sh, ne0, b0, need0, m1, out + nP, f > 0 ? sh.dpos : nullptr, nullptr);
-  }
-  int ne1 = 0;
-  if (!general && f > 0) {
-    ne1 = gather(sh, A, b, 1);
-    general = ne1 < 0;
-  }
-  if (general) {
+  // ---- finish (rank 0)
+  const int n0t = sh.cell[0][CS * kWarps], n1t = sh.cell[1][CS * kWarps];
+  int* dpos = &sh.h[0][0];   // the draft tier's positions (h[0] is no longer needed)
+  if (sh.overflow || m1 > kDCap) {
     select_general(sh, A, b, s_eff, w0, nP, m1, f, out);
     return;
   }
+  if (m1 > 0)
+    finish_tier(sh, sh.ekey, sh.epos, n0t, b0, need0, m1, out + nP, f > 0 ? dpos : nullptr, nullptr,
+                f > 0 ? sh.ek0t : nullptr, sh.h[1]);
   if (f > 0) {
-    // the target histogram of U minus the draft tier, and its threshold bin
-    for (int j = tid; j < m1; j += kThreads)
-      atomicSub(&sh.h[1][select_bin(importance_key(__ldg(row1 + sh.dpos[j]), A.err))], 1);
-    __syncthreads();
+    // the target histogram of U minus the draft tier (corrected above), and
+    // its threshold bin
     find_bin(sh, sh.h[1], kBins1, f);
     if (!sh.found) {   // cannot happen with matching keys
       if (tid == 0) flag_error(A.err, DUSTIN_DEV_NAN);
@@ -674,22 +673,23 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
     }
     const uint32_t bt = uint32_t(sh.bin);
     const int needt = sh.need;
-    // mark the list entries that the draft tier took (both lists ascending:
-    // one binary search per entry)
-    for (int j = tid; j < (ne1 + 31) / 32; j += kThreads) sh.drop[j] = 0u;
+    // mark the target entries that the draft tier took (both ascending: one
+    // binary search per entry)
+    for (int j = tid; j < (n1t + 31) / 32; j += kThreads) sh.drop[j] = 0u;
     __syncthreads();
-    for (int j = tid; j < ne1; j += kThreads) {
-      const int p = sh.u.e.pos[j];
+    for (int j = tid; j < n1t; j += kThreads) {
+      const int p = sh.epos[n0t + j];
       int lo = 0, hi = m1;
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
-        if (sh.dpos[mid] < p) lo = mid + 1;
+        if (dpos[mid] < p) lo = mid + 1;
         else hi = mid;
       }
-      if (lo < m1 && sh.dpos[lo] == p) atomicOr(&sh.drop[j >> 5], 1u << (j & 31));
+      if (lo < m1 && dpos[lo] == p) atomicOr(&sh.drop[j >> 5], 1u << (j & 31));
     }
     __syncthreads();
-    finish_tier(sh, ne1, bt, needt, f, out + nP + m1, nullptr, m1 > 0 ? sh.drop : nullptr);
+    finish_tier(sh, sh.ekey + n0t, sh.epos + n0t, n1t, bt, needt, f, out + nP + m1, nullptr,
+                m1 > 0 ? sh.drop : nullptr, nullptr, nullptr);
   }
 }
 
@@ -716,32 +716,67 @@ __global__ void __launch_bounds__(kHistThreads) select_hist_kernel(const __grid_
 
 }  // namespace
 
+namespace {
+
+// How many clusters of cs select CTAs can be resident at once on the current
+// device (cached per device and cluster size).
+int max_active_clusters(int cs) {
+  struct Entry {
+    int dev, cs, n;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : cache)
+    if (e.dev == dev && e.cs == cs) return e.n;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(cs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sizeof(SelShared);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = cs;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(SelShared))) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, select_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache.push_back({dev, cs, n});
+  return n;
+}
+
+}  // namespace
+
 int select_ctas_per_sequence(int B) {
-  // spread the scan over about 128 CTAs; the counters in the reserved
-  // workspace area bound the batches that use more than one per sequence
-  int cs = 128 / (B > 0 ? B : 1);
-  if (cs > kMaxSelectCtas) cs = kMaxSelectCtas;
-  if (cs < 1 || B > kSelectCountersMax) cs = 1;
-  return cs;
+  // the largest cluster (8, 4 or 2 CTAs) whose B clusters are all resident at
+  // once and that keeps the scan to about 128 CTAs; one CTA per sequence when
+  // even pairs do not fit
+  for (int cs = kMaxSelectCtas; cs >= 2; cs >>= 1)
+    if ((long long)B * cs <= 128 && B <= max_active_clusters(cs)) return cs;
+  return 1;
 }
 
 SelectPlan select_plan(int B, int Lcap, size_t off) {
   SelectPlan s{};
-  s.cs = select_ctas_per_sequence(B);
-  const int span = ((((Lcap + 128) + s.cs - 1) / s.cs) + 127) & ~127;
-  s.list_cap = span < kFinCap ? span : kFinCap;
   s.bits_words = (Lcap + 127) / 32 + 2;
   auto r256 = [](size_t x) { return (x + 255) & ~size_t(255); };
   s.hist_off = off;
-  s.lists_off = s.hist_off + r256(size_t(B) * 2 * kBins1 * 4);
-  s.counts_off = s.lists_off + r256(size_t(B) * 2 * s.cs * s.list_cap * 8);
-  s.bits_off = s.counts_off + r256(size_t(B) * 2 * s.cs * 4);
+  s.bits_off = s.hist_off + r256(size_t(B) * 2 * kBins1 * 4);
   s.end = s.bits_off + r256(size_t(B) * s.bits_words * 4);
   return s;
 }
 
 cudaError_t select_launch(const SelectArgs& a0, bool build_hist, cudaStream_t stream) {
   SelectArgs a = a0;
+  a.cs = select_ctas_per_sequence(a.B);
   a.vec4 = (a.Lcap % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.imp) & 15u) == 0);
   cudaError_t e;
   if (build_hist) {
@@ -754,7 +789,21 @@ cudaError_t select_launch(const SelectArgs& a0, bool build_hist, cudaStream_t st
   static const cudaError_t attr =
       cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (attr != cudaSuccess) return attr;
-  return launch_pdl(select_kernel, dim3(a.B * a.cs), dim3(kThreads), smem, stream, a);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.B * a.cs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = a.cs;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, select_kernel, a);
 }
 
 }  // namespace dustin

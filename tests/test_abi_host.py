@@ -50,12 +50,9 @@ def test_workspace_sizing(L):
     def r256(x):
         return (x + 255) // 256 * 256
 
-    # selection scratch, B = 2, Lcap = 1024: histograms [B][2][4096] int32;
-    # candidate lists [B][2][cs][cap] of (key, position) with cs = 8 scan CTAs
-    # per sequence and cap = 256 (one CTA's share of the positions, in whole
-    # 128-position rows); list counts [B][2][cs]; bitmaps [B][(Lcap+127)/32+2]
-    sel = (r256(2 * 2 * 4096 * 4) + r256(2 * 2 * 8 * 256 * 8) + r256(2 * 2 * 8 * 4)
-           + r256(2 * (1151 // 32 + 2) * 4))
+    # selection scratch, B = 2, Lcap = 1024: histograms [B][2][4096] int32
+    # and the general path's bitmaps [B][(Lcap + 127) / 32 + 2] words
+    sel = r256(2 * 2 * 4096 * 4) + r256(2 * (1151 // 32 + 2) * 4)
     assert lib.dustin_workspace_bytes(ctypes.byref(p), None, None, None, 0, 0, 0, 0, 0) == base + sel
     kv_t = (bd.CKV * 1)(bd.CKV(0x10000, 2, 128, 2 * 1024 * 128, 1024 * 128, 128))
     kv_d = (bd.CKV * 1)(bd.CKV(0x20000, 1, 64, 1024 * 64, 1024 * 64, 64))
