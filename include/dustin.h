@@ -224,8 +224,12 @@ int dustin_kv_append(const dustin_params* p, int32_t n_layers, const dustin_kv* 
  * (device, out) = the number of entries of i_verify[b] before its first -1
  * (the -1 entries must form a suffix, as dustin_select writes them).
  * dense_verify_attn over (kc, vc, seq_len_c) with Lcap = k then gives the same
- * result as dustin_verify_attn over (k, v, i_verify).  dustin_verify_attn
- * itself gathers the rows in-kernel and never writes such a copy. */
+ * result as dustin_verify_attn over (k, v, i_verify).  That equality holds
+ * only for calls that do not set DUSTIN_DEV_INDEX: sparse verification skips
+ * an invalid entry, while dense verification over the compact cache attends
+ * to its zero row.  seq_len_c must not be seq_len (other CTAs still read
+ * seq_len while it is written): DUSTIN_EINVAL.  dustin_verify_attn itself
+ * gathers the rows in-kernel and never writes such a copy. */
 int dustin_compact_kv(const dustin_params* p, int32_t n_layers, const dustin_kv* k,
                       const dustin_kv* v, const int32_t* i_verify, const int32_t* seq_len,
                       const dustin_kv* kc, const dustin_kv* vc, int32_t* seq_len_c, void* ws,
@@ -242,6 +246,33 @@ int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStre
  * the merge of the units it split).  Returns DUSTIN_EINVAL / DUSTIN_ERANGE for arguments
  * dustin_verify_step would reject while planning the scoring. */
 int dustin_step_launches(const dustin_step* s, int32_t* n_launches, int32_t* group_size);
+
+/* Host-only query (no device work): the stream-K split that
+ * dustin_verify_attn (dense = 0), dense_verify_attn (dense = 1) and the
+ * verification of dustin_verify_step use on the current device for this
+ * shape.  Units are (layer, sequence, KV head) triples, unit
+ * u = (l * B + b) * hkv + g, each of *tiles_per_unit tiles of 64 keys (the
+ * context tiles, then one draft-block tile); the T = units * tiles_per_unit
+ * tiles are cut among *grid CTAs, CTA c taking tiles [c*T/grid,
+ * (c+1)*T/grid).  A unit whose tiles fall to several CTAs is merged by the
+ * second verification kernel.  DUSTIN_EINVAL / DUSTIN_ERANGE as the
+ * verification calls would return for the shape. */
+int dustin_verify_split(const dustin_params* p, int32_t hq, int32_t hkv, int32_t d,
+                        int32_t n_layers, int32_t dense, int32_t* grid, int32_t* tiles_per_unit);
+
+/* Self-test of the bounded waits (no counterpart in the pages).  Every
+ * on-chip wait of the kernels above gives up after 2 s, sets
+ * DUSTIN_DEV_TIMEOUT in the error word and raises a CTA-wide abort flag that
+ * makes the CTA's other waits give up at once.  This call runs that wait in
+ * one CTA on an mbarrier that nothing ever arrives on, with no copy or MMA in
+ * flight: one thread waits limit_ns nanoseconds (1000 .. 1e9) and gives up,
+ * a second waits with the kernels' own 2 s limit and stops when the first
+ * raises the abort flag.  waited_ns: device int64 [2], 8-byte aligned (out):
+ * how long each waited (-1 if its wait had succeeded).  Afterwards
+ * dustin_check(ws) reports DUSTIN_DEV_TIMEOUT and the context stays usable.
+ * ws needs only its 256-byte header. */
+int dustin_wait_selftest(int64_t limit_ns, int64_t* waited_ns, void* ws, size_t ws_bytes,
+                         cudaStream_t stream);
 
 /* Bytes of the library-owned scratch array used by dustin_score_noalloc. */
 #define DUSTIN_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -262,8 +293,11 @@ int dustin_step_launches(const dustin_step* s, int32_t* n_launches, int32_t* gro
  * Limits: the scratch of at least one sequence -- its logits (SRH pairs x
  * Lcap x 4 bytes) and their statistics, plus a 256-byte header -- must fit in
  * the array; larger batches are scored in groups of sequences that fit.
- * Otherwise DUSTIN_ERANGE is returned and nothing is launched.  The device error word lives in the array too; it is
- * cleared at the start of every call and cannot be read by the caller.
+ * Otherwise DUSTIN_ERANGE is returned and nothing is launched.
+ *
+ * The device error word (DUSTIN_DEV_* bits) lives in the array's first bytes.
+ * It is sticky across calls, like a workspace's: dustin_score_noalloc_check
+ * reads and clears it.
  *
  * All calls share the one array and it keeps the last call's contents: calls
  * that overlap on the GPU (different streams, or different host threads
@@ -271,6 +305,13 @@ int dustin_step_launches(const dustin_step* s, int32_t* n_launches, int32_t* gro
 int dustin_score_noalloc(const dustin_params* p, const dustin_signal* draft,
                          const dustin_signal* target, const dustin_srh* srh, int32_t n_srh,
                          const int32_t* seq_len, float* importance, cudaStream_t stream);
+
+/* dustin_check for the static array of dustin_score_noalloc on the current
+ * device: synchronises the stream, returns the error word of every
+ * dustin_score_noalloc call since the last check in *flags (if non-NULL),
+ * clears it, and returns DUSTIN_EDEVICE if it was non-zero.  Allocates
+ * nothing; DUSTIN_ECUDA if a CUDA call fails. */
+int dustin_score_noalloc_check(cudaStream_t stream, int32_t* flags);
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,9 @@ MAX_SRH, MAX_PAIRS, MAX_LAYERS, MAX_QROWS, MAX_LCAP = 32, 32, 16, 128, 1 << 20
 
 EXPORTS = ["dustin_version", "dustin_workspace_bytes", "dustin_workspace_init", "dustin_check",
            "dustin_score", "dustin_select", "dustin_verify_attn", "dense_verify_attn",
-           "dustin_kv_append", "dustin_verify_step", "dustin_step_launches", "dustin_compact_kv"]
+           "dustin_kv_append", "dustin_verify_step", "dustin_step_launches", "dustin_compact_kv",
+           "dustin_score_noalloc", "dustin_score_noalloc_check", "dustin_wait_selftest",
+           "dustin_verify_split"]
 
 
 class DustinError(RuntimeError):
@@ -113,7 +115,10 @@ def lib():
                                         c_void_p, c_size_t, c_void_p]
         L.dustin_score_noalloc.argtypes = [POINTER(CParams), POINTER(CSignal), POINTER(CSignal),
                                            POINTER(CSRH), c_int32, c_void_p, c_void_p, c_void_p]
-        L.dustin_score_noalloc.restype = ctypes.c_int
+        L.dustin_score_noalloc_check.argtypes = [c_void_p, POINTER(c_int32)]
+        L.dustin_verify_split.argtypes = [POINTER(CParams), c_int32, c_int32, c_int32, c_int32,
+                                          c_int32, POINTER(c_int32), POINTER(c_int32)]
+        L.dustin_wait_selftest.argtypes = [ctypes.c_int64, c_void_p, c_void_p, c_size_t, c_void_p]
         for f in EXPORTS[1:]:
             if f != "dustin_workspace_bytes":
                 getattr(L, f).restype = ctypes.c_int
@@ -281,6 +286,48 @@ def dustin_score_noalloc(p: Params, draft: Signal, target: Signal, srh, seq_len:
                                     _ptr(importance, torch.float32), _stream(stream))
     _check("dustin_score_noalloc", st)
     return importance
+
+
+def verify_split(p: Params, hq: int, hkv: int, d: int, n_layers: int = 1, dense: bool = False):
+    """The verification kernel's stream-K split on the current device:
+    (grid, tiles_per_unit); CTA c takes tiles [c*T/grid, (c+1)*T/grid) of the
+    T = B * hkv * n_layers * tiles_per_unit tiles."""
+    grid, tiles = c_int32(0), c_int32(0)
+    st = lib().dustin_verify_split(ctypes.byref(p.c()), hq, hkv, d, n_layers, int(dense),
+                                   ctypes.byref(grid), ctypes.byref(tiles))
+    _check("dustin_verify_split", st)
+    return int(grid.value), int(tiles.value)
+
+
+def split_units(p: Params, hkv: int, n_layers: int, grid: int, tiles_per_unit: int):
+    """Units u whose tiles the split gives to more than one CTA."""
+    total = p.B * hkv * n_layers * tiles_per_unit
+
+    def cta_of(x):   # the CTA c with c*total//grid <= x < (c+1)*total//grid
+        return ((x + 1) * grid + total - 1) // total - 1
+
+    return [u for u in range(p.B * hkv * n_layers)
+            if cta_of(u * tiles_per_unit) != cta_of(u * tiles_per_unit + tiles_per_unit - 1)]
+
+
+def wait_selftest(limit_ns: int, ws: "Workspace", stream=None) -> torch.Tensor:
+    """Runs the bounded-wait self-test; returns the two waiters' times (ns)
+    as a device int64 tensor.  Read the error word with check(ws)."""
+    waited = torch.zeros(2, dtype=torch.int64, device=ws.buf.device)
+    st = lib().dustin_wait_selftest(int(limit_ns), waited.data_ptr(), ws.ptr, ws.nbytes,
+                                    _stream(stream))
+    _check("dustin_wait_selftest", st)
+    return waited
+
+
+def noalloc_check(stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device error flags
+    that dustin_score_noalloc calls raised since the last check."""
+    flags = c_int32(0)
+    st = lib().dustin_score_noalloc_check(_stream(stream), ctypes.byref(flags))
+    if st not in (0, -4):
+        raise DustinError("dustin_score_noalloc_check", st)
+    return int(flags.value)
 
 
 def dustin_select(p: Params, importance: torch.Tensor, seq_len: torch.Tensor,

@@ -686,6 +686,7 @@ int dustin_compact_kv(const dustin_params* p, int32_t n_layers, const dustin_kv*
   if (n_layers < 1) return DUSTIN_EINVAL;
   if (n_layers > DUSTIN_MAX_LAYERS) return DUSTIN_ERANGE;
   if (!k || !v || !kc || !vc || !i_verify || !seq_len || !seq_len_c) return DUSTIN_EINVAL;
+  if (seq_len_c == seq_len) return DUSTIN_EINVAL;
   if (!ws_ok(ws, ws_bytes, kScratch)) return DUSTIN_EWORKSPACE;
   CompactArgs a{};
   a.B = p->B;
@@ -726,6 +727,26 @@ int dustin_step_launches(const dustin_step* s, int32_t* n_launches, int32_t* gro
   // verify + merge
   *n_launches = groups + (groups + kGroupsPerNorm - 1) / kGroupsPerNorm + 3;
   *group_size = pl.nb;
+  return DUSTIN_OK;
+}
+
+int dustin_verify_split(const dustin_params* p, int32_t hq, int32_t hkv, int32_t d,
+                        int32_t n_layers, int32_t dense, int32_t* grid, int32_t* tiles_per_unit) {
+  if (!params_ok(p) || !grid || !tiles_per_unit) return DUSTIN_EINVAL;
+  if (n_layers < 1 || n_layers > DUSTIN_MAX_LAYERS || hkv < 1 || hq < 1 || hq % hkv ||
+      (d != 64 && d != 128))
+    return DUSTIN_EINVAL;
+  if (int64_t(p->gamma + 1) * (hq / hkv) > DUSTIN_MAX_QROWS || p->gamma + 1 > DUSTIN_MAX_BLOCK)
+    return DUSTIN_ERANGE;
+  VerifyShape vs;
+  vs.hq = hq;
+  vs.hkv = hkv;
+  vs.d = d;
+  vs.n_layers = n_layers;
+  const VerifyLaunch pl = plan_verify(p, vs, dense ? 1 : 0);
+  if (pl.units > kVerifyUnitsMax) return DUSTIN_ERANGE;
+  *grid = pl.grid;
+  *tiles_per_unit = pl.tiles_u;
   return DUSTIN_OK;
 }
 
@@ -773,6 +794,17 @@ int dustin_verify_step(const dustin_step* s, void* ws, size_t ws_bytes, cudaStre
   return DUSTIN_OK;
 }
 
+int dustin_wait_selftest(int64_t limit_ns, int64_t* waited_ns, void* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000ll) return DUSTIN_EINVAL;
+  if (!waited_ns || (reinterpret_cast<uintptr_t>(waited_ns) & 7u)) return DUSTIN_EINVAL;
+  if (!ws_ok(ws, ws_bytes, kHeader)) return DUSTIN_EWORKSPACE;
+  return wait_selftest_launch(err_word(ws), reinterpret_cast<long long*>(waited_ns),
+                              static_cast<unsigned long long>(limit_ns), stream) == cudaSuccess
+             ? DUSTIN_OK
+             : DUSTIN_ECUDA;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
@@ -788,8 +820,10 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 // Device address of g_noalloc_scratch on the current device (looked up once
-// per device, with that device current).
-int noalloc_scratch(void** out) {
+// per device, with that device current).  The first lookup on a device also
+// clears the array's error word, on the caller's stream, so the word starts
+// from zero whatever the loader left in the array.
+int noalloc_scratch(void** out, cudaStream_t stream) {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
   int dev = 0;
@@ -798,6 +832,7 @@ int noalloc_scratch(void** out) {
   if (!addr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DUSTIN_ECUDA;
+    if (cudaMemsetAsync(p, 0, kHeader, stream) != cudaSuccess) return DUSTIN_ECUDA;
     addr[dev] = p;
   }
   *out = addr[dev];
@@ -817,8 +852,14 @@ extern "C" int dustin_score_noalloc(const dustin_params* p, const dustin_signal*
   if (!seq_len || !importance || !aligned16(importance)) return DUSTIN_EINVAL;
   if (pl.total > DUSTIN_NOALLOC_SCRATCH_BYTES) return DUSTIN_ERANGE;
   void* ws = nullptr;
-  const int s2 = noalloc_scratch(&ws);
+  const int s2 = noalloc_scratch(&ws, stream);
   if (s2 != DUSTIN_OK) return s2;
-  if (cudaMemsetAsync(ws, 0, kHeader, stream) != cudaSuccess) return DUSTIN_ECUDA;
   return launch_score(p, draft, target, pl, seq_len, importance, ws, stream);
+}
+
+extern "C" int dustin_score_noalloc_check(cudaStream_t stream, int32_t* flags) {
+  void* ws = nullptr;
+  const int st = noalloc_scratch(&ws, stream);
+  if (st != DUSTIN_OK) return st;
+  return dustin_check(ws, stream, flags);
 }

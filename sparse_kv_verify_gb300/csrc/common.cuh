@@ -66,18 +66,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs (sets DUSTIN_DEV_TIMEOUT and, if given, *abort, which makes the
+// limit_ns (sets DUSTIN_DEV_TIMEOUT and, if given, *abort, which makes the
 // CTA's other waits give up too) so that a broken transaction count can never
 // hang the GPU.  Returns false on give-up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
-                                          volatile int* abort) {
+                                          volatile int* abort,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (abort && *abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         flag_error(err, DUSTIN_DEV_TIMEOUT);
         if (abort) *abort = 1;
         return false;

@@ -251,4 +251,8 @@ struct CompactArgs {
 };
 cudaError_t compact_launch(const CompactArgs& a, cudaStream_t stream);
 
+// ------------------------------------------------------------ wait self-test
+cudaError_t wait_selftest_launch(int* err, long long* waited, unsigned long long limit_ns,
+                                 cudaStream_t stream);
+
 }  // namespace dustin

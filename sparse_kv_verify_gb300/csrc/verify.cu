@@ -182,6 +182,9 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
 //   to 8; the next segment's rows load while this one runs), then as many
 //   K/V stages [K panels | V panels] of 64 keys as the rest holds, then the
 //   valid-key masks, the mbarriers and two words (tensor-memory base, abort).
+// Once any wait gives up (DUSTIN_DEV_TIMEOUT) every role stops issuing copies
+// and MMAs; before the CTA exits the loaders still wait for their copies in
+// flight and the MMA thread for its MMAs, so tensor memory is freed idle.
 // The S MMA reads 128 query rows per panel; the rows past q_rows fall on the
 // next buffer or the ring (whatever they hold only reaches S and O rows that
 // are never used: the softmax treats rows >= NQ as empty).
@@ -210,7 +213,7 @@ inline VLay make_lay(int D, int NQ) {
   L.nst = D == 128 ? StagesOf<128>::n : StagesOf<64>::n;
   L.mask_off = L.ring_off + uint32_t(L.nst) * L.stage_bytes;
   L.bar_off = L.mask_off + ((uint32_t(L.nst) * kLoaders + 7u) & ~7u);
-  L.misc_off = L.bar_off + uint32_t(2 * L.nst + 4 + 2 * NQB) * 8;
+  L.misc_off = L.bar_off + uint32_t(2 * L.nst + 4 + 2 * NQB + 1) * 8;
   L.total = L.misc_off + 16 + 1024;
   return L;
 }
@@ -250,6 +253,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
   uint64_t* p_full = s_full + 2;
   uint64_t* q_full = p_full + 2;
   uint64_t* q_empty = q_full + NQB;
+  uint64_t* mma_done = q_empty + NQB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly.misc_off + 8);
 
@@ -270,6 +274,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       mbar_init(&q_full[x], 1);
       mbar_init(&q_empty[x], 1);
     }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -311,7 +316,9 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     const int ksub = lane / CH;
     int gi = 0;
     int s = 0;
-    for (long long t = t0; t < t1; ++s) {
+    int q_end = 0;        // this warp loaded query rows of segments < q_end
+    bool live = true;     // false once a wait gave up
+    for (long long t = t0; t < t1 && live; ++s) {
       const Seg sg = next_seg(t, t1, tiles_u);
       const int layer = sg.u / units_per_layer;
       const int b = (sg.u % units_per_layer) / A.hkv;
@@ -326,15 +333,21 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       // this segment's query rows -> query buffer s % NQB, once the MMAs of the
       // segment that used it last are done
       const int qb = s % NQB;
-      if (s % kLoaders == lw && lane == 0) {
-        if (s >= NQB) mbar_wait(&q_empty[qb], uint32_t(s / NQB - 1) & 1u, A.err, abort_flag);
-        mbar_arrive_expect_tx(&q_full[qb], uint32_t(NQ) * D * 2);
+      if (s % kLoaders == lw) {
+        bool ok = true;
+        if (lane == 0) {
+          if (s >= NQB) ok = mbar_wait(&q_empty[qb], uint32_t(s / NQB - 1) & 1u, A.err, abort_flag);
+          if (ok) {
+            mbar_arrive_expect_tx(&q_full[qb], uint32_t(NQ) * D * 2);
 #pragma unroll
-        for (int h = 0; h < Ly.NP; ++h)
-          tma_load_3d(sbase + uint32_t(qb * Ly.q_buf + h * Ly.q_panel), &A.qmap[layer], h * 64,
-                      g * GQ, b * T, &q_full[qb]);
+            for (int h = 0; h < Ly.NP; ++h)
+              tma_load_3d(sbase + uint32_t(qb * Ly.q_buf + h * Ly.q_panel), &A.qmap[layer], h * 64,
+                          g * GQ, b * T, &q_full[qb]);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, int(ok), 0)) break;
+        q_end = s + 1;
       }
-      __syncwarp();
       const uint16_t* kbase = Lr.k + size_t(b) * Lr.ksb + size_t(g) * Lr.ksh;
       const uint16_t* vbase = Lr.v + size_t(b) * Lr.vsb + size_t(g) * Lr.vsh;
       const size_t blk_off = (size_t(b) * A.hkv + g) * T * D;
@@ -350,8 +363,11 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
           raw = jj < A.k ? __ldg(A.ivf + size_t(b) * A.k + jj) : -1;
         }
         const int st = int(gi % NSTAGE);
-        if (gi >= NSTAGE)
-          mbar_wait(&empty[st], uint32_t(gi / NSTAGE - 1) & 1u, A.err, abort_flag);
+        if (gi >= NSTAGE &&
+            !__all_sync(0xffffffffu, mbar_wait(&empty[st], uint32_t(gi / NSTAGE - 1) & 1u, A.err, abort_flag))) {
+          live = false;
+          break;
+        }
         bool valid;
         if (blk) valid = raw < T;
         else if (A.dense) valid = raw < L;
@@ -383,8 +399,9 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     }
     cp_async_wait_all();
     // the query loads this warp issued have landed before the CTA may exit
+    // (a load older than the last NQB segments was consumed by an MMA)
     if (lane == 0)
-      for (int x = s - NQB < 0 ? 0 : s - NQB; x < s; ++x)
+      for (int x = q_end - NQB < 0 ? 0 : q_end - NQB; x < q_end; ++x)
         if (x % kLoaders == lw) mbar_drain(&q_full[x % NQB], uint32_t(x / NQB) & 1u);
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -396,9 +413,11 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       int gi = 0;
       int s = 0;
       // S = Q K^T of tile g2 into S buffer g2 % 2, once its rows have landed
-      auto issue_s = [&](int g2, uint32_t qbuf) {
+      bool issued = false;
+      auto issue_s = [&](int g2, uint32_t qbuf) -> bool {
         const int st = int(g2 % NSTAGE);
-        mbar_wait(&full[st], uint32_t(g2 / NSTAGE) & 1u, A.err, abort_flag);
+        if (!mbar_wait(&full[st], uint32_t(g2 / NSTAGE) & 1u, A.err, abort_flag)) return false;
+        issued = true;
         fence_proxy_async();   // the rows were written by cp.async (generic proxy)
         tc_fence_after();
         const uint32_t kst = sbase + uint32_t(Ly.ring_off + size_t(st) * Ly.stage_bytes);
@@ -410,16 +429,21 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
           tc_mma_ss(tmem + uint32_t(kSCol + (g2 & 1) * TK), a, bd, kIdS, kk > 0);
         }
         tc_commit(&s_full[g2 & 1]);
+        return true;
       };
-      for (long long t = t0; t < t1; ++s) {
+      bool live = true;   // false once a wait gave up: issue nothing more
+      for (long long t = t0; t < t1 && live; ++s) {
         const Seg sg = next_seg(t, t1, tiles_u);
         const int qb = s % NQB;
         const uint32_t qbuf = sbase + uint32_t(qb * Ly.q_buf);
-        mbar_wait(&q_full[qb], uint32_t(s / NQB) & 1u, A.err, abort_flag);
-        issue_s(gi, qbuf);
+        if (!mbar_wait(&q_full[qb], uint32_t(s / NQB) & 1u, A.err, abort_flag) || !issue_s(gi, qbuf))
+          break;
         for (int i = 0; i < sg.n; ++i, ++gi) {
-          if (i + 1 < sg.n) issue_s(gi + 1, qbuf);
-          mbar_wait(&p_full[gi & 1], uint32_t(gi >> 1) & 1u, A.err, abort_flag);
+          if ((i + 1 < sg.n && !issue_s(gi + 1, qbuf)) ||
+              !mbar_wait(&p_full[gi & 1], uint32_t(gi >> 1) & 1u, A.err, abort_flag)) {
+            live = false;
+            break;
+          }
           tc_fence_after();
           const int st = int(gi % NSTAGE);
           const uint32_t vst =
@@ -432,10 +456,13 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
           }
           tc_commit(&empty[st]);   // P V of tile gi done: its stage is free
         }
-        tc_commit(&q_empty[qb]);
+        if (live) tc_commit(&q_empty[qb]);
       }
-      // every MMA of this CTA has completed
-      if (s > 0) mbar_drain(&q_empty[(s - 1) % NQB], uint32_t((s - 1) / NQB) & 1u);
+      // every MMA this thread issued has completed before tensor memory is freed
+      if (issued) {
+        tc_commit(mma_done);
+        mbar_drain(mma_done, 0);
+      }
     }
     __syncwarp();
   } else if (warp < n_act) {
@@ -447,7 +474,8 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
     const uint32_t o_lane = lane_base + uint32_t(Tm::o_col);
     int gi = 0;
-    for (long long t = t0; t < t1;) {
+    bool live = true;   // false once a wait gave up (warp-uniform)
+    for (long long t = t0; t < t1 && live;) {
       const Seg sg = next_seg(t, t1, tiles_u);
       const int u = sg.u, n = sg.n;
       const int layer = u / units_per_layer;
@@ -457,10 +485,13 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       float mref = -INFINITY, lsum = 0.f;   // reference max (log2 domain) and row sum
       for (int i = 0; i < n; ++i, ++gi) {
         const int st = int(gi % NSTAGE);
-        mbar_wait(&full[st], uint32_t(gi / NSTAGE) & 1u, A.err, abort_flag);
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[st], uint32_t(gi / NSTAGE) & 1u, A.err, abort_flag) &&
+                                         mbar_wait(&s_full[gi & 1], uint32_t(gi >> 1) & 1u, A.err, abort_flag))) {
+          live = false;
+          break;
+        }
         const unsigned long long mw = *reinterpret_cast<const unsigned long long*>(masks + st * kLoaders);
         const bool blk = sg.ta + i >= ctx_tiles;
-        mbar_wait(&s_full[gi & 1], uint32_t(gi >> 1) & 1u, A.err, abort_flag);
         tc_fence_after();
         float s[TK];
         tc_ld32(lane_base + uint32_t(kSCol + (gi & 1) * TK), reinterpret_cast<uint32_t*>(s));
@@ -505,7 +536,11 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
         // first tile of a segment overwrites O); tensor-memory loads and
         // stores are collective, so the whole warp takes part
         if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          mbar_wait(&empty[(gi - 1) % NSTAGE], uint32_t((gi - 1) / NSTAGE) & 1u, A.err, abort_flag);
+          if (!__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 1) % NSTAGE], uint32_t((gi - 1) / NSTAGE) & 1u,
+                                                 A.err, abort_flag))) {
+            live = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
@@ -521,6 +556,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
         mbar_arrive(&p_full[gi & 1]);
       }
 
+      if (!live) break;
       // ----------------------------------------------------------- epilogue
       const int seg_first = cta_of((long long)u * tiles_u, total, G);
       const int seg_last = cta_of((long long)u * tiles_u + tiles_u - 1, total, G);
@@ -528,8 +564,10 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       const int seg = blockIdx.x - seg_first;
       const size_t slot_floats = size_t(A.slot_floats);   // NQ*D + 2*NQ, rounded to 4
       float* part = A.partial + (size_t(u) * A.max_seg + seg) * slot_floats;
-      {
-        mbar_wait(&empty[(gi - 1) % NSTAGE], uint32_t((gi - 1) / NSTAGE) & 1u, A.err, abort_flag);
+      if (!__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 1) % NSTAGE], uint32_t((gi - 1) / NSTAGE) & 1u,
+                                             A.err, abort_flag))) {
+        live = false;
+      } else {
         tc_fence_after();
         const int tq = active ? row / GQ : 0, hl = active ? row - (row / GQ) * GQ : 0;
         float* dst = n_seg == 1 ? Lr.o + ((size_t(b) * T + tq) * A.hq + size_t(g) * GQ + hl) * D

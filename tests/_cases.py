@@ -108,3 +108,16 @@ def assert_select_near(I_gpu, imp_ref, seq_len, k, sinks, window, m):
 
 def flags_ok(ws):
     return dk.check(ws) == 0
+
+
+def sampled_units(p, wl, n_layers=1, dense=False):
+    """(layer, sequence, KV head) triples to check at full size: the first,
+    middle and last of the units the verification kernel's stream-K split
+    cuts across CTAs (their outputs come from the merge kernel), plus the
+    first and last unit.  Unit u = (layer * B + b) * Hkv + g."""
+    grid, tiles = dk.verify_split(p, wl.Hq, wl.Hkv, wl.d, n_layers, dense)
+    cut = dk.split_units(p, wl.Hkv, n_layers, grid, tiles)
+    assert len(cut) >= 2, (grid, tiles)
+    n_units = n_layers * p.B * wl.Hkv
+    us = sorted({cut[0], cut[len(cut) // 2], cut[-1], 0, n_units - 1})
+    return [(u // (p.B * wl.Hkv), (u // wl.Hkv) % p.B, u % wl.Hkv) for u in us]

@@ -156,6 +156,53 @@ def test_invalid_append_arguments_rejected(L):
     assert lib.dustin_kv_append(ctypes.byref(p), 2, k, k, kb_bad, kb, 0x1000, 0x2000, ws, 1 << 20, None) == -1
 
 
+def test_compact_refuses_seq_len_c_aliasing_seq_len(L):
+    """seq_len_c is written while other CTAs still read seq_len, so the two
+    may not be one array; the refusal comes before any launch."""
+    from sparse_kv_verify_gb300 import binding as bd
+    lib = L.lib()
+    p = bd.CParams(2, 1024, 4, 4, 32, 32, 128)
+    kv = (bd.CKV * 1)(bd.CKV(0x10000, 8, 128, 8 * 1024 * 128, 1024 * 128, 128))
+    kc = (bd.CKV * 1)(bd.CKV(0x20000, 8, 128, 8 * 128 * 128, 128 * 128, 128))
+    ws = 0x100000
+    assert lib.dustin_compact_kv(ctypes.byref(p), 1, kv, kv, 0x1000, 0x2000, kc, kc, 0x2000,
+                                 ws, 1 << 20, None) == -1
+    assert lib.dustin_compact_kv(ctypes.byref(p), 1, kv, kv, 0x1000, 0x2000, kc, kc, None,
+                                 ws, 1 << 20, None) == -1
+    assert lib.dustin_compact_kv(ctypes.byref(p), 1, kv, kv, 0x1000, 0x2000, kc, kc, 0x3000,
+                                 None, 1 << 20, None) == -5
+
+
+def test_wait_selftest_argument_checks(L):
+    """The wait limit must lie in [1 us, 1 s]; the output must be a non-null
+    8-byte-aligned device pointer; the workspace needs its header."""
+    lib = L.lib()
+    ws = 0x100000
+    assert lib.dustin_wait_selftest(999, 0x2000, ws, 256, None) == -1
+    assert lib.dustin_wait_selftest(1000000001, 0x2000, ws, 256, None) == -1
+    assert lib.dustin_wait_selftest(1000000, None, ws, 256, None) == -1
+    assert lib.dustin_wait_selftest(1000000, 0x2004, ws, 256, None) == -1
+    assert lib.dustin_wait_selftest(1000000, 0x2000, None, 256, None) == -5
+    assert lib.dustin_wait_selftest(1000000, 0x2000, ws, 128, None) == -5
+
+
+def test_split_units_matches_brute_force(L):
+    """The host's list of units that the verification split cuts across CTAs
+    equals a brute-force assignment of every tile to its CTA."""
+    from sparse_kv_verify_gb300 import binding as bd
+    for (B, hkv, nl, G, tu) in [(2, 8, 1, 152, 33), (16, 8, 1, 152, 33), (1, 1, 1, 5, 7),
+                                (3, 2, 2, 5, 4), (4, 8, 8, 152, 65)]:
+        p = bd.Params(B, 1024, 4, 4, 32, 32, 128)
+        T = B * hkv * nl * tu
+        owner = [0] * T
+        for c in range(G):
+            for t in range(c * T // G, (c + 1) * T // G):
+                owner[t] = c
+        brute = [u for u in range(B * hkv * nl)
+                 if len({owner[t] for t in range(u * tu, (u + 1) * tu)}) > 1]
+        assert bd.split_units(p, hkv, nl, G, tu) == brute
+
+
 def test_step_rejects_null_and_too_many_layers(L):
     from sparse_kv_verify_gb300 import binding as bd
     lib = L.lib()

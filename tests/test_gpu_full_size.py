@@ -6,7 +6,9 @@ and the attention-recovery report of the policies.
 
 Outputs are checked on samples the oracle computes one by one: the importance
 of one sequence in full, the selection of every sequence (bit-exact on the
-GPU's own scores), attention of sampled (sequence, layer, KV head) triples.
+GPU's own scores), attention of sampled (sequence, layer, KV head) triples,
+among them units that the verification kernel's stream-K split cuts across
+CTAs.
 Host copies are limited to the sampled slices."""
 from __future__ import annotations
 
@@ -18,7 +20,7 @@ import sparse_kv_verify_gb300 as dk
 from oracle import dustin_oracle as O
 from synth import WORKLOADS, generate, random_importance, sweep_points, to_bits
 
-from _cases import assert_attention, assert_importance, params_of
+from _cases import assert_attention, assert_importance, params_of, sampled_units
 
 pytestmark = pytest.mark.gpu
 
@@ -56,7 +58,8 @@ def test_sweep_full_size_sampled(k, gamma):
     assert_importance(imp_np[b:b + 1], _score_one(x, wl, b, {0}), x.seq_len[b:b + 1])
     I_ref, _ = O.select(imp_np, x.seq_len, wl.k, wl.sinks, wl.window, wl.m)
     assert np.array_equal(I.cpu().numpy(), I_ref)
-    for (bb, g) in [(b, k // 512 % wl.Hkv), (wl.B - 1, wl.Hkv - 1)]:
+    units = {(b, k // 512 % wl.Hkv)} | {(bb, g) for (_, bb, g) in sampled_units(p, wl)}
+    for (bb, g) in sorted(units):
         ref, hs = _verify_one(x, wl, I_ref, bb, 0, g)
         assert_attention(outs[0][bb:bb + 1, :, hs], ref)
 
@@ -85,7 +88,8 @@ def test_stack_full_size_step_and_append(stack):
     assert_importance(imp_np[:1], _score_one(x, wl, 0, srh_layers), x.seq_len[:1])
     I_ref, _ = O.select(imp_np, x.seq_len, wl.k, wl.sinks, wl.window, wl.m)
     assert np.array_equal(I.cpu().numpy(), I_ref)
-    for (b, l, g) in [(0, 0, 0), (1, 4, 3), (wl.B - 1, wl.n_layers - 1, wl.Hkv - 1)]:
+    units = {(1, 4, 3)} | {(b, l, g) for (l, b, g) in sampled_units(p, wl, wl.n_layers)}
+    for (b, l, g) in sorted(units):
         ref, hs = _verify_one(x, wl, I_ref, b, l, g)
         assert_attention(outs[l][b:b + 1, :, hs], ref)
 

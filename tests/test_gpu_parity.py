@@ -18,7 +18,7 @@ from oracle import dustin_oracle as O  # noqa: E402
 from synth import WORKLOADS, random_importance, to_bits  # noqa: E402
 
 from _cases import (Case, params_of, assert_importance, assert_attention,  # noqa: E402
-                    assert_select_near)
+                    assert_select_near, sampled_units)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -265,6 +265,45 @@ def test_verify_ragged_lengths():
     assert_attention(od, c.oracle_dense())
 
 
+def test_empty_and_one_position_sequences():
+    """seq_len[b] = 0 and 1 beside ordinary lengths, through scoring,
+    selection, sparse and dense verification and the fused step, against the
+    oracle.  An empty context scores 0 everywhere, selects nothing (all -1)
+    and its queries attend to the draft block alone; a one-position context
+    gives that position the number of (SRH head, query row) pairs of each
+    channel (each softmax over one position is 1)."""
+    wl = WORKLOADS["tiny"].with_(B=4)
+    c = Case(wl, seq_len=[0, 1, 1024, 2])
+    x = c.x
+    ws = dk.workspace(c.p, c.draft, c.target, wl.srh, verify=(wl.Hq, wl.Hkv, wl.d, 1))
+    imp = dk.dustin_score(c.p, c.draft, c.target, wl.srh, c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    assert_importance(imp, c.oracle_score(), x.seq_len)
+    imp_np = imp.double().cpu().numpy()
+    n_draft = sum(wl.gamma for e in wl.srh if e[0] == 0)
+    n_target = sum(wl.gamma + 1 for e in wl.srh if e[0] == 1)
+    assert np.all(imp_np[0] == 0.0)
+    assert np.allclose(imp_np[1, :, 0], [n_draft, n_target], rtol=1e-6, atol=0)
+    I = dk.dustin_select(c.p, imp, c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    I_ref, _ = O.select(imp_np, x.seq_len, wl.k, wl.sinks, wl.window, wl.m)
+    I_np = I.cpu().numpy()
+    assert np.array_equal(I_np, I_ref)
+    assert np.all(I_np[0] == -1) and I_np[1, 0] == 0 and np.all(I_np[1, 1:] == -1)
+    o = dk.dustin_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], I, c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    assert_attention(o, c.oracle_verify(I_ref))
+    od = dk.dense_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    assert_attention(od, c.oracle_dense())
+    layer = dk.VerifyLayer(x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0])
+    call = dk.StepCall(c.p, c.draft, c.target, wl.srh, [layer], c.seq)
+    imp2, I2, outs = call()
+    assert dk.check(call.ws) == 0
+    assert torch.equal(imp2, imp) and torch.equal(I2, I)
+    assert_attention(outs[0], c.oracle_verify(I_ref))
+
+
 # ------------------------------------------------------------------ append
 
 
@@ -349,7 +388,7 @@ def test_full_size_step_sampled(big):
     assert np.array_equal(I_np, I_ref)
     G = wl.Hq // wl.Hkv
     o = outs[0]
-    for (b, g) in [(0, 0), (5, 3), (wl.B - 1, wl.Hkv - 1)]:
+    for (_, b, g) in sampled_units(c.p, wl, dense=False):
         hs = slice(g * G, (g + 1) * G)
         ref = O.verify(to_bits(x.Q[0][b:b + 1, :, hs]), to_bits(x.K[0][b:b + 1, g:g + 1]),
                        to_bits(x.V[0][b:b + 1, g:g + 1]), to_bits(x.Kb[0][b:b + 1, g:g + 1]),
@@ -363,7 +402,7 @@ def test_full_size_dense_sampled(big):
     wl, x = c.wl, c.x
     o = dk.dense_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], c.seq)
     G = wl.Hq // wl.Hkv
-    for (b, g) in [(0, 0), (wl.B - 1, 5)]:
+    for (_, b, g) in sampled_units(c.p, wl, dense=True):
         hs = slice(g * G, (g + 1) * G)
         ref = O.dense(to_bits(x.Q[0][b:b + 1, :, hs]), to_bits(x.K[0][b:b + 1, g:g + 1]),
                       to_bits(x.V[0][b:b + 1, g:g + 1]), to_bits(x.Kb[0][b:b + 1, g:g + 1]),
@@ -374,8 +413,10 @@ def test_full_size_dense_sampled(big):
 @pytest.mark.parametrize("name,over", [("layer8k", {}), ("tiny", dict(k=1100, n_layers=2))])
 def test_compact_kv_then_dense_equals_sparse_verify(name, over):
     """The compacted-cache variant: the selected rows copied into compact
-    caches and verified densely give bit-for-bit the sparse verification of
-    the full caches (same keys in the same order), in every layer."""
+    caches and verified densely match the oracle's sparse verification, and
+    bit-for-bit the CUDA sparse verification of the full caches (same keys in
+    the same order), in every layer; every (sequence, KV head) pair's K and V
+    rows equal a gather of the full caches, zero past the compact length."""
     c = Case(WORKLOADS[name].with_(**over))
     wl, x = c.wl, c.x
     I_ref, _ = O.select(c.oracle_score(), x.seq_len, wl.k, wl.sinks, wl.window, wl.m)
@@ -389,8 +430,11 @@ def test_compact_kv_then_dense_equals_sparse_verify(name, over):
     for l in range(wl.n_layers):
         o_sparse = dk.dustin_verify_attn(c.p, x.Q[l], x.K[l], x.V[l], x.Kb[l], x.Vb[l], I, c.seq)
         o_dense = dk.dense_verify_attn(pc, x.Q[l], kcs[l], vcs[l], x.Kb[l], x.Vb[l], slc)
+        assert_attention(o_dense, c.oracle_verify(I_ref, layer=l))
         assert torch.equal(o_sparse, o_dense)
-        b, g = 0, x.K[l].shape[1] - 1
-        rows = I_ref[b][: valid[b]]
-        assert torch.equal(kcs[l][b, g, : valid[b]], x.K[l][b, g, torch.as_tensor(rows, device="cuda")])
-        assert torch.all(kcs[l][b, g, valid[b]:] == 0)
+        for b in range(wl.B):
+            rows = torch.as_tensor(I_ref[b][: valid[b]], device="cuda")
+            for g in range(x.K[l].shape[1]):
+                for full, comp in ((x.K[l], kcs[l]), (x.V[l], vcs[l])):
+                    assert torch.equal(comp[b, g, : valid[b]], full[b, g, rows]), (l, b, g)
+                    assert torch.all(comp[b, g, valid[b]:wl.k] == 0), (l, b, g)

@@ -47,6 +47,15 @@ MUTATIONS = [
     ("dense drops last context row", "return _attend(Q, K, V, Kb, Vb, lambda b: np.arange(int(seq_len[b])))",
      "return _attend(Q, K, V, Kb, Vb, lambda b: np.arange(int(seq_len[b]) - 1))",
      [P.test_verify_full_budget_equals_dense, P.test_dense_matches_torch_sdpa]),
+    ("recovery reads the other KV head", "keys = bf16(K[b, kv_group(h, hq, hkv), :L, :])",
+     "keys = bf16(K[b, hkv - 1 - kv_group(h, hq, hkv), :L, :])",
+     [P.test_attention_recovery_golden_two_heads]),
+    ("recovery without 1/sqrt(d)", "p = softmax(keys @ bf16(Q[b, t, h, :]) / math.sqrt(d))",
+     "p = softmax(keys @ bf16(Q[b, t, h, :]))", [P.test_attention_recovery_golden_two_heads]),
+    ("recovery past seq_len", "keys = bf16(K[b, kv_group(h, hq, hkv), :L, :])",
+     "keys = bf16(K[b, kv_group(h, hq, hkv), :, :])", [P.test_attention_recovery_golden_two_heads]),
+    ("recovery averaged over heads only", "arr[b] = tot / (hq * T)", "arr[b] = tot / hq",
+     [P.test_attention_recovery_golden_two_heads]),
     ("append shifted", "K2[b, :, L:L + n, :] = Kb[b, :, :n, :]",
      "K2[b, :, L + 1:L + n + 1, :] = Kb[b, :, :n, :]", [P.test_kv_append_exact_copy]),
 ]

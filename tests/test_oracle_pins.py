@@ -353,6 +353,20 @@ def test_attention_recovery_bounds():
     assert O.attention_recovery(Q, K, np.full((1, 3), -1), sl)[0] == 0.0
 
 
+def test_attention_recovery_golden_two_heads():
+    """Hand-derived recovery rates (tests/golden/arr_two_heads.json): the
+    per-head KV mapping, the 1/sqrt(d) scale, the seq_len cut and the mean
+    over heads and queries each change the value if wrong."""
+    g = load("arr_two_heads.json")
+    Q = bits(np.array(g["q"])[None])            # [1][T=2][hq=2][d]
+    K = bits(np.array(g["k"])[None])            # [1][hkv=2][3][d]
+    sl = np.array([g["seq_len"]], np.int32)
+    e = g["expected"]
+    for key, sel in (("sel_1", [1]), ("sel_0", [0, -1]), ("sel_0_1", [0, 1]), ("sel_none", [-1])):
+        got = O.attention_recovery(Q, K, np.array([sel]), sl)[0]
+        assert got == pytest.approx(e[key], rel=1e-14, abs=1e-16), key
+
+
 def test_planted_positions_are_recovered_on_tiny():
     """End-to-end sanity on the tiny workload: planted salient positions end up
     in I_verify (a sanity signal of the input recipe, not a parity pin)."""
