@@ -57,8 +57,9 @@ def assert_importance(got, ref, seq_len):
     got = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else got
     for b, L in enumerate(seq_len):
         g, r = got[b, :, :L], ref[b, :, :L]
-        rel = np.abs(g - r) / np.maximum(np.abs(r), IMP_FLOOR)
-        assert rel.max() <= IMP_RTOL, f"b={b}: max rel err {rel.max():.3e}"
+        if L > 0:
+            rel = np.abs(g - r) / np.maximum(np.abs(r), IMP_FLOOR)
+            assert rel.max() <= IMP_RTOL, f"b={b}: max rel err {rel.max():.3e}"
         assert np.all(got[b, :, L:] == 0.0)
 
 
