@@ -412,6 +412,29 @@ def dustin_kv_append(p: Params, ks, vs, kbs, vbs, n_accept, seq_len, ws=None, st
     _check("dustin_kv_append", st)
 
 
+class AppendCall:
+    """Pre-marshalled arguments of dustin_kv_append, reusable across calls
+    (the tensors it points to must stay alive and in place)."""
+
+    def __init__(self, p: Params, ks, vs, kbs, vbs, n_accept, seq_len, ws=None, stream=None):
+        n = len(ks)
+        self._p = p.c()
+        self._n = n
+        self._k = (CKV * n)(*[kv_view(t) for t in ks])
+        self._v = (CKV * n)(*[kv_view(t) for t in vs])
+        self._kb = (c_void_p * n)(*[_ptr(t, torch.bfloat16) for t in kbs])
+        self._vb = (c_void_p * n)(*[_ptr(t, torch.bfloat16) for t in vbs])
+        self._acc = _ptr(n_accept, torch.int32)
+        self._seq = _ptr(seq_len, torch.int32)
+        self.ws = ws if ws is not None else workspace(p, device=seq_len.device, stream=stream)
+
+    def __call__(self, stream=None):
+        st = lib().dustin_kv_append(ctypes.byref(self._p), self._n, self._k, self._v, self._kb,
+                                    self._vb, self._acc, self._seq, self.ws.ptr, self.ws.nbytes,
+                                    _stream(stream))
+        _check("dustin_kv_append", st)
+
+
 @dataclass
 class VerifyLayer:
     q: torch.Tensor
