@@ -33,6 +33,14 @@
 //            one ordered compaction of the list writes the tier; target tier
 //            -- the same over the target list minus the draft tier, with the
 //            target histogram corrected by the draft tier's target keys.
+// When the level-1 histograms show that the lists of whole threshold bins
+// would not fit rank 0's buffer (long sequences, large budgets), the list
+// thresholds are first narrowed by the next 10 key bits: every CTA
+// histograms those bits of its keys in the two threshold bins, rank 0 adds
+// the CTAs' histograms through distributed shared memory and finds the
+// sub-bins holding the m1-th draft and (m1 + f)-th target keys, and every CTA
+// then lists only the keys at or above those sub-bins.  The finish is
+// unchanged: it only needs every key at or above the tier's exact threshold.
 // If a list outgrows its buffer (heavy ties) or the draft tier is larger than
 // the on-chip copy of it, rank 0 selects that sequence with the general path:
 // candidates of the threshold bin in a shared list (or, past its capacity,
@@ -80,6 +88,7 @@ struct SelShared {
       uint32_t key[kCandCap];
       int pos[kCandCap];
     } c;
+    int r2[2][kBins2];       // list refinement: next 10 bits of the threshold bins
   } u;
   // rank 0: the gathered lists, draft entries [0, n0) then target [n0, n0 + n1)
   uint32_t ekey[kFinCap];
@@ -92,6 +101,7 @@ struct SelShared {
   int wgt[kWarps], weq[kWarps];   // per warp: keys above / equal to T
   int gtb[kWarps], eqb[kWarps];   // exclusive prefixes of wgt, weq
   int ncand, bin, need, found, overflow;
+  uint32_t thr[2];           // rank 0: refined list thresholds (keys) of both channels
 };
 
 // ------------------------------------------------------------------ helpers
@@ -497,21 +507,31 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   if (tid == 0) sh.overflow = 0;
   __syncthreads();
   uint32_t b0 = 0xFFFFFFFFu, b1 = 0xFFFFFFFFu;   // no key reaches these bins
-  int need0 = 0;
+  int need0 = 0, need1 = 0;
+  long long est = 0;   // entries of the lists of whole threshold bins
   if (m1 > 0) {
     find_bin(sh, sh.h[0], kBins1, m1);
     if (sh.found) {
       b0 = uint32_t(sh.bin);
       need0 = sh.need;
+      est += m1 - need0 + sh.h[0][b0];
     } else if (tid == 0) {
       sh.overflow = 1;
     }
   }
   if (f > 0) {
     find_bin(sh, sh.h[1], kBins1, m1 + f);
-    if (sh.found) b1 = uint32_t(sh.bin);
-    else if (tid == 0) sh.overflow = 1;
+    if (sh.found) {
+      b1 = uint32_t(sh.bin);
+      need1 = sh.need;
+      est += m1 + f - need1 + sh.h[1][b1];
+    } else if (tid == 0) {
+      sh.overflow = 1;
+    }
   }
+  // list thresholds as keys (0xFFFFFFFF: nothing listed)
+  uint32_t t0 = b0 == 0xFFFFFFFFu ? 0xFFFFFFFFu : b0 << 20;
+  uint32_t t1 = b1 == 0xFFFFFFFFu ? 0xFFFFFFFFu : b1 << 20;
 
   // ---- scan: this CTA's run of U, whole 128-position rows per warp
   const int a0 = s_eff & ~127;
@@ -521,45 +541,97 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   const int x0 = c0 + warp * wspan, x1 = min(x0 + wspan, c1);
   const float* row0 = A.imp + (size_t(b) * 2 + 0) * A.Lcap;
   const float* row1 = A.imp + (size_t(b) * 2 + 1) * A.Lcap;
-  int n0 = 0, n1 = 0;   // list entries of this warp (warp-uniform)
   bool bad = false;
-  for (int gb = x0; gb < x1; gb += 128) {
-    const int i0 = gb + 4 * lane;
-    float v[2][4];
+  // f(i0, kv): every 128-position row of this warp's run, lane holding keys
+  // i0 .. i0 + 3 of both channels (0 outside U or past the run)
+  auto for_rows4 = [&](auto f) {
+    for (int gb = x0; gb < x1; gb += 128) {
+      const int i0 = gb + 4 * lane;
+      float v[2][4];
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const float* row = c ? row1 : row0;
-      if (A.vec4) {
-        const float4 x = i0 < x1 ? __ldg(reinterpret_cast<const float4*>(row + i0)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[c][0] = x.x;
-        v[c][1] = x.y;
-        v[c][2] = x.z;
-        v[c][3] = x.w;
-      } else {
+      for (int c = 0; c < 2; ++c) {
+        const float* row = c ? row1 : row0;
+        if (A.vec4) {
+          const float4 x = i0 < x1 ? __ldg(reinterpret_cast<const float4*>(row + i0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[c][0] = x.x;
+          v[c][1] = x.y;
+          v[c][2] = x.z;
+          v[c][3] = x.w;
+        } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[c][e] = i0 + e < x1 ? __ldg(row + i0 + e) : 0.f;
+          for (int e = 0; e < 4; ++e) v[c][e] = i0 + e < x1 ? __ldg(row + i0 + e) : 0.f;
+        }
+      }
+      uint32_t kv[2][4];
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = i0 + e;
+          const bool ok = i >= s_eff && i < x1;
+          const uint32_t bits = __float_as_uint(v[c][e]);
+          bad |= ok && bits > 0x7F800000u && bits != 0x80000000u;
+          kv[c][e] = (ok && bits <= 0x7F800000u) ? bits : 0u;   // importance_key; flag raised once below
+        }
+      f(i0, kv);
+    }
+  };
+
+  // ---- narrower list thresholds when whole bins would not fit (see above)
+  if (est > kFinCap) {
+    for (int j = tid; j < 2 * kBins2; j += kThreads) (&sh.u.r2[0][0])[j] = 0;
+    __syncthreads();
+    for_rows4([&](int, const uint32_t (&kv)[2][4]) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t bb = c ? b1 : b0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          hist_add(sh.u.r2[c], (kv[c][e] >> 10) & 1023u, select_bin(kv[c][e]) == bb && kv[c][e] != 0u,
+                   lane);
+      }
+    });
+    cluster.sync();   // every rank's sub-bin histograms are complete
+    if (r == 0) {
+      int* sum = reinterpret_cast<int*>(sh.ekey);   // [2][kBins2], free until the hand-off
+      for (int j = tid; j < 2 * kBins2; j += kThreads) {
+        int acc = 0;
+        for (int rr = 0; rr < CS; ++rr) acc += (&cluster.map_shared_rank(&sh, rr)->u.r2[0][0])[j];
+        sum[j] = acc;
+      }
+      __syncthreads();
+      uint32_t thr0 = t0, thr1 = t1;
+      if (b0 != 0xFFFFFFFFu) {
+        find_bin(sh, sum, kBins2, need0);
+        if (sh.found) thr0 = (b0 << 20) | (uint32_t(sh.bin) << 10);
+      }
+      if (b1 != 0xFFFFFFFFu) {
+        find_bin(sh, sum + kBins2, kBins2, need1);
+        if (sh.found) thr1 = (b1 << 20) | (uint32_t(sh.bin) << 10);
+      }
+      if (tid == 0) {
+        sh.thr[0] = thr0;
+        sh.thr[1] = thr1;
       }
     }
-    uint32_t kv[2][4];
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = i0 + e;
-        const bool ok = i >= s_eff && i < x1;
-        const uint32_t bits = __float_as_uint(v[c][e]);
-        bad |= ok && bits > 0x7F800000u && bits != 0x80000000u;
-        kv[c][e] = (ok && bits <= 0x7F800000u) ? bits : 0u;   // importance_key; flag raised once below
-      }
+    cluster.sync();   // rank 0's thresholds are set; every histogram has been read
+    const SelShared* r0 = cluster.map_shared_rank(&sh, 0);
+    t0 = r0->thr[0];
+    t1 = r0->thr[1];
+  }
+
+  // ---- scan: the lists
+  int n0 = 0, n1 = 0;   // list entries of this warp (warp-uniform)
+  for_rows4([&](int i0, const uint32_t (&kv)[2][4]) {
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      const uint32_t thr = c ? b1 : b0;
+      const uint32_t thr = c ? t1 : t0;
       uint32_t m[4];
       int before = 0, total = 0;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const bool ok = i0 + e >= s_eff && i0 + e < x1;
-        m[e] = __ballot_sync(0xffffffffu, ok && select_bin(kv[c][e]) >= thr);
+        m[e] = __ballot_sync(0xffffffffu, ok && kv[c][e] >= thr);
         before += __popc(m[e] & lt);
         total += __popc(m[e]);
       }
@@ -584,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
       }
       n += total;
     }
-  }
+  });
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(A.err, DUSTIN_DEV_NAN);
   if (lane == 0) {
     sh.lcnt[0][warp] = n0;

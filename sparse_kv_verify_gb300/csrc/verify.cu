@@ -168,11 +168,14 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __device__ __forceinline__ uint32_t swz(int r, int c) { return uint32_t(r) * 128u + (uint32_t(c ^ (r & 7)) << 4); }
 
 // Bounded wait that ignores the abort flag (drains copies in flight before
-// the CTA exits).
-__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+// the CTA exits); giving up sets DUSTIN_DEV_TIMEOUT.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, int* err) {
   const unsigned long long t0 = globaltimer();
   while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > kWaitLimitNs) return;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      flag_error(err, DUSTIN_DEV_TIMEOUT);
+      return;
+    }
 }
 
 
@@ -256,6 +259,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
   uint64_t* mma_done = q_empty + NQB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly.misc_off + 8);
+  int* q_hi = reinterpret_cast<int*>(smem + Ly.misc_off + 12);   // query loads issued: [0, q_hi)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -276,6 +280,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
+    *q_hi = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -316,7 +321,6 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     const int ksub = lane / CH;
     int gi = 0;
     int s = 0;
-    int q_end = 0;        // this warp loaded query rows of segments < q_end
     bool live = true;     // false once a wait gave up
     for (long long t = t0; t < t1 && live; ++s) {
       const Seg sg = next_seg(t, t1, tiles_u);
@@ -343,10 +347,10 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
             for (int h = 0; h < Ly.NP; ++h)
               tma_load_3d(sbase + uint32_t(qb * Ly.q_buf + h * Ly.q_panel), &A.qmap[layer], h * 64,
                           g * GQ, b * T, &q_full[qb]);
+            atomicMax(q_hi, s + 1);
           }
         }
         if (!__shfl_sync(0xffffffffu, int(ok), 0)) break;
-        q_end = s + 1;
       }
       const uint16_t* kbase = Lr.k + size_t(b) * Lr.ksb + size_t(g) * Lr.ksh;
       const uint16_t* vbase = Lr.v + size_t(b) * Lr.vsb + size_t(g) * Lr.vsh;
@@ -398,11 +402,6 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       }
     }
     cp_async_wait_all();
-    // the query loads this warp issued have landed before the CTA may exit
-    // (a load older than the last NQB segments was consumed by an MMA)
-    if (lane == 0)
-      for (int x = q_end - NQB < 0 ? 0 : q_end - NQB; x < q_end; ++x)
-        if (x % kLoaders == lw) mbar_drain(&q_full[x % NQB], uint32_t(x / NQB) & 1u);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // =================================================================== MMA
@@ -461,7 +460,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       // every MMA this thread issued has completed before tensor memory is freed
       if (issued) {
         tc_commit(mma_done);
-        mbar_drain(mma_done, 0);
+        mbar_drain(mma_done, 0, A.err);
       }
     }
     __syncwarp();
@@ -594,6 +593,15 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     }
   }
 
+  // Every query load has been issued: the last NQB of them (each the latest
+  // phase of its buffer) have landed before the CTA exits.  Older ones were
+  // waited for by the MMA thread before the buffer was reloaded.
+  __syncthreads();
+  if (warp == kLoaderWarp0 && lane == 0) {
+    const int hi = *q_hi;
+    for (int x = hi - NQB < 0 ? 0 : hi - NQB; x < hi; ++x)
+      mbar_drain(&q_full[x % NQB], uint32_t(x / NQB) & 1u, A.err);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

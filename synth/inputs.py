@@ -303,14 +303,17 @@ def _fill_slack(cache, L: int, how: str):
         raise ValueError(how)
 
 
-def random_importance(seed: int, B: int, Lcap: int, ties: bool = False) -> np.ndarray:
+def random_importance(seed: int, B: int, Lcap: int, ties: bool = False,
+                      spread: float = 3.0) -> np.ndarray:
     """fp32 importance maps [B][2][Lcap] for selection-only tests.
 
-    Values are exponentials of N(0, 3) (positive, wide dynamic range); with
-    ``ties`` they are quantised to 16 levels so that many keys are equal.
+    Values are exponentials of N(0, spread) (positive; the default spread
+    gives a wide dynamic range, a small one packs most values into a few
+    binary orders of magnitude, so that the top bits of many keys agree);
+    with ``ties`` they are quantised to 16 levels so that many keys are equal.
     """
     g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 77])))
-    x = np.exp(3.0 * g.standard_normal((B, 2, Lcap))).astype(np.float32)
+    x = np.exp(spread * g.standard_normal((B, 2, Lcap))).astype(np.float32)
     if ties:
         x = (np.floor(x.clip(0, 15.999)) + 1.0).astype(np.float32) / 16.0
     return x

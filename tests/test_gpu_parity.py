@@ -93,6 +93,28 @@ def test_select_bit_exact_on_identical_keys(ties, L, k, s, w, m):
     assert np.array_equal(I.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("spread", [0.1, 0.02, 0.0003])
+@pytest.mark.parametrize("B,L,k,s,w,m", [(2, 131072, 4096, 16, 512, 1024),
+                                          (16, 32768, 2048, 16, 256, 512),
+                                          (1, 20000, 3000, 8, 64, 700)])
+def test_select_narrow_keys(spread, B, L, k, s, w, m):
+    """Keys packed into a narrow range: the 12-bit threshold bins hold tens of
+    thousands of keys, so the candidate lists are first narrowed by the next
+    10 key bits across the cluster (spreads 0.1 and 0.02), or, when even
+    those sub-bins are too full (0.0003), the general path runs; every case
+    is exact."""
+    Lcap = L + 64
+    keys = random_importance(int(spread * 1e4) + B, B, Lcap, spread=spread)
+    seq = np.array([L - 37 * b for b in range(B)], dtype=np.int32)
+    p = dk.Params(B, Lcap, 4, s, w, m, k)
+    ws = dk.workspace(p)
+    I = dk.dustin_select(p, torch.as_tensor(keys, device="cuda"), torch.as_tensor(seq, device="cuda"),
+                         ws=ws)
+    assert dk.check(ws) == 0
+    ref, _ = O.select(keys.astype(np.float64), seq, k, s, w, m)
+    assert np.array_equal(I.cpu().numpy(), ref)
+
+
 def test_select_long_cache_global_keys():
     """Caches too long to stage keys on chip select from global memory."""
     B, L, k = 2, 131072, 4096
@@ -229,6 +251,32 @@ def test_verify_full_budget_matches_dense():
     o_d = dk.dense_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], c.seq)
     assert torch.allclose(o_s, o_d, atol=2e-6, rtol=0)
     assert_attention(o_d, c.oracle_dense())
+
+
+def test_verify_many_segments_per_cta():
+    """Short units (two tiles) and many of them: every CTA of the stream-K
+    split runs several units in turn and reloads both query buffers; the
+    kernels end cleanly (no wait gives up) and match the oracle."""
+    wl = WORKLOADS["tiny"].with_(B=32, Hq=16, Hkv=8, L=512, k=64, sinks=4, window=16, m=16,
+                                 n_planted=4)
+    c = Case(wl)
+    x = c.x
+    for dense in (False, True):
+        grid, tiles = dk.verify_split(c.p, wl.Hq, wl.Hkv, wl.d, 1, dense)
+        T = wl.B * wl.Hkv * tiles
+        segs = max(len({t // tiles for t in range(cta * T // grid, (cta + 1) * T // grid)})
+                   for cta in range(grid))
+        assert segs >= 3, (grid, tiles, segs)
+    rng = np.random.default_rng(5)
+    I_ref = np.stack([np.sort(rng.choice(wl.L, wl.k, replace=False)) for _ in range(wl.B)])
+    I = torch.as_tensor(I_ref.astype(np.int32), device="cuda")
+    ws = dk.workspace(c.p, verify=(wl.Hq, wl.Hkv, wl.d, 1))
+    o = dk.dustin_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], I, c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    assert_attention(o, c.oracle_verify(I_ref))
+    od = dk.dense_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    assert_attention(od, c.oracle_dense())
 
 
 def test_verify_padding_and_bad_index():
