@@ -615,6 +615,8 @@ def headline_arm(args, rank, world, dist, dev, local):
     x, p, seq, call = make_step(wl, dev)
     stream = torch.cuda.current_stream(dev)
     ab = algorithmic_bytes(wl)
+    if args.profile and args.profile != "step":
+        return profile_op(args, wl, x, p, seq, call, dev, stream)
 
     # ---- device-resident timing of exactly `steps` steps
     for _ in range(args.warmup):
@@ -634,16 +636,17 @@ def headline_arm(args, rank, world, dist, dev, local):
     _barrier(dist)
     step_ms = max_over_ranks(total_ms / args.steps, dist, dev)
 
-    n_med = max(MIN_RUNS, args.steps)
-    stage = stage_medians(call, n_med, stream, dev)
-
     if args.profile:
         # profiling run (ncu): warm-up and timed steps only
-        dk.check(call.ws)
+        if dk.check(call.ws):
+            raise RuntimeError("device flags after the profiled steps")
         if rank == 0:
-            print(json.dumps({"profile_run": True, "workload": wl.name, "B": wl.B,
+            print(json.dumps({"profile_run": "step", "workload": wl.name, "B": wl.B,
                               "step_us": step_ms * 1e3}), flush=True)
         return 0
+
+    n_med = max(MIN_RUNS, args.steps)
+    stage = stage_medians(call, n_med, stream, dev)
 
     # ---- dense comparator on the same inputs
     dense = dense_fn(p, x, seq, dev, 1, stream)
@@ -776,6 +779,43 @@ def headline_arm(args, rank, world, dist, dev, local):
         except Exception as e:  # the GPU number stands without it
             line["cpu_baseline"] = {"value": None, "error": str(e)[-300:]}
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def profile_op(args, wl, x, p, seq, call, dev, stream):
+    """warm-up + timed calls of one operation on the step's inputs, for ncu:
+    dense verification, the compact-cache copy of one step's selection, or
+    kv_append of 3 rows (seq_len put back after each call)."""
+    import torch
+
+    import sparse_kv_verify_gb300 as dk
+    call()   # importance and I_verify of these inputs
+    torch.cuda.synchronize(dev)
+    if args.profile == "dense":
+        fn = dense_fn(p, x, seq, dev, 1, stream)
+    elif args.profile == "compact":
+        kc = torch.empty((wl.B, wl.Hkv, wl.k, wl.d), dtype=torch.bfloat16, device=dev)
+        vc = torch.empty_like(kc)
+        slc = torch.empty_like(seq)
+
+        def fn():
+            dk.dustin_compact_kv(p, [x.K[0]], [x.V[0]], call.i_verify, seq, [kc], [vc], slc,
+                                 ws=call.ws, stream=stream)
+    else:
+        seq0 = seq.clone()
+        n_acc = torch.full((wl.B,), APPEND_ROWS, dtype=torch.int32, device=dev)
+        app = dk.AppendCall(p, x.K, x.V, x.Kb, x.Vb, n_acc, seq, ws=call.ws)
+
+        def fn():
+            app(stream)
+            seq.copy_(seq0, non_blocking=True)
+    for _ in range(args.warmup):
+        fn()
+    ms = time_block(fn, args.steps, stream, dev)
+    if dk.check(call.ws):
+        raise RuntimeError("device flags after the profiled calls")
+    print(json.dumps({"profile_run": args.profile, "workload": wl.name, "B": wl.B,
+                      "call_us": ms * 1e3}), flush=True)
     return 0
 
 
@@ -936,7 +976,7 @@ def stack_arm(args, rank, world, dist, dev, local):
         "speedup_vs_dense": {"attention_only": dense_ms * 1e3 / stage["verify"],
                              "step": dense_ms / step_ms},
         "roofline": roofline_of(stage, wl, group, peak, peak_kind, False),
-        "gpu_launches": (n_launch + 1) * args.steps, "launches_per_step": n_launch + 1,
+        "gpu_launches": (n_launch + 2) * args.steps, "launches_per_step": n_launch + 2,
         "clocks": clocks,
         "e2e": None, "e2e_note": "the end-to-end (host buffers) figure is taken on the "
                                  "headline workload",
@@ -956,8 +996,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch size (profiling of smaller cases)")
-    ap.add_argument("--profile", action="store_true",
-                    help="run warm-up and timed steps only (for ncu captures)")
+    ap.add_argument("--profile", nargs="?", const="step", default=None,
+                    choices=["step", "dense", "compact", "append"],
+                    help="for ncu captures: run only warm-up + timed calls of the step (default) "
+                         "or of one other operation on the same inputs, and print no bench line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

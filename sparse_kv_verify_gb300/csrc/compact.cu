@@ -3,11 +3,13 @@
 // per layer and KV head, into compact caches of k rows, so that several
 // verification passes can read them densely.
 //
-// One CTA per (KV head, sequence, layer); 16-byte loads and stores, eight in
-// flight per thread.  Row j of the compact caches is row i_verify[b][j] of
+// One CTA per (run of kRows selected rows, KV head, sequence, layer), so that
+// even a small batch spreads over every SM; 16-byte loads and stores, eight
+// in flight per thread.  Row j of the compact caches is row i_verify[b][j] of
 // the full caches; entries -1 (padding) and invalid indices give zero rows
-// (invalid ones are flagged).  The CTAs of layer 0, head 0 also write the
-// compact length: the entries of i_verify[b] before its first -1.
+// (invalid ones are flagged).  The first CTA of layer 0, head 0 of each
+// sequence also writes the compact length: the entries of i_verify[b] before
+// its first -1.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -17,20 +19,24 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kBatch = 8;
+constexpr int kRows = 128;   // selected rows per CTA
 
 __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant__ CompactArgs A) {
   pdl_launch_dependents();
   pdl_wait();
-  const int g = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
+  const int nrun = (A.k + kRows - 1) / kRows;
+  const int g = blockIdx.x / nrun, run = blockIdx.x - g * nrun, b = blockIdx.y, l = blockIdx.z;
   const CompactLayerDev& Ly = A.layer[l];
   int L = A.seq_len[b];
   if (L < 0 || L > A.Lcap) {
-    if (threadIdx.x == 0 && g == 0 && l == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
+    if (threadIdx.x == 0 && g == 0 && run == 0 && l == 0) flag_error(A.err, DUSTIN_DEV_SEQLEN);
     L = 0;
   }
   const int32_t* I = A.ivf + size_t(b) * A.k;
-  const int chunks = A.D / 8;   // 16-byte chunks per row
-  const int total = A.k * chunks * 2;   // K rows, then V rows
+  const int j0 = run * kRows;
+  const int nr = min(kRows, A.k - j0);   // rows of this CTA
+  const int chunks = A.D / 8;            // 16-byte chunks per row
+  const int total = nr * chunks * 2;     // K rows, then V rows
   for (int base = threadIdx.x; base < total; base += kThreads * kBatch) {
     uint4 v[kBatch];
     int dst_row[kBatch], which[kBatch], ch[kBatch];
@@ -39,9 +45,9 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant
     for (int u = 0; u < kBatch; ++u) {
       const int q = base + u * kThreads;
       live[u] = q < total;
-      const int w = q / (A.k * chunks);
-      const int rem = q - w * (A.k * chunks);
-      const int j = rem / chunks, c = rem - (rem / chunks) * chunks;
+      const int w = q / (nr * chunks);
+      const int rem = q - w * (nr * chunks);
+      const int j = j0 + rem / chunks, c = rem - (rem / chunks) * chunks;
       which[u] = w;
       dst_row[u] = j;
       ch[u] = c;
@@ -65,7 +71,7 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant
       reinterpret_cast<uint4*>(dst)[ch[u]] = v[u];
     }
   }
-  if (g == 0 && l == 0 && threadIdx.x < 32) {
+  if (g == 0 && run == 0 && l == 0 && threadIdx.x < 32) {
     // the compact length: the entries before the first -1
     int first = A.k;
     for (int j0 = 0; j0 < A.k; j0 += 32) {
@@ -83,7 +89,8 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant
 }  // namespace
 
 cudaError_t compact_launch(const CompactArgs& a, cudaStream_t stream) {
-  return launch_pdl(compact_kernel, dim3(a.hkv, a.B, a.n_layers), dim3(kThreads), 0, stream, a);
+  const int nrun = (a.k + kRows - 1) / kRows;
+  return launch_pdl(compact_kernel, dim3(a.hkv * nrun, a.B, a.n_layers), dim3(kThreads), 0, stream, a);
 }
 
 }  // namespace dustin
