@@ -160,6 +160,37 @@ def test_attention_recovery_of_policies():
     assert all(0.0 < v <= 1.0 + 1e-12 for v in arr.values())
 
 
+def test_attention_recovery_by_policy_sweep(capsys):
+    """Attention recovery rate of each policy on the drift workload (B=8,
+    L=32768, k=2048, gamma=4; the historical and look-ahead planted sets share
+    90 %): GPU scores and GPU selection for every policy, the oracle's dense
+    probabilities for the recovery of the first sampled sequences.  Prints a
+    table of the rates; asserts only that they are rates and that the budgeted
+    signal-driven selection recovers more than sinks plus a window."""
+    wl = WORKLOADS["sweep32k"].with_(k=2048, gamma=4, m=512)
+    x = generate(wl, device="cuda")
+    seq = torch.as_tensor(x.seq_len, device="cuda")
+    imp = dk.dustin_score(params_of(wl), dk.Signal(x.draft_q, x.Kd), dk.Signal(x.hist_q, x.K),
+                          wl.srh, seq)
+    n = 2   # sampled sequences
+    Q, K = to_bits(x.Q[0][:n]), to_bits(x.K[0][:n])
+    arr = {}
+    for name, pp in _policies(wl.k, wl.sinks, wl.window).items():
+        p = dk.Params(wl.B, wl.Lcap, wl.gamma, pp["sinks"], pp["window"], pp["m"], pp["k"])
+        I = dk.dustin_select(p, imp, seq).cpu().numpy()[:n]
+        arr[name] = (pp, O.attention_recovery(Q, K, I, x.seq_len[:n]))
+    with capsys.disabled():
+        print("\n| policy | sinks | window | m (draft tier) | f (target tier) | "
+              + " | ".join(f"ARR seq {b}" for b in range(n)) + " | mean |")
+        print("|---|---|---|---|---|" + "---|" * (n + 1))
+        for name, (pp, r) in arr.items():
+            f = pp["k"] - pp["sinks"] - pp["window"] - pp["m"]
+            print(f"| {name} | {pp['sinks']} | {pp['window']} | {pp['m']} | {f} | "
+                  + " | ".join(f"{v:.4f}" for v in r) + f" | {r.mean():.4f} |")
+    assert all(np.all((r > 0.0) & (r <= 1.0 + 1e-12)) for _, r in arr.values())
+    assert arr["dustin"][1].mean() > arr["streaming"][1].mean()
+
+
 def test_collect_two_query_scoring():
     """Scoring on two query rows only (the first draft look-ahead row and the
     bonus row of the historical target queries): the caller passes signals
