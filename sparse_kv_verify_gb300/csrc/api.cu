@@ -156,8 +156,12 @@ bool encode_query_map(CUtensorMap* m, const void* q, int d, int hq, int BT, int 
 // ------------------------------------------------------------- score plan
 
 // Logits of one group of sequences are kept under this size so that they stay
-// in L2 between the stream and the normalise kernels.
-constexpr size_t kScoreL2Budget = size_t(48) << 20;
+// in L2 (about 126 MB) between the stream and the normalise kernels.  96 MB
+// scores the 16-sequence, 32 K-position batch in one group (92.5 MB of
+// logits): its stream kernel then moves 0.80 of the measured HBM peak against
+// 0.77 for two groups of 8, at the same step time; 48 MB split the
+// 68-pair sweep points into uneven groups and cost them 10 us of scoring.
+constexpr size_t kScoreL2Budget = size_t(96) << 20;
 
 // Groups per normalise launch.  With two, the second group's stream kernel
 // starts on the SMs the first one's stragglers leave and one normalise covers
@@ -267,6 +271,10 @@ int build_score_plan(const dustin_params* p, const dustin_signal* draft,
     budget = avail < budget ? avail : budget;
   }
   long long nb = (long long)(budget / (per_b + 1));
+  if (nb >= 1 && nb < p->B) {   // as many groups as needed, of near-equal size
+    const long long groups = (p->B + nb - 1) / nb;
+    nb = (p->B + groups - 1) / groups;
+  }
   for (;;) {
     if (nb > p->B) nb = p->B;
     if (nb < 1) {

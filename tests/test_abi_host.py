@@ -235,7 +235,11 @@ def test_step_launch_count(L):
 
     st, n, g, _ = step(2, 4096)
     assert (st, n, g) == (0, 5, 2)              # one group
-    st, n, g, _ = step(16, 32832)               # 44 logits rows of 32 K positions per sequence
-    assert st == 0 and 1 <= g < 16 and n == 2 * (-(-16 // g)) + 3
+    # 44 logits rows of 32 K positions per sequence: 5.78 MB; 16 sequences fit
+    # the L2 budget in one group, 20 need two, of equal size
+    st, n, g, _ = step(16, 32832)
+    assert (st, n, g) == (0, 5, 16)
+    st, n, g, _ = step(20, 32832)
+    assert (st, n, g) == (0, 2 * 2 + 3, 10)
     assert lib.dustin_step_launches(None, ctypes.byref(ctypes.c_int32()),
                                     ctypes.byref(ctypes.c_int32())) == -1

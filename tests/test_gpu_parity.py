@@ -394,6 +394,25 @@ def test_verify_step_end_to_end(name):
     assert np.isin(x.planted, I.cpu().numpy()).mean() > 0.99
 
 
+def test_verify_step_in_sequence_groups():
+    """A batch whose logits exceed the L2 budget is scored by the fused step in
+    groups of sequences (here 3 sequences of about 2^19 positions, 37.7 MB of
+    logits each: groups of 2 and 1); every stage still matches the oracle."""
+    wl = WORKLOADS["tiny"].with_(B=3, L=(1 << 19) - 64, n_planted=16)
+    c = Case(wl, seq_len=[wl.L, wl.L - 1000, 70000])
+    x = c.x
+    layer = dk.VerifyLayer(x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0])
+    call = dk.StepCall(c.p, c.draft, c.target, wl.srh, [layer], c.seq)
+    n, g = call.launches()
+    assert g == 2 and n == 2 * 2 + 3
+    imp, I, outs = call()
+    assert dk.check(call.ws) == 0
+    assert_importance(imp, c.oracle_score(), x.seq_len)
+    I_ref, _ = O.select(imp.double().cpu().numpy(), x.seq_len, wl.k, wl.sinks, wl.window, wl.m)
+    assert np.array_equal(I.cpu().numpy(), I_ref)
+    assert_attention(outs[0], c.oracle_verify(I_ref))
+
+
 def test_verify_step_multi_layer_shared_selection():
     wl = WORKLOADS["tiny"].with_(n_layers=3, srh=((1, 0, 0), (1, 2, 3), (0, 0, 1)))
     c = Case(wl)
