@@ -90,7 +90,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // packed cache [B][hkv][Lcap][d] is described as 2-D rows [B*hkv*Lcap][d]
 // (rows of a box that run past one head's Lcap positions are past seq_len and
 // masked); any other strides use a 4-D map (d, Lcap, hkv, B).  *rank is 2 or 4.
-bool encode_cache_map(CUtensorMap* m, const dustin_kv& v, int Lcap, int B, int* rank) {
+bool encode_cache_map(CUtensorMap* m, const dustin_kv& v, int Lcap, int B, int* rank,
+                      int box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   const bool packed = v.sl == v.d && v.sh == int64_t(Lcap) * v.d && v.sb == int64_t(v.hkv) * v.sh &&
@@ -99,7 +100,7 @@ bool encode_cache_map(CUtensorMap* m, const dustin_kv& v, int Lcap, int B, int* 
   if (packed) {
     cuuint64_t dims[2] = {cuuint64_t(v.d), cuuint64_t(B) * v.hkv * Lcap};
     cuuint64_t strides[1] = {cuuint64_t(v.sl) * 2};
-    cuuint32_t box[2] = {64, 128};
+    cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v.ptr, dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -108,7 +109,7 @@ bool encode_cache_map(CUtensorMap* m, const dustin_kv& v, int Lcap, int B, int* 
   } else {
     cuuint64_t dims[4] = {cuuint64_t(v.d), cuuint64_t(Lcap), cuuint64_t(v.hkv), cuuint64_t(B)};
     cuuint64_t strides[3] = {cuuint64_t(v.sl) * 2, cuuint64_t(v.sh) * 2, cuuint64_t(v.sb) * 2};
-    cuuint32_t box[4] = {64, 128, 1, 1};
+    cuuint32_t box[4] = {64, cuuint32_t(box_rows), 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v.ptr, dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -513,6 +514,19 @@ int run_verify(const dustin_params* p, int32_t hq, int hkv, int D, int n_layers,
     const VerifyLayerDev& L = layers[l];
     a.layer[l] = L;
     if (!encode_query_map(&a.qmap[l], L.q, D, hq, p->B * a.T, a.G, a.T)) return DUSTIN_ECUDA;
+  }
+  // dense: contiguous context tiles by TMA boxes when every cache can be
+  // described by a tensor map (else the row gathers serve every tile)
+  a.tma = dense ? 1 : 0;
+  for (int l = 0; l < n_layers && a.tma; ++l) {
+    const VerifyLayerDev& L = layers[l];
+    const dustin_kv kv{const_cast<uint16_t*>(L.k), hkv, D, L.ksb, L.ksh, L.ksl};
+    const dustin_kv vv{const_cast<uint16_t*>(L.v), hkv, D, L.vsb, L.vsh, L.vsl};
+    int rk = 0, rv = 0;   // boxes of one 64-key tile
+    if (!encode_cache_map(&a.kmap[l], kv, p->Lcap, p->B, &rk, DUSTIN_MAX_BLOCK) ||
+        !encode_cache_map(&a.vmap[l], vv, p->Lcap, p->B, &rv, DUSTIN_MAX_BLOCK) || rk != rv)
+      a.tma = 0;
+    a.kvrank[l] = rk;
   }
   if (verify_launch(a, pl, stream) != cudaSuccess) return DUSTIN_ECUDA;
   return DUSTIN_OK;

@@ -68,6 +68,15 @@ struct VerifyArgs {
   // per layer: the queries as 3-D (d, hq, B*T) with box (64, G, T) and the
   // 128-byte swizzle, so one load brings a unit's G x T query rows
   CUtensorMap qmap[DUSTIN_MAX_LAYERS];
+  // dense mode, tma = 1: per layer the K and V caches as tensor maps with a
+  // (64 columns, 64 rows) box and the 128-byte swizzle (rank 2: rows
+  // B*hkv*Lcap of a packed cache; rank 4: (d, Lcap, hkv, B) of a strided one),
+  // so that a context tile wholly inside the sequence comes in 2 * D / 64
+  // boxes instead of row gathers
+  int tma;
+  int kvrank[DUSTIN_MAX_LAYERS];
+  CUtensorMap kmap[DUSTIN_MAX_LAYERS];
+  CUtensorMap vmap[DUSTIN_MAX_LAYERS];
 };
 
 // The segment merge that follows the stream-K kernel.

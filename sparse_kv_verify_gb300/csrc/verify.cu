@@ -152,6 +152,25 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 2-D and 4-D tiled TMA loads to a shared-memory address, with an L2 policy.
+__device__ __forceinline__ void tma_load_2d_u32(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                                uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_u32(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                                int c2, int c3, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
@@ -322,6 +341,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     int gi = 0;
     int s = 0;
     bool live = true;     // false once a wait gave up
+    uint32_t tmask = 0;   // bit j: tile gi - 1 - j came by TMA boxes
     for (long long t = t0; t < t1 && live; ++s) {
       const Seg sg = next_seg(t, t1, tiles_u);
       const int layer = sg.u / units_per_layer;
@@ -372,6 +392,36 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
           live = false;
           break;
         }
+        // a dense context tile wholly inside the sequence: TMA boxes, issued by
+        // one lane, the byte count armed with that lane's arrival (the other
+        // threads arrive as for a gathered tile, with nothing in flight)
+        const bool by_tma = A.tma && !blk && (tt + 1) * TK <= L;
+        tmask = (tmask << 1) | uint32_t(by_tma);
+        if (by_tma) {
+          const uint32_t stage = sbase + uint32_t(Ly.ring_off + size_t(st) * Ly.stage_bytes);
+          if (lane == 0) masks[st * kLoaders + lw] = uint8_t((1u << kKpw) - 1u);
+          if (lw == 0 && lane == 0) {
+            mbar_arrive_expect_tx(&full[st], uint32_t(2 * TK * D * 2));
+            const uint64_t pol = policy_evict_first();
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+              const uint32_t dk = stage + uint32_t(h * Ly.kv_panel);
+              const uint32_t dv = dk + uint32_t(Ly.half_bytes);
+              if (A.kvrank[layer] == 2) {
+                const int row = (b * A.hkv + g) * A.Lcap + tt * TK;
+                tma_load_2d_u32(dk, &A.kmap[layer], h * 64, row, &full[st], pol);
+                tma_load_2d_u32(dv, &A.vmap[layer], h * 64, row, &full[st], pol);
+              } else {
+                tma_load_4d_u32(dk, &A.kmap[layer], h * 64, tt * TK, g, b, &full[st], pol);
+                tma_load_4d_u32(dv, &A.vmap[layer], h * 64, tt * TK, g, b, &full[st], pol);
+              }
+            }
+          } else if (lane == 0) {
+            mbar_arrive(&full[st]);
+          }
+          cp_async_arrive_noinc(&full[st]);
+          continue;
+        }
         bool valid;
         if (blk) valid = raw < T;
         else if (A.dense) valid = raw < L;
@@ -402,6 +452,12 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       }
     }
     cp_async_wait_all();
+    // the boxes this lane issued for the last NSTAGE tiles have landed (each
+    // is the latest phase of its stage) before the CTA may exit
+    if (lw == 0 && lane == 0)
+      for (int j = 0; j < NSTAGE && j < gi; ++j)
+        if ((tmask >> j) & 1u)
+          mbar_drain(&full[(gi - 1 - j) % NSTAGE], uint32_t((gi - 1 - j) / NSTAGE) & 1u, A.err);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // =================================================================== MMA
