@@ -41,8 +41,11 @@
 // sub-bins holding the m1-th draft and (m1 + f)-th target keys, and every CTA
 // then lists only the keys at or above those sub-bins.  The finish is
 // unchanged: it only needs every key at or above the tier's exact threshold.
-// If a list outgrows its buffer (heavy ties) or the draft tier is larger than
-// the on-chip copy of it, rank 0 selects that sequence with the general path:
+// Every target entry also carries the draft key of its position, so once the
+// draft tier's threshold key and tie cut are known, the target entries it
+// took are marked by comparing keys.
+// If a list outgrows its buffer (heavy ties), rank 0 selects that sequence
+// with the general path:
 // candidates of the threshold bin in a shared list (or, past its capacity,
 // refinement over the whole range) and ordered passes over all keys.  Every
 // path gives the same set.
@@ -67,7 +70,6 @@ constexpr int kBins2 = 1024;          // 10 bits per refinement pass
 constexpr int kListCap = 128;         // entries per warp list and channel (scan)
 constexpr int kCandCap = 4096;        // candidates of the general path
 constexpr int kFinCap = 6144;         // list entries of both channels gathered by rank 0
-constexpr int kDCap = kBins1;         // draft-tier positions kept on chip (in h[0])
 constexpr int kBatch = 8;             // rows of 32 keys loaded before use (general path)
 constexpr int kHistThreads = 1024;    // select_hist_kernel: positions per CTA
 constexpr int kCells = kMaxSelectCtas * kWarps;   // (rank, warp) lists per channel
@@ -82,7 +84,8 @@ struct SelShared {
       uint32_t k0t[kWarps][kListCap];   // ... the target keys of their positions ...
       int p0[kWarps][kListCap];         // ... and the positions
       uint32_t k1[kWarps][kListCap];    // target keys ...
-      int p1[kWarps][kListCap];         // ... and positions
+      int p1[kWarps][kListCap];         // ... positions ...
+      uint32_t k1d[kWarps][kListCap];   // ... and the draft keys of those positions
     } l;
     struct {                 // general path: threshold-bin candidates
       uint32_t key[kCandCap];
@@ -93,7 +96,7 @@ struct SelShared {
   // rank 0: the gathered lists, draft entries [0, n0) then target [n0, n0 + n1)
   uint32_t ekey[kFinCap];
   int epos[kFinCap];
-  uint32_t ek0t[kFinCap];    // target key of a draft entry
+  uint32_t ek0t[kFinCap];    // draft entry: its target key; target entry: its draft key
   uint32_t drop[kFinCap / 32];    // target entries in the draft tier
   int cell[2][kCells + 1];   // rank 0: list offsets per (rank, warp), then the total
   int lcnt[2][kWarps];
@@ -101,8 +104,13 @@ struct SelShared {
   int wgt[kWarps], weq[kWarps];   // per warp: keys above / equal to T
   int gtb[kWarps], eqb[kWarps];   // exclusive prefixes of wgt, weq
   int ncand, bin, need, found, overflow;
+  int wsum2[2][kWarps];      // find_bin2 scratch and results, per histogram
+  int bin2[2], need2[2], found2[2];
+  uint32_t t_draft;          // the draft tier's threshold key ...
+  int tie_cut;               // ... and the last position taken at that key
   uint32_t thr[2];           // rank 0: refined list thresholds (keys) of both channels
 };
+static_assert(sizeof(SelShared) + 16 <= 227 * 1024, "select state must fit one CTA's shared memory");
 
 // ------------------------------------------------------------------ helpers
 
@@ -207,6 +215,68 @@ __device__ void find_bin(SelShared& sh, const int* hist, int nbins, int need) {
         break;
       }
       acc += h;
+    }
+  }
+  __syncthreads();
+}
+
+// find_bin over the two level-1 histograms at once (one set of block
+// barriers): for c = 0, 1 with need_c > 0, the bin of h_c holding the
+// need_c-th key and how many keys of it are needed (sh.bin2[c], sh.need2[c];
+// sh.found2[c] = 0 if h_c holds fewer keys).  Whole-block call.
+__device__ void find_bin2(SelShared& sh, const int* h0, int need0, const int* h1, int need1) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int q = kBins1 / kThreads;
+  int loc[2] = {0, 0};
+#pragma unroll
+  for (int k = 0; k < q; ++k) {
+    const int bin = kBins1 - 1 - (tid * q + k);
+    loc[0] += h0[bin];
+    loc[1] += h1[bin];
+  }
+  int incl[2] = {loc[0], loc[1]};
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int y = __shfl_up_sync(0xffffffffu, incl[c], o);
+      if (lane >= o) incl[c] += y;
+    }
+  }
+  if (lane == 31) {
+    sh.wsum2[0][warp] = incl[0];
+    sh.wsum2[1][warp] = incl[1];
+  }
+  if (tid < 2) sh.found2[tid] = 0;
+  __syncthreads();
+  if (warp < 2) {   // warp c: exclusive prefix of histogram c's warp sums
+    const int w = sh.wsum2[warp][lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    sh.wsum2[warp][lane] = wi - w;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int need = c ? need1 : need0;
+    const int* h = c ? h1 : h0;
+    const int before = sh.wsum2[c][warp] + incl[c] - loc[c];
+    if (need > 0 && before < need && need <= before + loc[c]) {
+      int acc = before;
+      for (int k = 0; k < q; ++k) {
+        const int bin = kBins1 - 1 - (tid * q + k);
+        if (acc + h[bin] >= need) {
+          sh.bin2[c] = bin;
+          sh.need2[c] = need - acc;
+          sh.found2[c] = 1;
+          break;
+        }
+        acc += h[bin];
+      }
     }
   }
   __syncthreads();
@@ -422,10 +492,13 @@ __device__ void block_prefix2(SelShared& sh, int& a, int& b) {
 // Exact top cnt of the gathered entries key/pos[0..n) (in position order),
 // minus the entries marked in dropbits (if given), given the tier's level-1
 // bin b1 and how many of its keys are taken (need): written in position order
-// to out[0..cnt); to dcopy if given; and, with sub (the target keys of the
-// entries), each selected entry's target key is taken out of h1.
+// to out[0..cnt); with sub (the target keys of the entries), each selected
+// entry's target key is taken out of h1.  With record (the draft tier), the
+// exact threshold key goes to sh.t_draft and the last position taken at that
+// key to sh.tie_cut: a position is in the tier iff its key is above the
+// threshold, or equal to it at a position up to the cut.
 __device__ void finish_tier(SelShared& sh, const uint32_t* key, const int* pos, int n, uint32_t b1,
-                            int need, int cnt, int32_t* out, int* dcopy, const uint32_t* dropbits,
+                            int need, int cnt, int32_t* out, bool record, const uint32_t* dropbits,
                             const uint32_t* sub, int* h1) {
   auto drop = [&](int j) { return dropbits && ((dropbits[j >> 5] >> (j & 31)) & 1u); };
   const int tid = threadIdx.x;
@@ -453,16 +526,17 @@ __device__ void finish_tier(SelShared& sh, const uint32_t* key, const int* pos, 
     if (drop(j)) continue;
     const uint32_t kv = key[j];
     bool sel = kv > T;
-    if (kv == T) sel = eq_run++ < need_eq;
+    if (kv == T) {
+      sel = eq_run++ < need_eq;
+      if (sel && record) atomicMax(&sh.tie_cut, pos[j]);
+    }
     if (sel) {
-      if (o < cnt) {
-        out[o] = pos[j];
-        if (dcopy) dcopy[o] = pos[j];
-      }
+      if (o < cnt) out[o] = pos[j];
       if (sub) atomicSub(&h1[select_bin(sub[j])], 1);
       ++o;
     }
   }
+  if (record && tid == 0) sh.t_draft = T;
   __syncthreads();
 }
 
@@ -479,6 +553,12 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t lt = (1u << lane) - 1u;
   int32_t* out = A.out + size_t(b) * A.k;
+  // the level-1 histograms: their loads go out with the length's
+  const int* gh = A.hist + size_t(b) * 2 * kBins1;
+  constexpr int kHpt = 2 * kBins1 / kThreads;   // histogram words per thread
+  int hv[kHpt];
+#pragma unroll
+  for (int u = 0; u < kHpt; ++u) hv[u] = __ldcg(gh + tid + u * kThreads);
   const int L = A.seq_len[b];
   // the early cases depend on the sequence only: all its CTAs leave together
   if (L < 0 || L > A.Lcap) {
@@ -501,29 +581,48 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   if (r == 0)
     for (int j = tid; j < nP; j += kThreads) out[j] = j < s_eff ? j : w0 + (j - s_eff);
 
+  // this CTA's run of U, whole 128-position rows per warp; the first row's
+  // keys are loaded now, so that they arrive during the threshold search
+  const int a0 = s_eff & ~127;
+  const int span = ((((w0 - a0) + CS - 1) / CS) + 127) & ~127;
+  const int c0 = a0 + r * span, c1 = min(c0 + span, w0);
+  const int wspan = c1 > c0 ? ((((c1 - c0) + kWarps - 1) / kWarps) + 127) & ~127 : 128;
+  const int x0 = c0 + warp * wspan, x1 = min(x0 + wspan, c1);
+  const float* row0 = A.imp + (size_t(b) * 2 + 0) * A.Lcap;
+  const float* row1 = A.imp + (size_t(b) * 2 + 1) * A.Lcap;
+  bool have_pre = A.vec4 && x0 < x1;
+  float4 pre[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  if (have_pre && x0 + 4 * lane < x1) {
+    pre[0] = __ldg(reinterpret_cast<const float4*>(row0 + x0 + 4 * lane));
+    pre[1] = __ldg(reinterpret_cast<const float4*>(row1 + x0 + 4 * lane));
+  }
+
   // ---- scan: thresholds from the histograms
-  const int* gh = A.hist + size_t(b) * 2 * kBins1;
-  for (int j = tid; j < 2 * kBins1; j += kThreads) (&sh.h[0][0])[j] = __ldcg(gh + j);
-  if (tid == 0) sh.overflow = 0;
+#pragma unroll
+  for (int u = 0; u < kHpt; ++u) (&sh.h[0][0])[tid + u * kThreads] = hv[u];
+  if (tid == 0) {
+    sh.overflow = 0;
+    sh.tie_cut = -1;
+    sh.t_draft = 0xFFFFFFFFu;
+  }
   __syncthreads();
   uint32_t b0 = 0xFFFFFFFFu, b1 = 0xFFFFFFFFu;   // no key reaches these bins
   int need0 = 0, need1 = 0;
   long long est = 0;   // entries of the lists of whole threshold bins
+  find_bin2(sh, sh.h[0], m1, sh.h[1], f > 0 ? m1 + f : 0);
   if (m1 > 0) {
-    find_bin(sh, sh.h[0], kBins1, m1);
-    if (sh.found) {
-      b0 = uint32_t(sh.bin);
-      need0 = sh.need;
+    if (sh.found2[0]) {
+      b0 = uint32_t(sh.bin2[0]);
+      need0 = sh.need2[0];
       est += m1 - need0 + sh.h[0][b0];
     } else if (tid == 0) {
       sh.overflow = 1;
     }
   }
   if (f > 0) {
-    find_bin(sh, sh.h[1], kBins1, m1 + f);
-    if (sh.found) {
-      b1 = uint32_t(sh.bin);
-      need1 = sh.need;
+    if (sh.found2[1]) {
+      b1 = uint32_t(sh.bin2[1]);
+      need1 = sh.need2[1];
       est += m1 + f - need1 + sh.h[1][b1];
     } else if (tid == 0) {
       sh.overflow = 1;
@@ -533,14 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   uint32_t t0 = b0 == 0xFFFFFFFFu ? 0xFFFFFFFFu : b0 << 20;
   uint32_t t1 = b1 == 0xFFFFFFFFu ? 0xFFFFFFFFu : b1 << 20;
 
-  // ---- scan: this CTA's run of U, whole 128-position rows per warp
-  const int a0 = s_eff & ~127;
-  const int span = ((((w0 - a0) + CS - 1) / CS) + 127) & ~127;
-  const int c0 = a0 + r * span, c1 = min(c0 + span, w0);
-  const int wspan = c1 > c0 ? ((((c1 - c0) + kWarps - 1) / kWarps) + 127) & ~127 : 128;
-  const int x0 = c0 + warp * wspan, x1 = min(x0 + wspan, c1);
-  const float* row0 = A.imp + (size_t(b) * 2 + 0) * A.Lcap;
-  const float* row1 = A.imp + (size_t(b) * 2 + 1) * A.Lcap;
+  // ---- scan of this CTA's run
   bool bad = false;
   // f(i0, kv): every 128-position row of this warp's run, lane holding keys
   // i0 .. i0 + 3 of both channels (0 outside U or past the run)
@@ -551,7 +643,13 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const float* row = c ? row1 : row0;
-        if (A.vec4) {
+        if (have_pre) {   // the first row, loaded before the threshold search
+          const float4 x = pre[c];
+          v[c][0] = x.x;
+          v[c][1] = x.y;
+          v[c][2] = x.z;
+          v[c][3] = x.w;
+        } else if (A.vec4) {
           const float4 x = i0 < x1 ? __ldg(reinterpret_cast<const float4*>(row + i0)) : make_float4(0.f, 0.f, 0.f, 0.f);
           v[c][0] = x.x;
           v[c][1] = x.y;
@@ -562,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
           for (int e = 0; e < 4; ++e) v[c][e] = i0 + e < x1 ? __ldg(row + i0 + e) : 0.f;
         }
       }
+      have_pre = false;
       uint32_t kv[2][4];
 #pragma unroll
       for (int c = 0; c < 2; ++c)
@@ -645,6 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
             if (c) {
               sh.u.l.k1[warp][slot] = kv[1][e];
               sh.u.l.p1[warp][slot] = i0 + e;
+              sh.u.l.k1d[warp][slot] = kv[0][e];
             } else {
               sh.u.l.k0[warp][slot] = kv[0][e];
               sh.u.l.k0t[warp][slot] = kv[1][e];
@@ -715,6 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
           sh.epos[j] = rs->u.l.p0[w][slot];
         } else {
           sh.ekey[j] = rs->u.l.k1[w][slot];
+          sh.ek0t[j] = rs->u.l.k1d[w][slot];
           sh.epos[j] = rs->u.l.p1[w][slot];
         }
       }
@@ -727,13 +828,12 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
 
   // ---- finish (rank 0)
   const int n0t = sh.cell[0][CS * kWarps], n1t = sh.cell[1][CS * kWarps];
-  int* dpos = &sh.h[0][0];   // the draft tier's positions (h[0] is no longer needed)
-  if (sh.overflow || m1 > kDCap) {
+  if (sh.overflow) {
     select_general(sh, A, b, s_eff, w0, nP, m1, f, out);
     return;
   }
   if (m1 > 0)
-    finish_tier(sh, sh.ekey, sh.epos, n0t, b0, need0, m1, out + nP, f > 0 ? dpos : nullptr, nullptr,
+    finish_tier(sh, sh.ekey, sh.epos, n0t, b0, need0, m1, out + nP, f > 0, nullptr,
                 f > 0 ? sh.ek0t : nullptr, sh.h[1]);
   if (f > 0) {
     // the target histogram of U minus the draft tier (corrected above), and
@@ -745,22 +845,20 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
     }
     const uint32_t bt = uint32_t(sh.bin);
     const int needt = sh.need;
-    // mark the target entries that the draft tier took (both ascending: one
-    // binary search per entry)
+    // mark the target entries that the draft tier took: each carries the
+    // draft key of its position, so the tier's threshold and tie cut decide
     for (int j = tid; j < (n1t + 31) / 32; j += kThreads) sh.drop[j] = 0u;
     __syncthreads();
-    for (int j = tid; j < n1t; j += kThreads) {
-      const int p = sh.epos[n0t + j];
-      int lo = 0, hi = m1;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (dpos[mid] < p) lo = mid + 1;
-        else hi = mid;
+    if (m1 > 0) {
+      const uint32_t T0 = sh.t_draft;
+      const int cut = sh.tie_cut;
+      for (int j = tid; j < n1t; j += kThreads) {
+        const uint32_t k0 = sh.ek0t[n0t + j];
+        if (k0 > T0 || (k0 == T0 && sh.epos[n0t + j] <= cut)) atomicOr(&sh.drop[j >> 5], 1u << (j & 31));
       }
-      if (lo < m1 && dpos[lo] == p) atomicOr(&sh.drop[j >> 5], 1u << (j & 31));
     }
     __syncthreads();
-    finish_tier(sh, sh.ekey + n0t, sh.epos + n0t, n1t, bt, needt, f, out + nP + m1, nullptr,
+    finish_tier(sh, sh.ekey + n0t, sh.epos + n0t, n1t, bt, needt, f, out + nP + m1, false,
                 m1 > 0 ? sh.drop : nullptr, nullptr, nullptr);
   }
 }
