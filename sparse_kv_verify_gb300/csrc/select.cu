@@ -97,9 +97,8 @@ struct SelShared {
   uint32_t ekey[kFinCap];
   int epos[kFinCap];
   uint32_t ek0t[kFinCap];    // draft entry: its target key; target entry: its draft key
-  uint32_t drop[kFinCap / 32];    // target entries in the draft tier
-  int cell[2][kCells + 1];   // rank 0: list offsets per (rank, warp), then the total
-  int lcnt[2][kWarps];
+  int cell[2][kCells + 1];   // list counts, then offsets, per (rank, warp); then the total
+  int ovf_all[kCells];       // per (rank, warp): its list overflowed
   int wsum[kWarps];          // scan scratch
   int wgt[kWarps], weq[kWarps];   // per warp: keys above / equal to T
   int gtb[kWarps], eqb[kWarps];   // exclusive prefixes of wgt, weq
@@ -113,6 +112,14 @@ struct SelShared {
 static_assert(sizeof(SelShared) + 16 <= 227 * 1024, "select state must fit one CTA's shared memory");
 
 // ------------------------------------------------------------------ helpers
+
+// Split cluster barrier: a CTA arrives early and waits later; once the wait
+// returns, every CTA of the cluster has started (its shared memory may be
+// written by the others).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait;" ::: "memory"); }
 
 // Key of position i of one channel's importance row.
 struct Keys {
@@ -496,11 +503,21 @@ __device__ void block_prefix2(SelShared& sh, int& a, int& b) {
 // entry's target key is taken out of h1.  With record (the draft tier), the
 // exact threshold key goes to sh.t_draft and the last position taken at that
 // key to sh.tie_cut: a position is in the tier iff its key is above the
-// threshold, or equal to it at a position up to the cut.
+// threshold, or equal to it at a position up to the cut.  With dkey (the
+// target tier), entries in the draft tier are left out by that test.
 __device__ void finish_tier(SelShared& sh, const uint32_t* key, const int* pos, int n, uint32_t b1,
-                            int need, int cnt, int32_t* out, bool record, const uint32_t* dropbits,
+                            int need, int cnt, int32_t* out, bool record, const uint32_t* dkey,
                             const uint32_t* sub, int* h1) {
-  auto drop = [&](int j) { return dropbits && ((dropbits[j >> 5] >> (j & 31)) & 1u); };
+  // with dkey (the draft keys of the entries), an entry the draft tier took
+  // is left out: its draft key is above that tier's threshold, or equal to it
+  // at a position up to the tier's tie cut
+  const uint32_t T0 = sh.t_draft;
+  const int cut = sh.tie_cut;
+  auto drop = [&](int j) {
+    if (!dkey) return false;
+    const uint32_t k0 = dkey[j];
+    return k0 > T0 || (k0 == T0 && pos[j] <= cut);
+  };
   const int tid = threadIdx.x;
   const uint32_t T = refine(sh, b1, &need, [&](auto f) {
     for (int j = tid; j < n; j += kThreads) {
@@ -719,6 +736,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
     t1 = r0->thr[1];
   }
 
+  if (est <= kFinCap) cluster_arrive_relaxed();   // waited for before the hand-off
+
   // ---- scan: the lists
   int n0 = 0, n1 = 0;   // list entries of this warp (warp-uniform)
   for_rows4([&](int i0, const uint32_t (&kv)[2][4]) {
@@ -758,77 +777,63 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
     }
   });
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(A.err, DUSTIN_DEV_NAN);
+  // ---- hand-off: every warp's list counts (and whether its lists or the
+  // threshold search overflowed) go to every rank; after a cluster barrier
+  // each rank derives every list's offset and pushes its entries into rank
+  // 0's arrays, in position order; a second barrier completes them
+  if (est <= kFinCap) cluster_wait();   // every CTA of the cluster has started
   if (lane == 0) {
-    sh.lcnt[0][warp] = n0;
-    sh.lcnt[1][warp] = n1;
-    if (n0 > kListCap || n1 > kListCap) atomicOr(&sh.overflow, 1);
+    const int ovf = (n0 > kListCap || n1 > kListCap || sh.overflow) ? 1 : 0;
+    for (int rr = 0; rr < CS; ++rr) {
+      SelShared* rs = cluster.map_shared_rank(&sh, rr);
+      rs->cell[0][r * kWarps + warp] = min(n0, kListCap);
+      rs->cell[1][r * kWarps + warp] = min(n1, kListCap);
+      rs->ovf_all[r * kWarps + warp] = ovf;
+    }
   }
-  // ---- hand-off: every rank's lists are complete
   cluster.sync();
-  if (r == 0) {
-    // list offsets per (rank, warp), in position order
-    if (tid < 2 * 32) {
-      const int c = tid >> 5, w = tid & 31;
-      int run = 0;
-      for (int rr = 0; rr < CS; ++rr) {
-        const SelShared* rs = cluster.map_shared_rank(&sh, rr);
-        const int n = min(rs->lcnt[c][w], kListCap);
-        if (w == 0 && rs->overflow) atomicOr(&sh.overflow, 1);
-        sh.cell[c][rr * kWarps + w] = n;   // counts first
-        run += n;
-      }
-    }
-    __syncthreads();
-    if (tid < 2 * 32) {   // exclusive prefix over the CS * 32 cells of each channel
-      const int c = tid >> 5, lane2 = tid & 31;
-      int carry = 0;
-      for (int base = 0; base < CS * kWarps; base += 32) {
-        const int v = sh.cell[c][base + lane2];
-        int incl = v;
+  if (tid < 2 * 32) {   // exclusive prefix over the CS * 32 cells of each channel
+    const int c = tid >> 5, lane2 = tid & 31;
+    int carry = 0;
+    for (int base = 0; base < CS * kWarps; base += 32) {
+      const int v = sh.cell[c][base + lane2];
+      int incl = v;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane2 >= o) incl += y;
-        }
-        sh.cell[c][base + lane2] = carry + incl - v;
-        carry += __shfl_sync(0xffffffffu, incl, 31);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane2 >= o) incl += y;
       }
-      if (lane2 == 0) sh.cell[c][CS * kWarps] = carry;
+      sh.cell[c][base + lane2] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    __syncthreads();
-    const int n0t = sh.cell[0][CS * kWarps], n1t = sh.cell[1][CS * kWarps];
-    if (!sh.overflow && n0t + n1t <= kFinCap) {
-      // every rank's entries into ekey/epos (draft, then target), in order
-      for (int j = tid; j < n0t + n1t; j += kThreads) {
-        const int c = j < n0t ? 0 : 1, jj = c ? j - n0t : j;
-        int lo = 0, hi = CS * kWarps - 1;   // the last cell starting at or before jj
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (sh.cell[c][mid] <= jj) lo = mid;
-          else hi = mid - 1;
-        }
-        const int rr = lo / kWarps, w = lo - rr * kWarps, slot = jj - sh.cell[c][lo];
-        const SelShared* rs = cluster.map_shared_rank(&sh, rr);
-        if (c == 0) {
-          sh.ekey[j] = rs->u.l.k0[w][slot];
-          sh.ek0t[j] = rs->u.l.k0t[w][slot];
-          sh.epos[j] = rs->u.l.p0[w][slot];
-        } else {
-          sh.ekey[j] = rs->u.l.k1[w][slot];
-          sh.ek0t[j] = rs->u.l.k1d[w][slot];
-          sh.epos[j] = rs->u.l.p1[w][slot];
-        }
-      }
-    } else if (tid == 0) {
-      sh.overflow = 1;
+    if (lane2 == 0) sh.cell[c][CS * kWarps] = carry;
+  } else if (tid < 3 * 32) {   // any overflow anywhere
+    int o = 0;
+    for (int i = lane; i < CS * kWarps; i += 32) o |= sh.ovf_all[i];
+    o = __any_sync(0xffffffffu, o != 0);
+    if (lane == 0) sh.overflow = o;
+  }
+  __syncthreads();
+  const int n0t = sh.cell[0][CS * kWarps], n1t = sh.cell[1][CS * kWarps];
+  if (!sh.overflow && n0t + n1t <= kFinCap) {
+    SelShared* r0 = cluster.map_shared_rank(&sh, 0);
+    const int base0 = sh.cell[0][r * kWarps + warp], base1 = n0t + sh.cell[1][r * kWarps + warp];
+    for (int slot = lane; slot < n0; slot += 32) {
+      r0->ekey[base0 + slot] = sh.u.l.k0[warp][slot];
+      r0->ek0t[base0 + slot] = sh.u.l.k0t[warp][slot];
+      r0->epos[base0 + slot] = sh.u.l.p0[warp][slot];
+    }
+    for (int slot = lane; slot < n1; slot += 32) {
+      r0->ekey[base1 + slot] = sh.u.l.k1[warp][slot];
+      r0->ek0t[base1 + slot] = sh.u.l.k1d[warp][slot];
+      r0->epos[base1 + slot] = sh.u.l.p1[warp][slot];
     }
   }
-  cluster.sync();   // rank 0 has read every rank's lists: the others may leave
+  cluster.sync();   // rank 0 holds every entry: the others may leave
   if (r != 0) return;
 
   // ---- finish (rank 0)
-  const int n0t = sh.cell[0][CS * kWarps], n1t = sh.cell[1][CS * kWarps];
-  if (sh.overflow) {
+  if (sh.overflow || n0t + n1t > kFinCap) {
     select_general(sh, A, b, s_eff, w0, nP, m1, f, out);
     return;
   }
@@ -845,21 +850,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
     }
     const uint32_t bt = uint32_t(sh.bin);
     const int needt = sh.need;
-    // mark the target entries that the draft tier took: each carries the
-    // draft key of its position, so the tier's threshold and tie cut decide
-    for (int j = tid; j < (n1t + 31) / 32; j += kThreads) sh.drop[j] = 0u;
-    __syncthreads();
-    if (m1 > 0) {
-      const uint32_t T0 = sh.t_draft;
-      const int cut = sh.tie_cut;
-      for (int j = tid; j < n1t; j += kThreads) {
-        const uint32_t k0 = sh.ek0t[n0t + j];
-        if (k0 > T0 || (k0 == T0 && sh.epos[n0t + j] <= cut)) atomicOr(&sh.drop[j >> 5], 1u << (j & 31));
-      }
-    }
-    __syncthreads();
+    // the target entries the draft tier took are left out by their draft keys
     finish_tier(sh, sh.ekey + n0t, sh.epos + n0t, n1t, bt, needt, f, out + nP + m1, false,
-                m1 > 0 ? sh.drop : nullptr, nullptr, nullptr);
+                m1 > 0 ? sh.ek0t + n0t : nullptr, nullptr, nullptr);
   }
 }
 
