@@ -52,7 +52,8 @@ constexpr int kSoftmaxWarps = 4;    // one thread per tensor-memory lane
 constexpr int kLoaders = 8;         // loader warps, kKpw keys of every tile each
 constexpr int kKpw = TK / kLoaders;  // keys per loader warp and tile
 constexpr int kLoaderWarp0 = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + kLoaders;
-constexpr int NTH = 32 * (kMmaWarp + 1);
+constexpr int kPvWarp = kMmaWarp + 1;   // issues the P V MMAs (kMmaWarp issues S = Q K^T)
+constexpr int NTH = 32 * (kPvWarp + 1);
 constexpr int kSCol = 0;         // S buffers: columns [0, 64) and [64, 128)
 constexpr int kPCol = 128;       // P buffers (bf16 pairs): [128, 160) and [160, 192)
 static_assert(TK == DUSTIN_MAX_BLOCK, "the draft block must fit one tile");
@@ -235,7 +236,7 @@ inline VLay make_lay(int D, int NQ) {
   L.nst = D == 128 ? StagesOf<128>::n : StagesOf<64>::n;
   L.mask_off = L.ring_off + uint32_t(L.nst) * L.stage_bytes;
   L.bar_off = L.mask_off + ((uint32_t(L.nst) * kLoaders + 7u) & ~7u);
-  L.misc_off = L.bar_off + uint32_t(2 * L.nst + 4 + 2 * NQB + 1) * 8;
+  L.misc_off = L.bar_off + uint32_t(2 * L.nst + 4 + 2 * NQB + 2) * 8;
   L.total = L.misc_off + 16 + 1024;
   return L;
 }
@@ -275,7 +276,8 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
   uint64_t* p_full = s_full + 2;
   uint64_t* q_full = p_full + 2;
   uint64_t* q_empty = q_full + NQB;
-  uint64_t* mma_done = q_empty + NQB;
+  uint64_t* mma_done = q_empty + NQB;    // the S issuer's MMAs have completed
+  uint64_t* pv_done = mma_done + 1;      // the P V issuer's MMAs have completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly.misc_off + 8);
   int* q_hi = reinterpret_cast<int*>(smem + Ly.misc_off + 12);   // query loads issued: [0, q_hi)
@@ -298,6 +300,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       mbar_init(&q_empty[x], 1);
     }
     mbar_init(mma_done, 1);
+    mbar_init(pv_done, 1);
     *abort_flag = 0;
     *q_hi = 0;
     fence_barrier_init();
@@ -460,45 +463,68 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
           mbar_drain(&full[(gi - 1 - j) % NSTAGE], uint32_t((gi - 1 - j) / NSTAGE) & 1u, A.err);
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // =================================================================== MMA
+    // ================================================================ S MMAs
+    // S = Q K^T of tile g into S buffer g % 2, once its rows have landed and
+    // the softmax has read that buffer's previous tile (g - 2)
     if (lane == 0) {
       constexpr uint32_t kIdS = tc_idesc(128, TK, 0);
-      constexpr uint32_t kIdPV = tc_idesc(128, D, 1);
-      const uint32_t o_tmem = tmem + Tm::o_col;
       int gi = 0;
       int s = 0;
-      // S = Q K^T of tile g2 into S buffer g2 % 2, once its rows have landed
       bool issued = false;
-      auto issue_s = [&](int g2, uint32_t qbuf) -> bool {
-        const int st = int(g2 % NSTAGE);
-        if (!mbar_wait(&full[st], uint32_t(g2 / NSTAGE) & 1u, A.err, abort_flag)) return false;
-        issued = true;
-        fence_proxy_async();   // the rows were written by cp.async (generic proxy)
-        tc_fence_after();
-        const uint32_t kst = sbase + uint32_t(Ly.ring_off + size_t(st) * Ly.stage_bytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = uint32_t((kk & 3) * 32);
-          const uint64_t a = tc_desc(qbuf + uint32_t((kk >> 2) * Ly.q_panel) + koff, 16, 1024);
-          const uint64_t bd = tc_desc(kst + uint32_t((kk >> 2) * Ly.kv_panel) + koff, 16, 1024);
-          tc_mma_ss(tmem + uint32_t(kSCol + (g2 & 1) * TK), a, bd, kIdS, kk > 0);
-        }
-        tc_commit(&s_full[g2 & 1]);
-        return true;
-      };
       bool live = true;   // false once a wait gave up: issue nothing more
       for (long long t = t0; t < t1 && live; ++s) {
         const Seg sg = next_seg(t, t1, tiles_u);
         const int qb = s % NQB;
         const uint32_t qbuf = sbase + uint32_t(qb * Ly.q_buf);
-        if (!mbar_wait(&q_full[qb], uint32_t(s / NQB) & 1u, A.err, abort_flag) || !issue_s(gi, qbuf))
-          break;
+        if (!mbar_wait(&q_full[qb], uint32_t(s / NQB) & 1u, A.err, abort_flag)) break;
         for (int i = 0; i < sg.n; ++i, ++gi) {
-          if ((i + 1 < sg.n && !issue_s(gi + 1, qbuf)) ||
-              !mbar_wait(&p_full[gi & 1], uint32_t(gi >> 1) & 1u, A.err, abort_flag)) {
+          const int st = int(gi % NSTAGE);
+          if ((gi >= 2 && !mbar_wait(&p_full[gi & 1], uint32_t((gi >> 1) - 1) & 1u, A.err, abort_flag)) ||
+              !mbar_wait(&full[st], uint32_t(gi / NSTAGE) & 1u, A.err, abort_flag)) {
             live = false;
             break;
           }
+          issued = true;
+          fence_proxy_async();   // the rows were written by cp.async (generic proxy)
+          tc_fence_after();
+          const uint32_t kst = sbase + uint32_t(Ly.ring_off + size_t(st) * Ly.stage_bytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = uint32_t((kk & 3) * 32);
+            const uint64_t a = tc_desc(qbuf + uint32_t((kk >> 2) * Ly.q_panel) + koff, 16, 1024);
+            const uint64_t bd = tc_desc(kst + uint32_t((kk >> 2) * Ly.kv_panel) + koff, 16, 1024);
+            tc_mma_ss(tmem + uint32_t(kSCol + (gi & 1) * TK), a, bd, kIdS, kk > 0);
+          }
+          tc_commit(&s_full[gi & 1]);
+        }
+        if (live) tc_commit(&q_empty[qb]);   // the segment's query rows are no longer read
+      }
+      // every MMA this thread issued has completed before tensor memory is freed
+      if (issued) {
+        tc_commit(mma_done);
+        mbar_drain(mma_done, 0, A.err);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ============================================================== P V MMAs
+    // O (+)= P V of tile g once the softmax has stored P (the first tile of a
+    // segment overwrites O, which the softmax read for the previous segment
+    // before it stored that P); the commit frees the tile's stage
+    if (lane == 0) {
+      constexpr uint32_t kIdPV = tc_idesc(128, D, 1);
+      const uint32_t o_tmem = tmem + Tm::o_col;
+      int gi = 0;
+      bool issued = false;
+      bool live = true;
+      for (long long t = t0; t < t1 && live;) {
+        const Seg sg = next_seg(t, t1, tiles_u);
+        for (int i = 0; i < sg.n; ++i, ++gi) {
+          if (!mbar_wait(&p_full[gi & 1], uint32_t(gi >> 1) & 1u, A.err, abort_flag)) {
+            live = false;
+            break;
+          }
+          issued = true;
           tc_fence_after();
           const int st = int(gi % NSTAGE);
           const uint32_t vst =
@@ -509,14 +535,12 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
             const uint64_t bd = tc_desc(vst + uint32_t(kk * 2048), uint32_t(Ly.kv_panel), 1024);
             tc_mma_ts(o_tmem, p_tmem + uint32_t(kk * 8), bd, kIdPV, (i > 0 || kk > 0) ? 1 : 0);
           }
-          tc_commit(&empty[st]);   // P V of tile gi done: its stage is free
+          tc_commit(&empty[st]);   // S and P V of tile gi done: its stage is free
         }
-        if (live) tc_commit(&q_empty[qb]);
       }
-      // every MMA this thread issued has completed before tensor memory is freed
       if (issued) {
-        tc_commit(mma_done);
-        mbar_drain(mma_done, 0, A.err);
+        tc_commit(pv_done);
+        mbar_drain(pv_done, 0, A.err);
       }
     }
     __syncwarp();
@@ -605,6 +629,14 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
             for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
             tc_st32(o_lane + uint32_t(c), o);
           }
+        }
+        // P buffer gi % 2 is free once P V of tile gi - 2 has completed (the
+        // two issuers' MMAs are not ordered with each other)
+        if (gi >= 2 && !__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 2) % NSTAGE],
+                                                         uint32_t((gi - 2) / NSTAGE) & 1u, A.err,
+                                                         abort_flag))) {
+          live = false;
+          break;
         }
         tc_st32(lane_base + uint32_t(kPCol + (gi & 1) * (TK / 2)), pk);
         tc_fence_before();
