@@ -106,6 +106,9 @@ __device__ __forceinline__ void consume_segment(const uint32_t (&qb)[NT][kMaxKs]
   constexpr int NKS = D / 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float scale = kLog2e * rsqrtf(float(D));
+  // the logits are read once more, by the normalise kernel: keep them in L2
+  // (the K rows stream through it with evict-first)
+  const uint64_t keep = policy_evict_last();
   for (int k = 0; k < n; ++k, r0 += ROWS) {
     const int i = i0 + k;
     const int st = i % kStages;
@@ -141,7 +144,7 @@ __device__ __forceinline__ void consume_segment(const uint32_t (&qb)[NT][kMaxKs]
             const int pos = pos_lo + ((e >> 1) << 3);
             if (pair < npairs && (full_tile || pos < L)) {
               const float v = c[j][e] * scale;
-              lrow[size_t(pair) * LSP + pos] = v;
+              st_global_hint(lrow + size_t(pair) * LSP + pos, v, keep);
               // online sum of 2^(v - m) with a lazily raised reference m: the
               // reference only moves when v passes it by more than 8, so the
               // common path is one ex2 and one add
