@@ -13,28 +13,33 @@
 // B, Hkv and k are.
 //
 // Roles inside a CTA (warp specialised, handing over through mbarriers):
-//   warps 4-7        loaders: warp w copies keys [16 w, 16 w + 16) of every
-//   (loaders)        tile, K and V rows, with 16-byte cp.async straight into
-//                    the 128-byte-swizzled K-major layout the MMA reads (rows
-//                    the tile does not use are zero-filled) through a ring of
-//                    five 32 KB stages (eight 16 KB ones for d = 64; the loads
-//                    take about 3 us under full load, so the stages in flight
-//                    set the pace); each copy's completion arrives on the
-//                    stage's barrier (cp.async.mbarrier.arrive).  A segment's
-//                    query rows come with one tiled TMA load into one of two
-//                    query buffers;
-//   warp 8 (MMA)     one thread issues the tensor-core MMAs (after a proxy
-//                    fence, since the rows were written through the generic
-//                    proxy): S = Q K^T of the next tile into one of two S
-//                    buffers in tensor memory as soon as its rows have landed,
-//                    then O += P V of the current tile with P read from tensor
-//                    memory;
+//   warps 4-11       loaders: warp w copies keys [8 (w-4), 8 (w-4) + 8) of
+//   (loaders)        every tile, K and V rows, with 16-byte cp.async straight
+//                    into the 128-byte-swizzled K-major layout the MMA reads
+//                    (rows the tile does not use are zero-filled) through a
+//                    ring of five 32 KB stages (eight 16 KB ones for d = 64);
+//                    each copy's completion arrives on the stage's barrier
+//                    (cp.async.mbarrier.arrive).  A dense tile that lies wholly
+//                    inside the cache comes instead as tiled TMA loads (a K
+//                    and a V box of 64 rows x 64 columns per 64-column panel)
+//                    issued by one loader thread.  A
+//                    segment's query rows come with one tiled TMA load into one
+//                    of two query buffers;
+//   warp 12 (S)      one thread issues S = Q K^T of each tile into one of two S
+//                    buffers in tensor memory as soon as its rows have landed
+//                    (after a proxy fence, since cp.async rows were written
+//                    through the generic proxy);
+//   warp 13 (P V)    one thread issues O += P V of each tile with P read from
+//                    tensor memory, then frees the tile's stage; splitting the
+//                    two MMA streams over two warps keeps one issuing thread
+//                    from bounding a tile;
 //   warps 0-3        one thread per query row (tensor-memory lane; warps with
 //                    no query row sit the loop out): online softmax of its S
 //                    row in the log2 domain, with the reference max moved only
 //                    when a tile passes it by more than 2^8 (so O is rarely
 //                    rescaled), P rounded to bf16 and stored back to tensor
-//                    memory; then the epilogue.
+//                    memory once the P V MMA two tiles back has read that P
+//                    buffer; then the epilogue.
 //
 // Merge: a segment that covers a whole unit writes O directly; otherwise it
 // writes (row max, row sum, unnormalised O) to the workspace, and a second,
