@@ -147,6 +147,55 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t* v) {
       : "memory");
 }
 
+// 16-lane shapes (M = 64 accumulators: rows 16 q .. 16 q + 15 in lanes 32 q ..
+// 32 q + 15).  16x256b: thread t holds lanes base + t / 4 and base + 8 + t / 4,
+// columns 2 (t % 4) and 2 (t % 4) + 1 of each 8-column chunk (registers 4 c ..
+// 4 c + 3 for chunk c: lane t / 4 both columns, then lane 8 + t / 4).
+// 16x128b: column t % 4 of each 4-column chunk, same two lanes (registers 2 c,
+// 2 c + 1).
+__device__ __forceinline__ void tc_ld16x256_x8(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_ld16x256_x4(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_st16x256_x4(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_st16x128_x8(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
 // ---- TMA -------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
@@ -266,8 +315,11 @@ __device__ __forceinline__ Seg next_seg(long long& t, long long t1, int tiles_u)
   return s;
 }
 
-template <int D>
+// M: rows of the S and P V MMAs, 64 when the query rows fit (they then spread
+// over the four lane quarters, 16 each), else 128 (one row per lane).
+template <int D, int M>
 __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ VerifyArgs A) {
+  static_assert(M == 64 || M == 128, "MMA rows");
   using Tm = TmemCfg<D>;
   const VLay& Ly = A.lay;
   constexpr int NSTAGE = StagesOf<D>::n;   // == A.lay.nst
@@ -290,7 +342,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int T = A.T, NQ = A.NQ, GQ = A.G;
-  const int n_act = (NQ + 31) >> 5;   // softmax warps that hold query rows
+  const int n_act = M == 64 ? (NQ + 15) >> 4 : (NQ + 31) >> 5;   // softmax warps holding query rows
   if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&full[s], 32 * kLoaders + kLoaders);
@@ -333,11 +385,11 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
 
   if (warp >= kLoaderWarp0 && warp < kLoaderWarp0 + kLoaders) {
     // =============================================================== loaders
-    // Loader warp lw fetches keys [16 lw, 16 lw + 16) of every tile: lanes
-    // 0-15 read one key index each, then the warp copies the K and V rows of
-    // its keys with 16-byte cp.async (one row of 256 bytes per half-warp)
-    // straight into the 128-byte-swizzled layout the MMA reads; unused rows
-    // are zero-filled.  Each thread's copies arrive on the stage's barrier as
+    // Loader warp lw fetches keys [8 lw, 8 lw + 8) of every tile: lane l holds
+    // the index of key 8 lw + l % 8, then the warp copies the K and V rows of
+    // its keys with 16-byte cp.async (one row of 256 bytes per half-warp at
+    // d = 128) straight into the 128-byte-swizzled layout the MMA reads;
+    // unused rows are zero-filled.  Each thread's copies arrive on the stage's barrier as
     // they complete (cp.async.mbarrier.arrive), and lane 0 arrives once more
     // after publishing the warp's valid-key bits.
     const int lw = warp - kLoaderWarp0;
@@ -349,6 +401,35 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     int gi = 0;
     int s = 0;
     bool live = true;     // false once a wait gave up
+    const int kk = kKpw * lw + (lane % kKpw);   // key whose index this lane reads
+    // The I_verify entry of key kk is loaded one tile ahead, so that a tile's
+    // copies do not wait for its index to come back from memory.  The walk
+    // over (sequence, KV head, tile) of the prefetched tile advances by
+    // increments (no division on the loaders' path).
+    long long tp = t0;
+    int ptt = int(t0 % tiles_u), pg, pb;
+    {
+      const int pu = int(t0 / tiles_u);
+      pg = pu % A.hkv;
+      pb = (pu % units_per_layer) / A.hkv;
+    }
+    auto fetch_index = [&]() -> int {
+      int v = -1;
+      if (!A.dense && tp < t1 && ptt < ctx_tiles) {
+        const int jj = ptt * TK + kk;
+        if (jj < A.k) v = __ldg(A.ivf + size_t(pb) * A.k + jj);
+      }
+      ++tp;
+      if (++ptt == tiles_u) {
+        ptt = 0;
+        if (++pg == A.hkv) {
+          pg = 0;
+          if (++pb == A.B) pb = 0;
+        }
+      }
+      return v;
+    };
+    int raw_next = fetch_index();
     uint32_t tmask = 0;   // bit j: tile gi - 1 - j came by TMA boxes
     for (long long t = t0; t < t1 && live; ++s) {
       const Seg sg = next_seg(t, t1, tiles_u);
@@ -383,17 +464,13 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
       const uint16_t* kbase = Lr.k + size_t(b) * Lr.ksb + size_t(g) * Lr.ksh;
       const uint16_t* vbase = Lr.v + size_t(b) * Lr.vsb + size_t(g) * Lr.vsh;
       const size_t blk_off = (size_t(b) * A.hkv + g) * T * D;
-      const int kk = kKpw * lw + (lane % kKpw);   // key whose index this lane reads
       for (int i = 0; i < sg.n; ++i, ++gi) {
         const int tt = sg.ta + i;
         const bool blk = tt >= ctx_tiles;
-        int raw;                                 // loaded before the wait
+        int raw = raw_next;                      // this tile's index (sparse context tiles)
+        raw_next = fetch_index();
         if (blk) raw = kk;
         else if (A.dense) raw = tt * TK + kk;
-        else {
-          const int jj = tt * TK + kk;
-          raw = jj < A.k ? __ldg(A.ivf + size_t(b) * A.k + jj) : -1;
-        }
         const int st = int(gi % NSTAGE);
         if (gi >= NSTAGE &&
             !__all_sync(0xffffffffu, mbar_wait(&empty[st], uint32_t(gi / NSTAGE - 1) & 1u, A.err, abort_flag))) {
@@ -472,7 +549,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     // S = Q K^T of tile g into S buffer g % 2, once its rows have landed and
     // the softmax has read that buffer's previous tile (g - 2)
     if (lane == 0) {
-      constexpr uint32_t kIdS = tc_idesc(128, TK, 0);
+      constexpr uint32_t kIdS = tc_idesc(M, TK, 0);
       int gi = 0;
       int s = 0;
       bool issued = false;
@@ -517,7 +594,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     // segment overwrites O, which the softmax read for the previous segment
     // before it stored that P); the commit frees the tile's stage
     if (lane == 0) {
-      constexpr uint32_t kIdPV = tc_idesc(128, D, 1);
+      constexpr uint32_t kIdPV = tc_idesc(M, D, 1);
       const uint32_t o_tmem = tmem + Tm::o_col;
       int gi = 0;
       bool issued = false;
@@ -550,139 +627,321 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
     }
     __syncwarp();
   } else if (warp < n_act) {
-    // =============================================================== softmax
-    const int row = tid;             // query row == tensor-memory lane
-    const bool active = row < NQ;
-    const int tq_row = active ? row / GQ : 0;
-    const float scale = A.scale_log2;
-    const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-    const uint32_t o_lane = lane_base + uint32_t(Tm::o_col);
-    int gi = 0;
-    bool live = true;   // false once a wait gave up (warp-uniform)
-    for (long long t = t0; t < t1 && live;) {
-      const Seg sg = next_seg(t, t1, tiles_u);
-      const int u = sg.u, n = sg.n;
-      const int layer = u / units_per_layer;
-      const int b = (u % units_per_layer) / A.hkv;
-      const int g = u % A.hkv;
-      const VerifyLayerDev& Lr = A.layer[layer];
-      float mref = -INFINITY, lsum = 0.f;   // reference max (log2 domain) and row sum
-      for (int i = 0; i < n; ++i, ++gi) {
-        const int st = int(gi % NSTAGE);
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[st], uint32_t(gi / NSTAGE) & 1u, A.err, abort_flag) &&
-                                         mbar_wait(&s_full[gi & 1], uint32_t(gi >> 1) & 1u, A.err, abort_flag))) {
-          live = false;
-          break;
-        }
-        const unsigned long long mw = *reinterpret_cast<const unsigned long long*>(masks + st * kLoaders);
-        const bool blk = sg.ta + i >= ctx_tiles;
-        tc_fence_after();
-        float s[TK];
-        tc_ld32(lane_base + uint32_t(kSCol + (gi & 1) * TK), reinterpret_cast<uint32_t*>(s));
-        tc_ld32(lane_base + uint32_t(kSCol + (gi & 1) * TK + 32), reinterpret_cast<uint32_t*>(s + 32));
-        if (blk || mw != ~0ull) {
-          // rows the tile does not use (and, in the block tile, u > t) get -inf
-#pragma unroll
-          for (int j = 0; j < TK; ++j) {
-            const bool valid = ((mw >> j) & 1ull) != 0 && (!blk || j <= tq_row);
-            s[j] = valid ? s[j] : -INFINITY;
-          }
-        }
-        // raw row max (the scale is positive)
-        float m8[8];
-#pragma unroll
-        for (int x = 0; x < 8; ++x)
-          m8[x] = fmaxf(fmaxf(fmaxf(s[x], s[x + 8]), fmaxf(s[x + 16], s[x + 24])),
-                        fmaxf(fmaxf(s[x + 32], s[x + 40]), fmaxf(s[x + 48], s[x + 56])));
-        // (a query row past NQ has an S row computed from whatever lies past
-        // the query rows: its max is taken as -inf, so it never rescales O;
-        // its P and O rows are never read)
-        const float mx = active ? fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                        fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * scale
-                                : -INFINITY;
-        float alpha = 1.f;
-        if (mx > mref + 8.f) {   // also the first tile with a valid key
-          alpha = fast_exp2(mref - mx);   // 0 while mref is -inf
-          mref = mx;
-          lsum *= alpha;
-        }
-        const float nb = (mref == -INFINITY) ? 0.f : -mref;
-        uint32_t pk[TK / 2];
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < TK; j += 2) {
-          const uint32_t v = pack_bf16(fast_exp2(fmaf(s[j], scale, nb)), fast_exp2(fmaf(s[j + 1], scale, nb)));
-          pk[j / 2] = v;
-          ls[(j >> 1) & 3] += __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
-        }
-        lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        // rescale this row of O once P V of the previous tile is in (the
-        // first tile of a segment overwrites O); tensor-memory loads and
-        // stores are collective, so the whole warp takes part
-        if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 1) % NSTAGE], uint32_t((gi - 1) / NSTAGE) & 1u,
-                                                 A.err, abort_flag))) {
+    if constexpr (M == 64) {
+      // ====================================================== softmax (M = 64)
+      // Warp w holds query rows 16 w .. 16 w + 15 (lanes 32 w .. 32 w + 15).
+      // Thread t takes rows r0 = 16 w + t / 4 and r1 = r0 + 8 and, of each, the
+      // keys 8 c + 2 (t % 4) + {0, 1} of the eight 8-key chunks c (16x256b
+      // loads).  The four threads of a quad share their rows' maxima by
+      // shuffles and keep partial row sums, added up in the epilogue.  P goes
+      // back with the 16x128b shape, whose column t % 4 of each 4-column chunk
+      // is exactly this thread's bf16 pair of keys.
+      const int q4 = lane & 3;
+      const int r0 = 16 * warp + (lane >> 2), r1 = r0 + 8;
+      const bool act0 = r0 < NQ, act1 = r1 < NQ;
+      const int tq0 = act0 ? r0 / GQ : 0, tq1 = act1 ? r1 / GQ : 0;
+      const float scale = A.scale_log2;
+      const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+      const uint32_t o_lane = lane_base + uint32_t(Tm::o_col);
+      int gi = 0;
+      bool live = true;   // false once a wait gave up (warp-uniform)
+      for (long long t = t0; t < t1 && live;) {
+        const Seg sg = next_seg(t, t1, tiles_u);
+        const int u = sg.u, n = sg.n;
+        const int layer = u / units_per_layer;
+        const int b = (u % units_per_layer) / A.hkv;
+        const int g = u % A.hkv;
+        const VerifyLayerDev& Lr = A.layer[layer];
+        float mref0 = -INFINITY, mref1 = -INFINITY;   // reference maxima (log2 domain)
+        float lsum0 = 0.f, lsum1 = 0.f;               // this thread's share of the row sums
+        for (int i = 0; i < n; ++i, ++gi) {
+          const int st = int(gi % NSTAGE);
+          if (!__all_sync(0xffffffffu, mbar_wait(&full[st], uint32_t(gi / NSTAGE) & 1u, A.err, abort_flag) &&
+                                           mbar_wait(&s_full[gi & 1], uint32_t(gi >> 1) & 1u, A.err, abort_flag))) {
             live = false;
             break;
           }
+          const unsigned long long mw = *reinterpret_cast<const unsigned long long*>(masks + st * kLoaders);
+          const bool blk = sg.ta + i >= ctx_tiles;
           tc_fence_after();
-#pragma unroll 1
+          float x0[16], x1[16];   // scores of rows r0, r1: entry 2 c + e is key 8 c + 2 q4 + e
+          {
+            uint32_t sv[32];
+            tc_ld16x256_x8(lane_base + uint32_t(kSCol + (gi & 1) * TK), sv);
+  #pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              x0[2 * c] = __uint_as_float(sv[4 * c]);
+              x0[2 * c + 1] = __uint_as_float(sv[4 * c + 1]);
+              x1[2 * c] = __uint_as_float(sv[4 * c + 2]);
+              x1[2 * c + 1] = __uint_as_float(sv[4 * c + 3]);
+            }
+          }
+          if (blk || mw != ~0ull) {
+            // keys the tile does not use (and, in the block tile, u > t) get -inf
+  #pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int key = 8 * (j >> 1) + 2 * q4 + (j & 1);
+              const bool v = ((mw >> key) & 1ull) != 0;
+              x0[j] = v && (!blk || key <= tq0) ? x0[j] : -INFINITY;
+              x1[j] = v && (!blk || key <= tq1) ? x1[j] : -INFINITY;
+            }
+          }
+          float m0 = x0[0], m1 = x1[0];
+  #pragma unroll
+          for (int j = 1; j < 16; ++j) {
+            m0 = fmaxf(m0, x0[j]);
+            m1 = fmaxf(m1, x1[j]);
+          }
+          m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+          m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+          // (a row past NQ takes -inf as its max: it never rescales O, and its
+          // P and O rows are never read)
+          const float mx0 = act0 ? m0 * scale : -INFINITY, mx1 = act1 ? m1 * scale : -INFINITY;
+          float alpha0 = 1.f, alpha1 = 1.f;
+          if (mx0 > mref0 + 8.f) {
+            alpha0 = fast_exp2(mref0 - mx0);
+            mref0 = mx0;
+            lsum0 *= alpha0;
+          }
+          if (mx1 > mref1 + 8.f) {
+            alpha1 = fast_exp2(mref1 - mx1);
+            mref1 = mx1;
+            lsum1 *= alpha1;
+          }
+          const float nb0 = (mref0 == -INFINITY) ? 0.f : -mref0;
+          const float nb1 = (mref1 == -INFINITY) ? 0.f : -mref1;
+          uint32_t pk[16];   // 16x128b order: pk[2 c] row r0, pk[2 c + 1] row r1
+          float la[2] = {0.f, 0.f}, lb[2] = {0.f, 0.f};
+  #pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t v0 = pack_bf16(fast_exp2(fmaf(x0[2 * c], scale, nb0)), fast_exp2(fmaf(x0[2 * c + 1], scale, nb0)));
+            const uint32_t v1 = pack_bf16(fast_exp2(fmaf(x1[2 * c], scale, nb1)), fast_exp2(fmaf(x1[2 * c + 1], scale, nb1)));
+            pk[2 * c] = v0;
+            pk[2 * c + 1] = v1;
+            la[c & 1] += __uint_as_float(v0 << 16) + __uint_as_float(v0 & 0xFFFF0000u);
+            lb[c & 1] += __uint_as_float(v1 << 16) + __uint_as_float(v1 & 0xFFFF0000u);
+          }
+          lsum0 += la[0] + la[1];
+          lsum1 += lb[0] + lb[1];
+          // rescale this thread's O rows once P V of the previous tile is in
+          if (i > 0 && __any_sync(0xffffffffu, alpha0 != 1.f || alpha1 != 1.f)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 1) % NSTAGE], uint32_t((gi - 1) / NSTAGE) & 1u,
+                                                   A.err, abort_flag))) {
+              live = false;
+              break;
+            }
+            tc_fence_after();
+  #pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t o[16];
+              tc_ld16x256_x4(o_lane + uint32_t(c), o);
+  #pragma unroll
+              for (int x = 0; x < 16; ++x)
+                o[x] = __float_as_uint(__uint_as_float(o[x]) * ((x & 2) ? alpha1 : alpha0));
+              tc_st16x256_x4(o_lane + uint32_t(c), o);
+            }
+          }
+          // P buffer gi % 2 is free once P V of tile gi - 2 has completed
+          if (gi >= 2 && !__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 2) % NSTAGE],
+                                                           uint32_t((gi - 2) / NSTAGE) & 1u, A.err,
+                                                           abort_flag))) {
+            live = false;
+            break;
+          }
+          tc_st16x128_x8(lane_base + uint32_t(kPCol + (gi & 1) * (TK / 2)), pk);
+          tc_fence_before();
+          mbar_arrive(&p_full[gi & 1]);
+        }
+
+        if (!live) break;
+        // ----------------------------------------------------------- epilogue
+        lsum0 += __shfl_xor_sync(0xffffffffu, lsum0, 1);
+        lsum1 += __shfl_xor_sync(0xffffffffu, lsum1, 1);
+        lsum0 += __shfl_xor_sync(0xffffffffu, lsum0, 2);
+        lsum1 += __shfl_xor_sync(0xffffffffu, lsum1, 2);
+        const int seg_first = cta_of((long long)u * tiles_u, total, G);
+        const int seg_last = cta_of((long long)u * tiles_u + tiles_u - 1, total, G);
+        const int n_seg = seg_last - seg_first + 1;
+        const int seg = blockIdx.x - seg_first;
+        const size_t slot_floats = size_t(A.slot_floats);   // NQ*D + 2*NQ, rounded to 4
+        float* part = A.partial + (size_t(u) * A.max_seg + seg) * slot_floats;
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 1) % NSTAGE], uint32_t((gi - 1) / NSTAGE) & 1u,
+                                               A.err, abort_flag))) {
+          live = false;
+        } else {
+          tc_fence_after();
+          const int ra = act0 ? r0 : 0, rb = act1 ? r1 : 0;
+          float* d0 = n_seg == 1 ? Lr.o + ((size_t(b) * T + ra / GQ) * A.hq + size_t(g) * GQ + ra % GQ) * D
+                                 : part + size_t(ra) * D;
+          float* d1 = n_seg == 1 ? Lr.o + ((size_t(b) * T + rb / GQ) * A.hq + size_t(g) * GQ + rb % GQ) * D
+                                 : part + size_t(rb) * D;
+          const float os0 = n_seg == 1 ? (lsum0 > 0.f ? 1.f / lsum0 : 0.f) : 1.f;
+          const float os1 = n_seg == 1 ? (lsum1 > 0.f ? 1.f / lsum1 : 0.f) : 1.f;
+  #pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[16];
+            tc_ld16x256_x4(o_lane + uint32_t(c), o);   // collective: every lane loads
+  #pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const int col = c + 8 * cc + 2 * q4;
+              if (act0)
+                *reinterpret_cast<float2*>(d0 + col) =
+                    make_float2(__uint_as_float(o[4 * cc]) * os0, __uint_as_float(o[4 * cc + 1]) * os0);
+              if (act1)
+                *reinterpret_cast<float2*>(d1 + col) =
+                    make_float2(__uint_as_float(o[4 * cc + 2]) * os1, __uint_as_float(o[4 * cc + 3]) * os1);
+            }
+          }
+          if (n_seg > 1 && q4 == 0) {
+            if (act0) {
+              part[size_t(NQ) * D + r0] = mref0;
+              part[size_t(NQ) * D + NQ + r0] = lsum0;
+            }
+            if (act1) {
+              part[size_t(NQ) * D + r1] = mref1;
+              part[size_t(NQ) * D + NQ + r1] = lsum1;
+            }
+          }
+        }
+        tc_fence_before();
+      }
+    } else {
+      // =============================================================== softmax
+      const int row = tid;             // query row == tensor-memory lane
+      const bool active = row < NQ;
+      const int tq_row = active ? row / GQ : 0;
+      const float scale = A.scale_log2;
+      const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+      const uint32_t o_lane = lane_base + uint32_t(Tm::o_col);
+      int gi = 0;
+      bool live = true;   // false once a wait gave up (warp-uniform)
+      for (long long t = t0; t < t1 && live;) {
+        const Seg sg = next_seg(t, t1, tiles_u);
+        const int u = sg.u, n = sg.n;
+        const int layer = u / units_per_layer;
+        const int b = (u % units_per_layer) / A.hkv;
+        const int g = u % A.hkv;
+        const VerifyLayerDev& Lr = A.layer[layer];
+        float mref = -INFINITY, lsum = 0.f;   // reference max (log2 domain) and row sum
+        for (int i = 0; i < n; ++i, ++gi) {
+          const int st = int(gi % NSTAGE);
+          if (!__all_sync(0xffffffffu, mbar_wait(&full[st], uint32_t(gi / NSTAGE) & 1u, A.err, abort_flag) &&
+                                           mbar_wait(&s_full[gi & 1], uint32_t(gi >> 1) & 1u, A.err, abort_flag))) {
+            live = false;
+            break;
+          }
+          const unsigned long long mw = *reinterpret_cast<const unsigned long long*>(masks + st * kLoaders);
+          const bool blk = sg.ta + i >= ctx_tiles;
+          tc_fence_after();
+          float s[TK];
+          tc_ld32(lane_base + uint32_t(kSCol + (gi & 1) * TK), reinterpret_cast<uint32_t*>(s));
+          tc_ld32(lane_base + uint32_t(kSCol + (gi & 1) * TK + 32), reinterpret_cast<uint32_t*>(s + 32));
+          if (blk || mw != ~0ull) {
+            // rows the tile does not use (and, in the block tile, u > t) get -inf
+  #pragma unroll
+            for (int j = 0; j < TK; ++j) {
+              const bool valid = ((mw >> j) & 1ull) != 0 && (!blk || j <= tq_row);
+              s[j] = valid ? s[j] : -INFINITY;
+            }
+          }
+          // raw row max (the scale is positive)
+          float m8[8];
+  #pragma unroll
+          for (int x = 0; x < 8; ++x)
+            m8[x] = fmaxf(fmaxf(fmaxf(s[x], s[x + 8]), fmaxf(s[x + 16], s[x + 24])),
+                          fmaxf(fmaxf(s[x + 32], s[x + 40]), fmaxf(s[x + 48], s[x + 56])));
+          // (a query row past NQ has an S row computed from whatever lies past
+          // the query rows: its max is taken as -inf, so it never rescales O;
+          // its P and O rows are never read)
+          const float mx = active ? fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                          fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * scale
+                                  : -INFINITY;
+          float alpha = 1.f;
+          if (mx > mref + 8.f) {   // also the first tile with a valid key
+            alpha = fast_exp2(mref - mx);   // 0 while mref is -inf
+            mref = mx;
+            lsum *= alpha;
+          }
+          const float nb = (mref == -INFINITY) ? 0.f : -mref;
+          uint32_t pk[TK / 2];
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+          for (int j = 0; j < TK; j += 2) {
+            const uint32_t v = pack_bf16(fast_exp2(fmaf(s[j], scale, nb)), fast_exp2(fmaf(s[j + 1], scale, nb)));
+            pk[j / 2] = v;
+            ls[(j >> 1) & 3] += __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
+          }
+          lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          // rescale this row of O once P V of the previous tile is in (the
+          // first tile of a segment overwrites O); tensor-memory loads and
+          // stores are collective, so the whole warp takes part
+          if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 1) % NSTAGE], uint32_t((gi - 1) / NSTAGE) & 1u,
+                                                   A.err, abort_flag))) {
+              live = false;
+              break;
+            }
+            tc_fence_after();
+  #pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t o[32];
+              tc_ld32(o_lane + uint32_t(c), o);
+  #pragma unroll
+              for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+              tc_st32(o_lane + uint32_t(c), o);
+            }
+          }
+          // P buffer gi % 2 is free once P V of tile gi - 2 has completed (the
+          // two issuers' MMAs are not ordered with each other)
+          if (gi >= 2 && !__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 2) % NSTAGE],
+                                                           uint32_t((gi - 2) / NSTAGE) & 1u, A.err,
+                                                           abort_flag))) {
+            live = false;
+            break;
+          }
+          tc_st32(lane_base + uint32_t(kPCol + (gi & 1) * (TK / 2)), pk);
+          tc_fence_before();
+          mbar_arrive(&p_full[gi & 1]);
+        }
+
+        if (!live) break;
+        // ----------------------------------------------------------- epilogue
+        const int seg_first = cta_of((long long)u * tiles_u, total, G);
+        const int seg_last = cta_of((long long)u * tiles_u + tiles_u - 1, total, G);
+        const int n_seg = seg_last - seg_first + 1;
+        const int seg = blockIdx.x - seg_first;
+        const size_t slot_floats = size_t(A.slot_floats);   // NQ*D + 2*NQ, rounded to 4
+        float* part = A.partial + (size_t(u) * A.max_seg + seg) * slot_floats;
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 1) % NSTAGE], uint32_t((gi - 1) / NSTAGE) & 1u,
+                                               A.err, abort_flag))) {
+          live = false;
+        } else {
+          tc_fence_after();
+          const int tq = active ? row / GQ : 0, hl = active ? row - (row / GQ) * GQ : 0;
+          float* dst = n_seg == 1 ? Lr.o + ((size_t(b) * T + tq) * A.hq + size_t(g) * GQ + hl) * D
+                                  : part + size_t(active ? row : 0) * D;
+          const float osc = n_seg == 1 ? (lsum > 0.f ? 1.f / lsum : 0.f) : 1.f;
+  #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
             uint32_t o[32];
-            tc_ld32(o_lane + uint32_t(c), o);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-            tc_st32(o_lane + uint32_t(c), o);
+            tc_ld32(o_lane + uint32_t(c), o);   // collective: every lane loads
+            if (active) {
+  #pragma unroll
+              for (int x = 0; x < 32; x += 4)
+                *reinterpret_cast<float4*>(dst + c + x) =
+                    make_float4(__uint_as_float(o[x]) * osc, __uint_as_float(o[x + 1]) * osc,
+                                __uint_as_float(o[x + 2]) * osc, __uint_as_float(o[x + 3]) * osc);
+            }
+          }
+          if (active && n_seg > 1) {
+            part[size_t(NQ) * D + row] = mref;
+            part[size_t(NQ) * D + NQ + row] = lsum;
           }
         }
-        // P buffer gi % 2 is free once P V of tile gi - 2 has completed (the
-        // two issuers' MMAs are not ordered with each other)
-        if (gi >= 2 && !__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 2) % NSTAGE],
-                                                         uint32_t((gi - 2) / NSTAGE) & 1u, A.err,
-                                                         abort_flag))) {
-          live = false;
-          break;
-        }
-        tc_st32(lane_base + uint32_t(kPCol + (gi & 1) * (TK / 2)), pk);
         tc_fence_before();
-        mbar_arrive(&p_full[gi & 1]);
       }
-
-      if (!live) break;
-      // ----------------------------------------------------------- epilogue
-      const int seg_first = cta_of((long long)u * tiles_u, total, G);
-      const int seg_last = cta_of((long long)u * tiles_u + tiles_u - 1, total, G);
-      const int n_seg = seg_last - seg_first + 1;
-      const int seg = blockIdx.x - seg_first;
-      const size_t slot_floats = size_t(A.slot_floats);   // NQ*D + 2*NQ, rounded to 4
-      float* part = A.partial + (size_t(u) * A.max_seg + seg) * slot_floats;
-      if (!__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 1) % NSTAGE], uint32_t((gi - 1) / NSTAGE) & 1u,
-                                             A.err, abort_flag))) {
-        live = false;
-      } else {
-        tc_fence_after();
-        const int tq = active ? row / GQ : 0, hl = active ? row - (row / GQ) * GQ : 0;
-        float* dst = n_seg == 1 ? Lr.o + ((size_t(b) * T + tq) * A.hq + size_t(g) * GQ + hl) * D
-                                : part + size_t(active ? row : 0) * D;
-        const float osc = n_seg == 1 ? (lsum > 0.f ? 1.f / lsum : 0.f) : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t o[32];
-          tc_ld32(o_lane + uint32_t(c), o);   // collective: every lane loads
-          if (active) {
-#pragma unroll
-            for (int x = 0; x < 32; x += 4)
-              *reinterpret_cast<float4*>(dst + c + x) =
-                  make_float4(__uint_as_float(o[x]) * osc, __uint_as_float(o[x + 1]) * osc,
-                              __uint_as_float(o[x + 2]) * osc, __uint_as_float(o[x + 3]) * osc);
-          }
-        }
-        if (active && n_seg > 1) {
-          part[size_t(NQ) * D + row] = mref;
-          part[size_t(NQ) * D + NQ + row] = lsum;
-        }
-      }
-      tc_fence_before();
     }
   }
 
@@ -751,13 +1010,19 @@ __global__ void __launch_bounds__(kCombineThreads) verify_combine_kernel(const _
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
-template <int D>
-cudaError_t launch_t(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t stream) {
-  auto kern = verify_kernel<D>;
+template <int D, int M>
+cudaError_t launch_main(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t stream) {
+  auto kern = verify_kernel<D, M>;
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kVerifySmem));
   if (attr != cudaSuccess) return attr;
-  cudaError_t e = launch_pdl(kern, dim3(pl.grid), dim3(NTH), pl.smem, stream, a);
+  return launch_pdl(kern, dim3(pl.grid), dim3(NTH), pl.smem, stream, a);
+}
+
+template <int D>
+cudaError_t launch_t(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t stream) {
+  // 64-row MMAs while the query rows fit them (NQ <= 64)
+  cudaError_t e = a.NQ <= 64 ? launch_main<D, 64>(a, pl, stream) : launch_main<D, 128>(a, pl, stream);
   if (e != cudaSuccess) return e;
   VerifyCombineArgs c;
   c.NQ = a.NQ;

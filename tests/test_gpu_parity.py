@@ -215,6 +215,28 @@ def test_verify_gamma_range(gamma):
     assert_attention(od, c.oracle_dense())
 
 
+@pytest.mark.parametrize("gamma,hq,hkv,d", [(12, 24, 8, 128), (7, 64, 8, 128), (20, 3, 1, 64),
+                                             (21, 3, 1, 64)])
+def test_verify_query_rows_near_mma_width(gamma, hq, hkv, d):
+    """(gamma + 1) * Hq / Hkv query rows of 39, 64, 63 and 66: up to 64 the
+    verification MMAs are 64 rows wide (16 rows in each tensor-memory lane
+    quarter, the last quarter partly or wholly in use), beyond it 128 rows
+    wide; row counts that are not multiples of 8 included."""
+    wl = WORKLOADS["tiny"].with_(gamma=gamma, Hq=hq, Hkv=hkv, d=d, L=1024, k=256, sinks=4,
+                                 window=64, m=64)
+    c = Case(wl)
+    x = c.x
+    rng = np.random.default_rng(gamma * 7 + d)
+    I_ref = np.stack([np.sort(rng.choice(wl.L, wl.k, replace=False)) for _ in range(wl.B)]).astype(np.int64)
+    I = torch.as_tensor(I_ref.astype(np.int32), device="cuda")
+    ws = dk.workspace(c.p, verify=(hq, hkv, d, 1))
+    o = dk.dustin_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], I, c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    assert_attention(o, c.oracle_verify(I_ref))
+    od = dk.dense_verify_attn(c.p, x.Q[0], x.K[0], x.V[0], x.Kb[0], x.Vb[0], c.seq, ws=ws)
+    assert_attention(od, c.oracle_dense())
+
+
 @pytest.mark.parametrize("d,hq,hkv", [(64, 2, 1), (128, 16, 8)])
 def test_verify_largest_draft_block(d, hq, hkv):
     """gamma + 1 = 64 draft-block rows (one whole block tile under the causal
