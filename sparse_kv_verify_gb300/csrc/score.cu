@@ -453,8 +453,9 @@ __global__ void __launch_bounds__(kNormThreads, 2) score_norm_kernel(const __gri
     if (bf) src1 = src;
     else src0 = src;
   };
+  // item 0's copies go out first; item 1's wait until the statistics loads
+  // below have been served, so that those do not queue behind its rows
   if (n_items > 0) issue(0);
-  if (n_items > 1) issue(1);
   int L = A.seq_len[b];
   if (L < 0 || L > A.Lcap) L = 0;
   // merged statistics, one row per thread: M and 1 / S over the segments
@@ -479,6 +480,7 @@ __global__ void __launch_bounds__(kNormThreads, 2) score_norm_kernel(const __gri
     Mg[row] = m;
     Ig[row] = sm > 0.f ? 1.f / sm : 0.f;
   }
+  if (n_items > 1) issue(1);
   __syncthreads();
   const int s_eff = min(A.sinks, L);
   const int w0 = max(L - A.window, s_eff);
