@@ -984,22 +984,47 @@ __global__ void __launch_bounds__(kCombineThreads) verify_combine_kernel(const _
   const size_t slot = size_t(C.slot_floats);
   const float* base0 = C.partial + size_t(u) * C.max_seg * slot;
   const size_t mo = size_t(C.NQ) * D;   // m at mo + r, l at mo + NQ + r
+  // the (m, l, O) of up to four segments are loaded at once (one round trip
+  // to memory), then merged; more segments are taken in further rounds
   float M = -INFINITY;
-#pragma unroll 4
-  for (int s2 = 0; s2 < n_seg; ++s2) M = fmaxf(M, __ldg(base0 + s2 * slot + mo + r));
-  const float bv = (M == -INFINITY) ? 0.f : M;
   float lsc = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int s2 = 0; s2 < n_seg; ++s2) {
-    const float* ps = base0 + s2 * slot;
-    const float w = exp2f(__ldg(ps + mo + r) - bv);
-    lsc += w * __ldg(ps + mo + C.NQ + r);
-    const float4 x = __ldg(reinterpret_cast<const float4*>(ps + size_t(r) * D) + c4);
-    acc.x += w * x.x;
-    acc.y += w * x.y;
-    acc.z += w * x.z;
-    acc.w += w * x.w;
+  for (int g0 = 0; g0 < n_seg; g0 += 4) {
+    float mv[4], lv[4];
+    float4 xv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      mv[u] = -INFINITY;
+      lv[u] = 0.f;
+      xv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g0 + u < n_seg) {
+        const float* ps = base0 + size_t(g0 + u) * slot;
+        mv[u] = __ldg(ps + mo + r);
+        lv[u] = __ldg(ps + mo + C.NQ + r);
+        xv[u] = __ldg(reinterpret_cast<const float4*>(ps + size_t(r) * D) + c4);
+      }
+    }
+    float Mn = M;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) Mn = fmaxf(Mn, mv[u]);
+    const float bv = (Mn == -INFINITY) ? 0.f : Mn;
+    // rescale what the earlier rounds merged to the new reference
+    const float a = (M == -INFINITY) ? 0.f : exp2f(M - bv);
+    lsc *= a;
+    acc.x *= a;
+    acc.y *= a;
+    acc.z *= a;
+    acc.w *= a;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = (mv[u] == -INFINITY) ? 0.f : exp2f(mv[u] - bv);
+      lsc += w * lv[u];
+      acc.x += w * xv[u].x;
+      acc.y += w * xv[u].y;
+      acc.z += w * xv[u].z;
+      acc.w += w * xv[u].w;
+    }
+    M = Mn;
   }
   const float inv = lsc > 0.f ? 1.f / lsc : 0.f;
   const int layer = u / C.units_per_layer;
