@@ -390,14 +390,16 @@ __device__ __forceinline__ int slab_of_row(const SlabInfo* si, int ns, int r) {
 
 // Normalise kernel: over one or two stream launches' groups (a.ng), cps CTAs
 // per sequence, each owning the 256-position chunks x = r, r + cps, ... of its
-// sequence.  A work item is
-// (chunk, batch of up to kNormRowsMax logits rows); items go through two
-// shared-memory buffers, so the bulk copies of item i + 2 (one per row,
-// issued by eight warps) are in flight while item i is computed.  Each
-// issuing thread arms the buffer's mbarrier for its own row (arrive +
-// expected bytes), so a refill needs one block barrier.  Thread t owns
-// position t of a chunk.
-__global__ void __launch_bounds__(kNormThreads, 2) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
+// sequence.  A work item is (chunk, batch of up to kNormRowsMax logits rows).
+// Warp kNormWarps (the producer) bulk-copies each item's rows (one copy per
+// row, completion on the buffer's full barrier) into one of two
+// shared-memory buffers as soon as the compute warps have released it (their
+// empty barrier), so no compute warp issues copies or waits on a block
+// barrier.  Compute thread t owns position t of a chunk.
+constexpr int kNormWarps = kNormThreads / 32;              // compute warps
+constexpr int kNormBlock = kNormThreads + 32;              // plus the producer warp
+
+__global__ void __launch_bounds__(kNormBlock, 2) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
   extern __shared__ __align__(128) unsigned char nsm[];
   __shared__ SlabInfo si[DUSTIN_MAX_SRH];
   const int nr = A.n_rows, n0 = A.n_rows0, ns = A.n_slab;
@@ -405,8 +407,9 @@ __global__ void __launch_bounds__(kNormThreads, 2) score_norm_kernel(const __gri
   float* lg = reinterpret_cast<float*>(nsm);                       // [2][nbr][256]
   float* Mg = lg + size_t(2) * nbr * kNormThreads;                 // [nr]
   float* Ig = Mg + nr;                                              // [nr]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(Ig + nr);            // [2]; 2 nr floats above
-  const int tid = threadIdx.x, lane = tid & 31;
+  uint64_t* full = reinterpret_cast<uint64_t*>(Ig + nr);           // [2]; 2 nr floats above
+  uint64_t* empty = full + 2;                                       // [2]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gr = (A.n_groups > 1 && int(blockIdx.x) >= A.ng[0].nb * A.ng[0].cps) ? 1 : 0;
   const NormGroup& NG = A.ng[gr];
   const int cps = NG.cps;
@@ -420,42 +423,51 @@ __global__ void __launch_bounds__(kNormThreads, 2) score_norm_kernel(const __gri
   const int n_items = my_chunks * nbat;
   // the slab table: one parameter word per thread, all loads in flight at once
   constexpr int kInfoWords = int(sizeof(SlabInfo) / 4);
-  for (int j = tid; j < ns * kInfoWords; j += kNormThreads)
+  for (int j = tid; j < ns * kInfoWords; j += kNormBlock)
     reinterpret_cast<int*>(si)[j] = reinterpret_cast<const int*>(A.info[gr])[j];
   if (tid == 0) {
-    mbar_init(&bar[0], nbr);
-    mbar_init(&bar[1], nbr);
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(&empty[0], kNormWarps);
+    mbar_init(&empty[1], kNormWarps);
     fence_barrier_init();
   }
   pdl_launch_dependents();
   pdl_wait();
   __syncthreads();
-  // Item it = (chunk r + (it / nbat) cps, batch it % nbat) into buffer it % 2.
-  // Batch row q is issued by thread 32 (q % 8) + q / 8 (eight warps share it).
-  const int q = (tid & 31) * 8 + (tid >> 5);
-  const float* src0 = nullptr;   // this thread's row in buffer 0 ...
-  const float* src1 = nullptr;   // ... and in buffer 1
-  auto issue = [&](int it) {
-    const int x = r + (it / nbat) * cps, k = it - (it / nbat) * nbat;
-    const int r0 = k * kNormRowsMax, n = min(kNormRowsMax, nr - r0);
-    const int base = x * kNormThreads, npos = min(kNormThreads, A.LSP - base);
-    const int bf = it & 1;
-    const float* src = nullptr;
-    if (tid < 8 * 32 && q < nbr) {
-      if (q < n) {
-        const int row = r0 + q;
-        const int j = slab_of_row(si, ns, row);
-        src = logits + si[j].logit_off + (size_t(bl) * si[j].npairs + (row - si[j].row0)) * A.LSP + base;
-      }
-      mbar_arrive_expect_tx(&bar[bf], src ? uint32_t(npos) * 4 : 0u);
-      if (src) bulk_g2s(lg + (size_t(bf) * nbr + q) * kNormThreads, src, uint32_t(npos) * 4, &bar[bf]);
-    }
-    if (bf) src1 = src;
-    else src0 = src;
+  // Item it = (chunk r + (it / nbat) cps, batch it % nbat) in buffer it % 2.
+  // Logits row `row` of the item starting at position `base`.
+  auto row_src = [&](int row, int base) -> const float* {
+    const int j = slab_of_row(si, ns, row);
+    return logits + si[j].logit_off + (size_t(bl) * si[j].npairs + (row - si[j].row0)) * A.LSP + base;
   };
-  // item 0's copies go out first; item 1's wait until the statistics loads
-  // below have been served, so that those do not queue behind its rows
-  if (n_items > 0) issue(0);
+  if (warp == kNormWarps) {
+    // ------------------------------------------------------------- producer
+    auto issue = [&](int it) {
+      const int x = r + (it / nbat) * cps, k = it - (it / nbat) * nbat;
+      const int r0 = k * kNormRowsMax, n = min(kNormRowsMax, nr - r0);
+      const int base = x * kNormThreads, npos = min(kNormThreads, A.LSP - base);
+      const int bf = it & 1;
+      if (lane == 0) mbar_arrive_expect_tx(&full[bf], uint32_t(n) * uint32_t(npos) * 4u);
+      __syncwarp();
+      for (int q = lane; q < n; q += 32)
+        bulk_g2s(lg + (size_t(bf) * nbr + q) * kNormThreads, row_src(r0 + q, base), uint32_t(npos) * 4,
+                 &full[bf]);
+    };
+    // item 0 at once; item 1 once the statistics loads below have been served
+    // (so that they do not queue behind its rows); then each item as soon as
+    // its buffer is released
+    if (n_items > 0) issue(0);
+    named_bar(2, kNormBlock);
+    for (int it = 1; it < n_items; ++it) {
+      if (it >= 2 && !__all_sync(0xffffffffu, mbar_wait(&empty[it & 1], uint32_t((it >> 1) - 1) & 1u,
+                                                          A.err, nullptr)))
+        break;
+      issue(it);
+    }
+    return;
+  }
+  // ------------------------------------------------------------- compute
   int L = A.seq_len[b];
   if (L < 0 || L > A.Lcap) L = 0;
   // merged statistics, one row per thread: M and 1 / S over the segments
@@ -480,8 +492,7 @@ __global__ void __launch_bounds__(kNormThreads, 2) score_norm_kernel(const __gri
     Mg[row] = m;
     Ig[row] = sm > 0.f ? 1.f / sm : 0.f;
   }
-  if (n_items > 1) issue(1);
-  __syncthreads();
+  named_bar(2, kNormBlock);   // Mg, Ig complete (and the producer may issue item 1)
   const int s_eff = min(A.sinks, L);
   const int w0 = max(L - A.window, s_eff);
   int* h = A.hist ? A.hist + size_t(b) * 2 * kSelectBins : nullptr;
@@ -491,12 +502,14 @@ __global__ void __launch_bounds__(kNormThreads, 2) score_norm_kernel(const __gri
     const int x = r + (it / nbat) * cps, k = it - (it / nbat) * nbat;
     const int r0 = k * kNormRowsMax, n = min(kNormRowsMax, nr - r0);
     const int base = x * kNormThreads, npos = min(kNormThreads, A.LSP - base);
-    mbar_wait(&bar[bf], uint32_t(it >> 1) & 1u, A.err, nullptr);
-    // this thread's row has landed: drop its lines from L2 without write-back
-    // (the logits are dead once staged)
-    if (const float* src = bf ? src1 : src0)
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[bf], uint32_t(it >> 1) & 1u, A.err, nullptr))) break;
+    // row tid has landed: drop its lines from L2 without write-back (the
+    // logits are dead once staged)
+    if (tid < n) {
+      const float* src = row_src(r0 + tid, base);
       for (int ln = 0; ln < npos * 4 / 128; ++ln)
         asm volatile("discard.global.L2 [%0], 128;" ::"l"(src + ln * 32) : "memory");
+    }
     if (tid < npos) {
       const float* lb = lg + size_t(bf) * nbr * kNormThreads + tid;
 #pragma unroll 4
@@ -507,6 +520,9 @@ __global__ void __launch_bounds__(kNormThreads, 2) score_norm_kernel(const __gri
         else acc1 += v;
       }
     }
+    // this warp is done with the buffer
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[bf]);
     if (k == nbat - 1) {   // the chunk's last batch: write it
       const int pos = base + tid;
       const bool live = pos < L;
@@ -521,10 +537,6 @@ __global__ void __launch_bounds__(kNormThreads, 2) score_norm_kernel(const __gri
         hist_red(h + kSelectBins, in_u ? select_bin(importance_key(acc1, A.err)) : 0u, in_u, lane);
       }
       acc0 = acc1 = 0.f;
-    }
-    if (it + 2 < n_items) {
-      __syncthreads();   // every thread is done with this buffer
-      issue(it + 2);
     }
   }
 }
@@ -545,13 +557,13 @@ size_t score_stream_smem() {
 
 size_t score_norm_smem(int n_rows) {
   const int nb = n_rows < kNormRowsMax ? n_rows : kNormRowsMax;
-  return size_t(2) * nb * kNormThreads * 4 + size_t(2 * n_rows) * 4 + 2 * 8 + 16;
+  return size_t(2) * nb * kNormThreads * 4 + size_t(2 * n_rows) * 4 + 4 * 8 + 16;
 }
 
 int score_norm_ctas_per_sm(int n_rows) {
   const size_t per = score_norm_smem(n_rows) + sizeof(SlabInfo) * DUSTIN_MAX_SRH + 1024;
   const int by_smem = int((size_t(228) * 1024) / per);
-  const int by_threads = 2048 / kNormThreads;
+  const int by_threads = 2048 / kNormBlock;
   const int n = by_smem < by_threads ? by_smem : by_threads;
   return n > 0 ? n : 1;
 }
@@ -581,7 +593,7 @@ cudaError_t score_norm_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStr
   if (attr != cudaSuccess) return attr;
   int ctas = 0;
   for (int g = 0; g < a.n_groups; ++g) ctas += a.ng[g].nb * a.ng[g].cps;
-  return launch_pdl(score_norm_kernel, dim3(ctas), dim3(kNormThreads), pl.norm_smem, stream, a);
+  return launch_pdl(score_norm_kernel, dim3(ctas), dim3(kNormBlock), pl.norm_smem, stream, a);
 }
 
 }  // namespace dustin
