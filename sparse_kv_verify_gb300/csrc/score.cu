@@ -400,6 +400,8 @@ constexpr int kNormWarps = kNormThreads / 32;              // compute warps
 constexpr int kNormBlock = kNormThreads + 32;              // plus the producer warp
 
 __global__ void __launch_bounds__(kNormBlock, 2) score_norm_kernel(const __grid_constant__ ScoreArgs A) {
+  // (the slab table is the only static shared memory; ptxas rounds it up to
+  // whole KB, and the dynamic array starts after it)
   extern __shared__ __align__(128) unsigned char nsm[];
   __shared__ SlabInfo si[DUSTIN_MAX_SRH];
   const int nr = A.n_rows, n0 = A.n_rows0, ns = A.n_slab;
