@@ -89,6 +89,7 @@ struct VerifyCombineArgs {
 
 struct VerifyLaunch {
   int D, NST;
+  int cps;               // CTAs per SM (1 or 2)
   VLay lay;
   int ctx_tiles, tiles_u, grid, max_seg;
   long long units, total, slot_floats;

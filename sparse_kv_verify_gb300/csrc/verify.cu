@@ -63,10 +63,15 @@ constexpr int kSCol = 0;         // S buffers: columns [0, 64) and [64, 128)
 constexpr int kPCol = 128;       // P buffers (bf16 pairs): [128, 160) and [160, 192)
 static_assert(TK == DUSTIN_MAX_BLOCK, "the draft block must fit one tile");
 
-template <int D>
+// Tensor-memory columns per CTA.  With one CTA per SM the P buffers sit at
+// kPCol and O after them; with two CTAs per SM (256 columns each) P is stored
+// over the S buffer it was computed from, and O follows the S buffers.
+template <int D, int CPS>
 struct TmemCfg {
-  static constexpr int cols = D == 128 ? 512 : 256;
-  static constexpr int o_col = D == 128 ? 256 : 192;
+  static constexpr int cols = CPS == 2 ? 256 : (D == 128 ? 512 : 256);
+  static constexpr int o_col = CPS == 2 ? 128 : (D == 128 ? 256 : 192);
+  static constexpr int p_col = CPS == 2 ? kSCol : kPCol;     // P buffer 0
+  static constexpr int p_stride = CPS == 2 ? TK : TK / 2;    // columns from P buffer 0 to 1
 };
 
 // ---- tcgen05 ---------------------------------------------------------------
@@ -255,42 +260,50 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, int* 
 
 // Shared-memory layout (bytes from the 1024-aligned base), fixed per launch
 // by the head dimension D and the query rows NQ:
-//   two query buffers [NP panels][q_rows rows][128 B] (q_rows = NQ rounded up
-//   to 8; the next segment's rows load while this one runs), then as many
-//   K/V stages [K panels | V panels] of 64 keys as the rest holds, then the
-//   valid-key masks, the mbarriers and two words (tensor-memory base, abort).
+//   query buffers [NP panels][q_rows rows][128 B] (q_rows = NQ rounded up
+//   to 8; with two buffers the next segment's rows load while this one runs,
+//   with one (two CTAs per SM) they wait for its last MMAs), then the K/V
+//   stages [K panels | V panels] of 64 keys, then the valid-key masks, the
+//   mbarriers and two words (tensor-memory base, abort).
 // Once any wait gives up (DUSTIN_DEV_TIMEOUT) every role stops issuing copies
 // and MMAs; before the CTA exits the loaders still wait for their copies in
 // flight and the MMA thread for its MMAs, so tensor memory is freed idle.
 // The S MMA reads 128 query rows per panel; the rows past q_rows fall on the
 // next buffer or the ring (whatever they hold only reaches S and O rows that
 // are never used: the softmax treats rows >= NQ as empty).
-constexpr int NQB = 2;
+template <int CPS>
+struct QBufsOf {
+  static constexpr int n = CPS == 2 ? 1 : 2;
+};
 constexpr uint32_t kVerifySmem = 227 * 1024;
+constexpr uint32_t kSmemPerSm = 228 * 1024;   // shared memory of an SM (1 KB reserved per CTA)
 
-// K/V stages per head dimension (compile-time: the stage and phase of tile
-// gi are gi % n and gi / n on the hot paths).  More than five 32 KB stages
-// measured no faster at d = 128 (the MMA issue rate bounds a tile, not the
-// bytes in flight) and slower for contiguous rows.
-template <int D>
+// K/V stages per head dimension and CTAs per SM (compile-time: the stage and
+// phase of tile gi are gi % n and gi / n on the hot paths).  More than five
+// 32 KB stages measured no faster at d = 128 with one CTA per SM (the MMA
+// issue rate bounds a tile, not the bytes in flight) and slower for
+// contiguous rows; two CTAs per SM hold three (d = 128) or six (d = 64) each.
+template <int D, int CPS>
 struct StagesOf {
-  static constexpr int n = D == 128 ? 5 : 8;
+  static constexpr int n = CPS == 2 ? (D == 128 ? 3 : 6) : (D == 128 ? 5 : 8);
 };
 
-inline VLay make_lay(int D, int NQ) {
+inline VLay make_lay(int D, int NQ, int cps) {
   VLay L{};
   L.NP = D / 64;
+  const int nqb = cps == 2 ? QBufsOf<2>::n : QBufsOf<1>::n;
   const int q_rows = NQ < 8 ? 8 : (NQ + 7) & ~7;
   L.q_panel = uint32_t(q_rows) * 128;
   L.q_buf = uint32_t(L.NP) * L.q_panel;
-  L.ring_off = (NQB * L.q_buf + 1023u) & ~1023u;
+  L.ring_off = (uint32_t(nqb) * L.q_buf + 1023u) & ~1023u;
   L.kv_panel = uint32_t(TK) * 128;
   L.half_bytes = uint32_t(L.NP) * L.kv_panel;
   L.stage_bytes = 2 * L.half_bytes;
-  L.nst = D == 128 ? StagesOf<128>::n : StagesOf<64>::n;
+  L.nst = cps == 2 ? (D == 128 ? StagesOf<128, 2>::n : StagesOf<64, 2>::n)
+                   : (D == 128 ? StagesOf<128, 1>::n : StagesOf<64, 1>::n);
   L.mask_off = L.ring_off + uint32_t(L.nst) * L.stage_bytes;
   L.bar_off = L.mask_off + ((uint32_t(L.nst) * kLoaders + 7u) & ~7u);
-  L.misc_off = L.bar_off + uint32_t(2 * L.nst + 4 + 2 * NQB + 2) * 8;
+  L.misc_off = L.bar_off + uint32_t(2 * L.nst + 4 + 2 * nqb + 2) * 8;
   L.total = L.misc_off + 16 + 1024;
   return L;
 }
@@ -317,12 +330,16 @@ __device__ __forceinline__ Seg next_seg(long long& t, long long t1, int tiles_u)
 
 // M: rows of the S and P V MMAs, 64 when the query rows fit (they then spread
 // over the four lane quarters, 16 each), else 128 (one row per lane).
-template <int D, int M>
-__global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ VerifyArgs A) {
+// CPS: CTAs resident per SM (2 only with M = 64: 72 registers a thread, 256
+// tensor-memory columns, one query buffer and fewer stages each).
+template <int D, int M, int CPS>
+__global__ void __launch_bounds__(NTH, CPS) verify_kernel(const __grid_constant__ VerifyArgs A) {
   static_assert(M == 64 || M == 128, "MMA rows");
-  using Tm = TmemCfg<D>;
+  static_assert(CPS == 1 || (CPS == 2 && M == 64), "two CTAs per SM only with 64-row MMAs");
+  using Tm = TmemCfg<D, CPS>;
   const VLay& Ly = A.lay;
-  constexpr int NSTAGE = StagesOf<D>::n;   // == A.lay.nst
+  constexpr int NSTAGE = StagesOf<D, CPS>::n;   // == A.lay.nst
+  constexpr int NQB = QBufsOf<CPS>::n;          // query buffers
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -547,7 +564,8 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
   } else if (warp == kMmaWarp) {
     // ================================================================ S MMAs
     // S = Q K^T of tile g into S buffer g % 2, once its rows have landed and
-    // the softmax has read that buffer's previous tile (g - 2)
+    // the softmax has read that buffer's previous tile (g - 2); with P stored
+    // over S, once P V of tile g - 2 has read that P
     if (lane == 0) {
       constexpr uint32_t kIdS = tc_idesc(M, TK, 0);
       int gi = 0;
@@ -561,7 +579,10 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
         if (!mbar_wait(&q_full[qb], uint32_t(s / NQB) & 1u, A.err, abort_flag)) break;
         for (int i = 0; i < sg.n; ++i, ++gi) {
           const int st = int(gi % NSTAGE);
-          if ((gi >= 2 && !mbar_wait(&p_full[gi & 1], uint32_t((gi >> 1) - 1) & 1u, A.err, abort_flag)) ||
+          if ((gi >= 2 && !(CPS == 2 ? mbar_wait(&empty[(gi - 2) % NSTAGE], uint32_t((gi - 2) / NSTAGE) & 1u,
+                                                   A.err, abort_flag)
+                                     : mbar_wait(&p_full[gi & 1], uint32_t((gi >> 1) - 1) & 1u, A.err,
+                                                 abort_flag))) ||
               !mbar_wait(&full[st], uint32_t(gi / NSTAGE) & 1u, A.err, abort_flag)) {
             live = false;
             break;
@@ -611,7 +632,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
           const int st = int(gi % NSTAGE);
           const uint32_t vst =
               sbase + uint32_t(Ly.ring_off + size_t(st) * Ly.stage_bytes + Ly.half_bytes);
-          const uint32_t p_tmem = tmem + uint32_t(kPCol + (gi & 1) * (TK / 2));
+          const uint32_t p_tmem = tmem + uint32_t(Tm::p_col + (gi & 1) * Tm::p_stride);
 #pragma unroll
           for (int kk = 0; kk < TK / 16; ++kk) {
             const uint64_t bd = tc_desc(vst + uint32_t(kk * 2048), uint32_t(Ly.kv_panel), 1024);
@@ -743,14 +764,15 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
               tc_st16x256_x4(o_lane + uint32_t(c), o);
             }
           }
-          // P buffer gi % 2 is free once P V of tile gi - 2 has completed
-          if (gi >= 2 && !__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 2) % NSTAGE],
-                                                           uint32_t((gi - 2) / NSTAGE) & 1u, A.err,
-                                                           abort_flag))) {
+          // P buffer gi % 2 is free once P V of tile gi - 2 has completed (when
+          // P is stored over S, S of tile gi was issued only after that)
+          if (CPS == 1 && gi >= 2 &&
+              !__all_sync(0xffffffffu, mbar_wait(&empty[(gi - 2) % NSTAGE], uint32_t((gi - 2) / NSTAGE) & 1u,
+                                                 A.err, abort_flag))) {
             live = false;
             break;
           }
-          tc_st16x128_x8(lane_base + uint32_t(kPCol + (gi & 1) * (TK / 2)), pk);
+          tc_st16x128_x8(lane_base + uint32_t(Tm::p_col + (gi & 1) * Tm::p_stride), pk);
           tc_fence_before();
           mbar_arrive(&p_full[gi & 1]);
         }
@@ -901,7 +923,7 @@ __global__ void __launch_bounds__(NTH, 1) verify_kernel(const __grid_constant__ 
             live = false;
             break;
           }
-          tc_st32(lane_base + uint32_t(kPCol + (gi & 1) * (TK / 2)), pk);
+          tc_st32(lane_base + uint32_t(Tm::p_col + (gi & 1) * Tm::p_stride), pk);
           tc_fence_before();
           mbar_arrive(&p_full[gi & 1]);
         }
@@ -1035,19 +1057,27 @@ __global__ void __launch_bounds__(kCombineThreads) verify_combine_kernel(const _
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
-template <int D, int M>
+template <int D, int M, int CPS>
 cudaError_t launch_main(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t stream) {
-  auto kern = verify_kernel<D, M>;
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kVerifySmem));
+  auto kern = verify_kernel<D, M, CPS>;
+  static const cudaError_t attr = [&] {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kVerifySmem));
+    if (e == cudaSuccess && CPS > 1)   // room for CPS CTAs' shared memory
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               int(cudaSharedmemCarveoutMaxShared));
+    return e;
+  }();
   if (attr != cudaSuccess) return attr;
   return launch_pdl(kern, dim3(pl.grid), dim3(NTH), pl.smem, stream, a);
 }
 
 template <int D>
 cudaError_t launch_t(const VerifyArgs& a, const VerifyLaunch& pl, cudaStream_t stream) {
-  // 64-row MMAs while the query rows fit them (NQ <= 64)
-  cudaError_t e = a.NQ <= 64 ? launch_main<D, 64>(a, pl, stream) : launch_main<D, 128>(a, pl, stream);
+  // 64-row MMAs while the query rows fit them (NQ <= 64), two CTAs per SM
+  // when the plan found room for them
+  cudaError_t e = pl.cps == 2  ? launch_main<D, 64, 2>(a, pl, stream)
+                  : a.NQ <= 64 ? launch_main<D, 64, 1>(a, pl, stream)
+                               : launch_main<D, 128, 1>(a, pl, stream);
   if (e != cudaSuccess) return e;
   VerifyCombineArgs c;
   c.NQ = a.NQ;
@@ -1074,15 +1104,19 @@ VerifyLaunch verify_plan(int D, int NQ, int nkeys_cap, int B, int hkv, int n_lay
   (void)dense;
   VerifyLaunch pl{};
   pl.D = D;
-  const VLay lay = make_lay(D, NQ);
+  // two CTAs per SM when the query rows fit 64-row MMAs and two CTAs' shared
+  // memory fits an SM
+  const VLay lay2 = make_lay(D, NQ, 2);
+  pl.cps = (NQ <= 64 && 2 * (size_t(lay2.total) + 1024) <= kSmemPerSm) ? 2 : 1;
+  const VLay lay = pl.cps == 2 ? lay2 : make_lay(D, NQ, 1);
   pl.lay = lay;
   pl.NST = lay.nst;
   pl.ctx_tiles = (nkeys_cap + TK - 1) / TK;
   pl.tiles_u = pl.ctx_tiles + 1;
   pl.units = (long long)B * hkv * n_layers;
   pl.total = pl.units * pl.tiles_u;
-  // persistent: one CTA per SM (the shared memory holds one)
-  long long grid = num_sms > 0 ? num_sms : 148;
+  // persistent: cps CTAs per SM
+  long long grid = (long long)pl.cps * (num_sms > 0 ? num_sms : 148);
   if (grid > kVerifyGridMax) grid = kVerifyGridMax;
   if (grid > pl.total) grid = pl.total;
   pl.grid = int(grid);

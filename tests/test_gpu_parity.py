@@ -277,9 +277,10 @@ def test_verify_full_budget_matches_dense():
 
 def test_verify_many_segments_per_cta():
     """Short units (two tiles) and many of them: every CTA of the stream-K
-    split runs several units in turn and reloads both query buffers; the
-    kernels end cleanly (no wait gives up) and match the oracle."""
-    wl = WORKLOADS["tiny"].with_(B=32, Hq=16, Hkv=8, L=512, k=64, sinks=4, window=16, m=16,
+    split runs several units in turn and reloads its query buffers; the
+    kernels end cleanly (no wait gives up) and match the oracle.  (80
+    sequences keep three or more units per CTA with two CTAs per SM.)"""
+    wl = WORKLOADS["tiny"].with_(B=80, Hq=16, Hkv=8, L=512, k=64, sinks=4, window=16, m=16,
                                  n_planted=4)
     c = Case(wl)
     x = c.x
