@@ -237,6 +237,22 @@ def test_verify_query_rows_near_mma_width(gamma, hq, hkv, d):
     assert_attention(od, c.oracle_dense())
 
 
+@pytest.mark.parametrize("gamma,hq,hkv,d,per_sm", [(5, 64, 8, 128, 2), (12, 24, 8, 128, 2),
+                                                    (7, 64, 8, 128, 1), (20, 3, 1, 64, 2),
+                                                    (21, 3, 1, 64, 1)])
+def test_verify_ctas_per_sm(gamma, hq, hkv, d, per_sm):
+    """Two verification CTAs per SM while the query rows fit 64-row MMAs and
+    two CTAs' shared memory fits an SM (48 and 39 rows at d = 128, 63 at
+    d = 64); one beyond (64 rows at d = 128: a query buffer and three stages
+    no longer fit twice; 66 rows: 128-row MMAs need 512 tensor-memory
+    columns).  The parity tests above run each of these shapes."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = dk.Params(B=16, Lcap=32768, gamma=gamma, sinks=16, window=256, m=512, k=2048)
+    grid, tiles = dk.verify_split(p, hq, hkv, d, 1, False)
+    assert tiles == 2048 // 64 + 1
+    assert grid == per_sm * sms
+
+
 @pytest.mark.parametrize("d,hq,hkv", [(64, 2, 1), (128, 16, 8)])
 def test_verify_largest_draft_block(d, hq, hkv):
     """gamma + 1 = 64 draft-block rows (one whole block tile under the causal
