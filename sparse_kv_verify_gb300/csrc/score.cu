@@ -562,11 +562,31 @@ size_t score_norm_smem(int n_rows) {
   return size_t(2) * nb * kNormThreads * 4 + size_t(2 * n_rows) * 4 + 4 * 8 + 16;
 }
 
+// Shared-memory limit and carveout of the normalise kernel, set once: the
+// largest layout, and all of the SM's unified memory as shared memory so that
+// as many CTAs are resident as their shared memory allows.
+static cudaError_t score_norm_attrs() {
+  static const cudaError_t e = [] {
+    cudaError_t r = cudaFuncSetAttribute(score_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(score_norm_smem(DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS)));
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(score_norm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               int(cudaSharedmemCarveoutMaxShared));
+    return r;
+  }();
+  return e;
+}
+
 int score_norm_ctas_per_sm(int n_rows) {
-  const size_t per = score_norm_smem(n_rows) + sizeof(SlabInfo) * DUSTIN_MAX_SRH + 1024;
-  const int by_smem = int((size_t(228) * 1024) / per);
-  const int by_threads = 2048 / kNormBlock;
-  const int n = by_smem < by_threads ? by_smem : by_threads;
+  // as the occupancy calculator counts them: registers, static and dynamic
+  // shared memory, the carveout (a grid sized from the dynamic shared memory
+  // alone can ask for more CTAs than fit, and the rest then run as a second
+  // wave)
+  int n = 0;
+  if (score_norm_attrs() != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_norm_kernel, kNormBlock, score_norm_smem(n_rows)) !=
+          cudaSuccess)
+    return 1;
   return n > 0 ? n : 1;
 }
 
@@ -590,8 +610,7 @@ cudaError_t score_stream_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaS
 }
 
 cudaError_t score_norm_launch(const ScoreArgs& a, const ScoreLaunch& pl, cudaStream_t stream) {
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      score_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(score_norm_smem(DUSTIN_MAX_SRH * DUSTIN_MAX_PAIRS)));
+  const cudaError_t attr = score_norm_attrs();
   if (attr != cudaSuccess) return attr;
   int ctas = 0;
   for (int g = 0; g < a.n_groups; ++g) ctas += a.ng[g].nb * a.ng[g].cps;
