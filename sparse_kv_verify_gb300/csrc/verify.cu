@@ -8,23 +8,27 @@
 // draft-block rows under the causal mask u <= t.
 //
 // Schedule (stream-K): each unit is cut into 64-key tiles followed by one
-// block tile; all units' tiles form one sequence that is split evenly over one
-// persistent CTA per SM, so every CTA moves the same number of bytes whatever
-// B, Hkv and k are.
+// block tile; all units' tiles form one sequence that is split evenly over the
+// persistent CTAs (two per SM when the query rows fit 64-row MMAs and two
+// CTAs' shared memory fits an SM, else one), so every CTA moves the same
+// number of bytes whatever B, Hkv and k are.  Two CTAs per SM gather faster
+// than one: each drains its ring in order, and two rings cover each other's
+// late rows.
 //
 // Roles inside a CTA (warp specialised, handing over through mbarriers):
 //   warps 4-11       loaders: warp w copies keys [8 (w-4), 8 (w-4) + 8) of
 //   (loaders)        every tile, K and V rows, with 16-byte cp.async straight
 //                    into the 128-byte-swizzled K-major layout the MMA reads
 //                    (rows the tile does not use are zero-filled) through a
-//                    ring of five 32 KB stages (eight 16 KB ones for d = 64);
+//                    ring of five 32 KB stages (eight 16 KB ones for d = 64;
+//                    three and six with two CTAs per SM);
 //                    each copy's completion arrives on the stage's barrier
 //                    (cp.async.mbarrier.arrive).  A dense tile that lies wholly
 //                    inside the cache comes instead as tiled TMA loads (a K
 //                    and a V box of 64 rows x 64 columns per 64-column panel)
 //                    issued by one loader thread.  A
 //                    segment's query rows come with one tiled TMA load into one
-//                    of two query buffers;
+//                    of two query buffers (one with two CTAs per SM);
 //   warp 12 (S)      one thread issues S = Q K^T of each tile into one of two S
 //                    buffers in tensor memory as soon as its rows have landed
 //                    (after a proxy fence, since cp.async rows were written
@@ -39,7 +43,9 @@
 //                    when a tile passes it by more than 2^8 (so O is rarely
 //                    rescaled), P rounded to bf16 and stored back to tensor
 //                    memory once the P V MMA two tiles back has read that P
-//                    buffer; then the epilogue.
+//                    buffer (with two CTAs per SM, P overwrites the S buffer it
+//                    came from, and the S thread waits for that P V instead);
+//                    then the epilogue.
 //
 // Merge: a segment that covers a whole unit writes O directly; otherwise it
 // writes (row max, row sum, unnormalised O) to the workspace, and a second,
