@@ -254,8 +254,10 @@ int dustin_step_launches(const dustin_step* s, int32_t* n_launches, int32_t* gro
  * u = (l * B + b) * hkv + g, each of *tiles_per_unit tiles of 64 keys (the
  * context tiles, then one draft-block tile); the T = units * tiles_per_unit
  * tiles are cut among *grid CTAs, CTA c taking tiles [c*T/grid,
- * (c+1)*T/grid).  A unit whose tiles fall to several CTAs is merged by the
- * second verification kernel.  DUSTIN_EINVAL / DUSTIN_ERANGE as the
+ * (c+1)*T/grid).  The grid is two CTAs per SM when (gamma+1)*hq/hkv <= 64
+ * and two CTAs' shared-memory layouts fit an SM, else one (at most T).  A
+ * unit whose tiles fall to several CTAs is merged by the second verification
+ * kernel.  DUSTIN_EINVAL / DUSTIN_ERANGE as the
  * verification calls would return for the shape. */
 int dustin_verify_split(const dustin_params* p, int32_t hq, int32_t hkv, int32_t d,
                         int32_t n_layers, int32_t dense, int32_t* grid, int32_t* tiles_per_unit);
