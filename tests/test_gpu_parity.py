@@ -413,6 +413,30 @@ def test_kv_append_and_overflow_flag():
         assert np.array_equal(to_bits(x.K[l])[2], before[l][0][2])
 
 
+def test_kv_append_twice_in_a_row():
+    """Two appends back to back on one stream, nothing in between: the second
+    copies at the seq_len the first one left, in every sequence and layer
+    (gamma + 1 = 5 rows at most per call)."""
+    wl = WORKLOADS["tiny"].with_(B=3, n_layers=2)
+    c = Case(wl, seq_len=[1000, 1010, 900])
+    x = c.x
+    before = [(to_bits(k).copy(), to_bits(v).copy()) for k, v in zip(x.K, x.V)]
+    n1, n2 = [3, 0, 5], [1, 4, 0]
+    ws = dk.workspace(c.p)
+    for n in (n1, n2):
+        dk.dustin_kv_append(c.p, x.K, x.V, x.Kb, x.Vb, torch.tensor(n, dtype=torch.int32, device="cuda"),
+                            c.seq, ws=ws)
+    assert dk.check(ws) == 0
+    assert c.seq.cpu().tolist() == [1004, 1014, 905]
+    for l in range(2):
+        kb, vb = to_bits(x.Kb[l]), to_bits(x.Vb[l])
+        K1, V1, s1 = O.kv_append(before[l][0], before[l][1], kb, vb, n1, [1000, 1010, 900])
+        K2, V2, s2 = O.kv_append(K1, V1, kb, vb, n2, s1)
+        assert s2.tolist() == [1004, 1014, 905]
+        assert np.array_equal(to_bits(x.K[l]), K2)
+        assert np.array_equal(to_bits(x.V[l]), V2)
+
+
 # ------------------------------------------------------------------ fused step
 
 
