@@ -215,13 +215,14 @@ def test_verify_gamma_range(gamma):
     assert_attention(od, c.oracle_dense())
 
 
-@pytest.mark.parametrize("gamma,hq,hkv,d", [(12, 24, 8, 128), (7, 64, 8, 128), (20, 3, 1, 64),
-                                             (21, 3, 1, 64)])
+@pytest.mark.parametrize("gamma,hq,hkv,d", [(12, 24, 8, 128), (6, 64, 8, 128), (18, 24, 8, 128),
+                                             (7, 64, 8, 128), (20, 3, 1, 64), (21, 3, 1, 64)])
 def test_verify_query_rows_near_mma_width(gamma, hq, hkv, d):
-    """(gamma + 1) * Hq / Hkv query rows of 39, 64, 63 and 66: up to 64 the
-    verification MMAs are 64 rows wide (16 rows in each tensor-memory lane
-    quarter, the last quarter partly or wholly in use), beyond it 128 rows
-    wide; row counts that are not multiples of 8 included."""
+    """(gamma + 1) * Hq / Hkv query rows of 39, 56, 57, 64, 63 and 66: up to
+    64 the verification MMAs are 64 rows wide (16 rows in each tensor-memory
+    lane quarter, the last quarter partly or wholly in use), beyond it 128
+    rows wide; at d = 128 two CTAs share an SM up to 56 rows and one runs
+    alone from 57; row counts that are not multiples of 8 included."""
     wl = WORKLOADS["tiny"].with_(gamma=gamma, Hq=hq, Hkv=hkv, d=d, L=1024, k=256, sinks=4,
                                  window=64, m=64)
     c = Case(wl)
@@ -238,14 +239,15 @@ def test_verify_query_rows_near_mma_width(gamma, hq, hkv, d):
 
 
 @pytest.mark.parametrize("gamma,hq,hkv,d,per_sm", [(5, 64, 8, 128, 2), (12, 24, 8, 128, 2),
+                                                    (6, 64, 8, 128, 2), (18, 24, 8, 128, 1),
                                                     (7, 64, 8, 128, 1), (20, 3, 1, 64, 2),
                                                     (21, 3, 1, 64, 1)])
 def test_verify_ctas_per_sm(gamma, hq, hkv, d, per_sm):
     """Two verification CTAs per SM while the query rows fit 64-row MMAs and
-    two CTAs' shared memory fits an SM (48 and 39 rows at d = 128, 63 at
-    d = 64); one beyond (64 rows at d = 128: a query buffer and three stages
-    no longer fit twice; 66 rows: 128-row MMAs need 512 tensor-memory
-    columns).  The parity tests above run each of these shapes."""
+    two CTAs' shared memory fits an SM (48, 39 and 56 rows at d = 128, 63 at
+    d = 64); one beyond (57 and 64 rows at d = 128: a query buffer and three
+    stages no longer fit twice; 66 rows: 128-row MMAs need 512 tensor-memory
+    columns).  The parity tests above run the boundary shapes."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     p = dk.Params(B=16, Lcap=32768, gamma=gamma, sinks=16, window=256, m=512, k=2048)
     grid, tiles = dk.verify_split(p, hq, hkv, d, 1, False)
