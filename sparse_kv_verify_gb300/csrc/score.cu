@@ -581,13 +581,20 @@ int score_norm_ctas_per_sm(int n_rows) {
   // as the occupancy calculator counts them: registers, static and dynamic
   // shared memory, the carveout (a grid sized from the dynamic shared memory
   // alone can ask for more CTAs than fit, and the rest then run as a second
-  // wave)
+  // wave); the last answer per calling thread is kept (device, rows)
+  static thread_local int last_dev = -1, last_rows = -1, last_n = 1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev == last_dev && n_rows == last_rows) return last_n;
   int n = 0;
   if (score_norm_attrs() != cudaSuccess ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_norm_kernel, kNormBlock, score_norm_smem(n_rows)) !=
           cudaSuccess)
     return 1;
-  return n > 0 ? n : 1;
+  last_dev = dev;
+  last_rows = n_rows;
+  last_n = n > 0 ? n : 1;
+  return last_n;
 }
 
 int score_rows_per_tile(int D) { return D == 128 ? kBoxRows : 2 * kBoxRows; }
