@@ -69,7 +69,7 @@ constexpr int kBins1 = kSelectBins;   // top 12 bits
 constexpr int kBins2 = 1024;          // 10 bits per refinement pass
 constexpr int kListCap = 128;         // entries per warp list and channel (scan)
 constexpr int kCandCap = 4096;        // candidates of the general path
-constexpr int kFinCap = 6144;         // list entries of both channels gathered by rank 0
+constexpr int kFinCap = 7424;         // list entries of both channels gathered by rank 0
 constexpr int kBatch = 8;             // rows of 32 keys loaded before use (general path)
 constexpr int kHistThreads = 1024;    // select_hist_kernel: positions per CTA
 constexpr int kCells = kMaxSelectCtas * kWarps;   // (rank, warp) lists per channel
